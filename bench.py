@@ -1,0 +1,598 @@
+"""Benchmark: achieved HBM GB/s of the fused QK-Norm + RoPE + FP8 prologue on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-extras]
+
+A step is one launch of the whole hot path (load -> sum of squares -> normalise -> NeoX RoPE ->
+amax/scale -> e4m3 codes -> store) over one batch of the prologue workload: 4096 tokens x (32 q + 8
+kv heads) x head_dim 128, bf16 in, fp32 cos/sin tables, e4m3 + fp32 scale out. The throughput is
+the ideal byte ledger per step (every input read once, every output written once, tables and
+weights once) divided by the step time.
+
+Timing: 8 rotating input/output sets (8 x 65.7 MB > the 129 MB L2), launches captured in CUDA
+graphs and replayed, CUDA events on the launching stream, a barrier + synchronize on both sides,
+max over ranks. N > 1 (torchrun, one process per GPU): every rank runs its own batch (weak
+scaling, no data-path collective; the process group only carries the barrier and the max).
+
+--impl reference times the oracle (plain single-threaded C++) on this machine's host cores over
+bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s (and % of ~8 TB/s) for fused QK-norm+RoPE+FP8, 1 GB300"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+T_TOK, HQ, HK, D = 4096, 32, 8, 128
+WORKLOAD = "qk_norm_rope_quant T=4096 Hq=32 Hk=8 D=128 rope_dim=128 bf16->e4m3 fp32-tables"
+KERNEL_SOURCES = ["fp8_quant_memory_gb300/csrc/fq_rows.cu", "fp8_quant_memory_gb300/csrc/fq_device.cuh"]
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "qk_norm_rope_quant_4k.md")
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel."""
+    try:
+        with open(PROFILE_SUMMARY) as f:
+            text = f.read()
+    except OSError:
+        return None
+    m = re.search(r"kernel_source_sha256:\s*([0-9a-f]+)", text)
+    t = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if not (m and t) or m.group(1) != kernel_source_hash():
+        return None
+    return int(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 100 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r for r in csv.reader(io.StringIO(out)) if len(r) >= 9]
+        sm = [float(r[1]) for r in rows if r[1].strip().replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].strip().replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, val in zip(names, r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------------------------------------ cases
+class Case:
+    """One workload: rotating device buffer sets, a launch per set, and the ideal bytes per launch."""
+
+    name = ""
+    kernels_per_step = 1
+
+    def bytes_per_step(self) -> int:
+        raise NotImplementedError
+
+    def launch(self, i: int):
+        raise NotImplementedError
+
+
+def _make_sets(host: dict, n_sets: int, dev):
+    import torch
+
+    sets = []
+    for _ in range(n_sets):
+        sets.append({k: (v.to(dev).clone() if isinstance(v, torch.Tensor) else v) for k, v in host.items()})
+    return sets
+
+
+class PrologueCase(Case):
+    def __init__(self, dev, T=T_TOK, Hq=HQ, Hk=HK, D_=D, std=2.0, theta=1e4, positions="arange",
+                 outlier_frac=0.0, n_sets=8, seed=20261202 + 2):
+        import torch
+
+        import fp8_quant_memory_gb300 as fq
+        from fp8_quant_memory_gb300 import ledger
+        from fp8_quant_memory_gb300 import workloads as wl
+
+        self.fq = fq
+        self.T, self.Hq, self.Hk, self.D = T, Hq, Hk, D_
+        self.name = f"qk_norm_rope_quant T={T} Hq={Hq} Hk={Hk} D={D_}"
+        self.host = wl.qk_inputs(T, Hq, Hk, D_, "bf16", "fp32", seed=seed, std=std, theta=theta,
+                                 positions=positions, outlier_frac=outlier_frac)
+        self.sets = _make_sets({k: self.host[k] for k in ("qk", "wq", "wk", "cos", "sin")}, n_sets, dev)
+        for s in self.sets:
+            s["q"] = torch.empty((T, Hq + Hk, D_), dtype=torch.uint8, device=dev)
+            s["scale"] = torch.empty((T, Hq + Hk), dtype=torch.float32, device=dev)
+        self._bytes = ledger.qk_prologue_bytes(T, Hq, Hk, D_)
+
+    def bytes_per_step(self):
+        return self._bytes
+
+    def launch(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.fq.qk_norm_rope_quant(s["qk"], s["wq"], s["wk"], s["cos"], s["sin"], self.Hq, self.Hk,
+                                   q_out=s["q"], scale=s["scale"])
+
+
+class RmsnormFwdCase(Case):
+    def __init__(self, dev, M=8192, N=4096, n_sets=3):
+        import torch
+
+        import fp8_quant_memory_gb300 as fq
+        from fp8_quant_memory_gb300 import ledger
+        from fp8_quant_memory_gb300 import workloads as wl
+
+        self.fq = fq
+        self.name = f"rmsnorm_fwd M={M} N={N} bf16"
+        h = wl.rmsnorm_inputs(M, N, "bf16", seed=20261202 + 1)
+        self.sets = _make_sets({"x": h["x"], "w": h["w"]}, n_sets, dev)
+        for s in self.sets:
+            s["y"] = torch.empty_like(s["x"])
+        self._bytes = ledger.rmsnorm_fwd_bytes(M, N)
+
+    def bytes_per_step(self):
+        return self._bytes
+
+    def launch(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.fq.rmsnorm_fwd(s["x"], s["w"], out=s["y"])
+
+
+class RmsnormBwdCase(Case):
+    kernels_per_step = 2
+
+    def __init__(self, dev, M=8192, N=4096, n_sets=2):
+        import torch
+
+        import fp8_quant_memory_gb300 as fq
+        from fp8_quant_memory_gb300 import ledger
+        from fp8_quant_memory_gb300 import workloads as wl
+
+        self.fq = fq
+        self.name = f"rmsnorm_bwd M={M} N={N} bf16 (dx + deterministic dw)"
+        h = wl.rmsnorm_inputs(M, N, "bf16", seed=20261202 + 1)
+        self.sets = _make_sets({"x": h["x"], "w": h["w"], "g": h["g"]}, n_sets, dev)
+        nbytes = fq.rmsnorm_bwd_workspace_bytes(M, N)
+        for s in self.sets:
+            s["ws"] = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
+        self._bytes = ledger.rmsnorm_bwd_bytes(M, N)
+        self.workspace_bytes = nbytes
+
+    def bytes_per_step(self):
+        return self._bytes
+
+    def launch(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.fq.rmsnorm_bwd(s["x"], s["w"], s["g"], workspace=s["ws"], want_dw_f32=False)
+
+
+class RopeCase(Case):
+    def __init__(self, dev, M=65536, N=192, R=64, n_sets=8):
+        import torch
+
+        import fp8_quant_memory_gb300 as fq
+        from fp8_quant_memory_gb300 import ledger
+        from fp8_quant_memory_gb300 import workloads as wl
+
+        self.fq = fq
+        self.name = f"rmsnorm_rope M={M} N={N} R={R} fp16"
+        h = wl.rows_inputs(M, N, R, "fp16", "fp16", seed=20261202 + 3, heads_per_token=32)
+        self.sets = _make_sets(h, n_sets, dev)
+        for s in self.sets:
+            s["y"] = torch.empty_like(s["x"])
+        self._bytes = ledger.rope_bytes(M, N, R, "fp16", "fp16")
+
+    def bytes_per_step(self):
+        return self._bytes
+
+    def launch(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.fq.rmsnorm_rope(s["x"], s["w"], s["cos"], s["sin"], out=s["y"])
+
+
+class RopeQuantTinyCase(Case):
+    def __init__(self, dev, M=256, N=512, R=64, n_sets=8):
+        import fp8_quant_memory_gb300 as fq
+        from fp8_quant_memory_gb300 import ledger
+        from fp8_quant_memory_gb300 import workloads as wl
+
+        import torch
+
+        self.fq = fq
+        self.name = f"rmsnorm_rope_quant M={M} N={N} R={R} bf16 (launch-bound)"
+        h = wl.rows_inputs(M, N, R, "bf16", "bf16", seed=20261202)
+        self.sets = _make_sets(h, n_sets, dev)
+        for s in self.sets:
+            s["y"] = torch.empty_like(s["x"])
+            s["q"] = torch.empty((M, N), dtype=torch.uint8, device=dev)
+            s["scale"] = torch.empty((M,), dtype=torch.float32, device=dev)
+        self._bytes = ledger.rope_quant_bytes(M, N, R, "bf16", "bf16", write_y=True)
+
+    def bytes_per_step(self):
+        return self._bytes
+
+    def launch(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.fq.rmsnorm_rope_quant(s["x"], s["w"], s["cos"], s["sin"], y=s["y"], q=s["q"], scale=s["scale"])
+
+
+class TorchEagerPrologueCase(Case):
+    """Unfused per-op PyTorch sequence for the same prologue (RMSNorm -> RoPE -> amax -> divide ->
+    cast), the comparison the Ch.13 ledger's unfused plan models. Bench-only comparator."""
+
+    def __init__(self, prologue: PrologueCase):
+        import torch
+
+        self.torch = torch
+        self.p = prologue
+        self.name = "torch eager unfused prologue (same workload)"
+        self.kernels_per_step = None
+
+    def bytes_per_step(self):
+        return self.p.bytes_per_step()
+
+    def launch(self, i):
+        torch = self.torch
+        p = self.p
+        s = p.sets[i % len(p.sets)]
+        x = s["qk"].float()
+        rstd = torch.rsqrt(x.pow(2).mean(-1, keepdim=True) + 1e-6)
+        w = torch.cat([s["wq"].float().expand(p.Hq, p.D), s["wk"].float().expand(p.Hk, p.D)])
+        n = x * rstd * w
+        half = p.D // 2
+        c = s["cos"][:, None, :]
+        sn = s["sin"][:, None, :]
+        lo, hi = n[..., :half], n[..., half:]
+        y = torch.cat([lo * c - hi * sn, hi * c + lo * sn], dim=-1)
+        amax = y.abs().amax(-1, keepdim=True).clamp(min=1e-4)
+        scale = amax / 448.0
+        s["q"].copy_((y / scale).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8))
+        s["scale"].copy_(scale.squeeze(-1))
+
+
+# ------------------------------------------------------------------------------------------------ timing
+def time_case(case: Case, steps: int, warmup: int, stream, use_graph=True, graph_len=256):
+    """Run `warmup` untimed steps then exactly `steps` timed steps; returns (ms_total, launches)."""
+    import torch
+
+    torch.cuda.synchronize()
+    graph = None
+    if use_graph:
+        case.launch(0)  # eager first call: caches occupancy queries outside capture
+        torch.cuda.synchronize()
+        n = max(1, min(graph_len, steps))
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            for i in range(n):
+                case.launch(i)
+        rem = steps % n
+        graph_rem = None
+        if rem:
+            graph_rem = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph_rem, stream=stream):
+                for i in range(rem):
+                    case.launch(i)
+        # warm-up: W steps, at least one replay of each graph (uploads the graphs)
+        done = 0
+        with torch.cuda.stream(stream):
+            graph.replay()
+            done += n
+            if graph_rem is not None:
+                graph_rem.replay()
+                done += rem
+            while done < warmup:
+                graph.replay()
+                done += n
+        warm_done = done
+    else:
+        with torch.cuda.stream(stream):
+            for i in range(warmup):
+                case.launch(i)
+        warm_done = warmup
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        if use_graph:
+            for _ in range(steps // n):
+                graph.replay()
+            if graph_rem is not None:
+                graph_rem.replay()
+        else:
+            for i in range(steps):
+                case.launch(i)
+        end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    return start.elapsed_time(end), warm_done
+
+
+_PG = None
+
+
+def barrier():
+    if _PG is not None:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v: float) -> float:
+    if _PG is None:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def e2e_prologue(case: PrologueCase, steps: int, stream):
+    """Same metric through the public API with host buffers: per step, pinned host -> device copies of
+    the step's inputs, the kernel, device -> pinned host copies of q and scale."""
+    import torch
+
+    fq = case.fq
+    s = case.sets[0]
+    host_in = {k: case.host[k].pin_memory() for k in ("qk", "wq", "wk", "cos", "sin")}
+    host_q = torch.empty(s["q"].shape, dtype=torch.uint8).pin_memory()
+    host_s = torch.empty(s["scale"].shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = host_q.numel() + host_s.numel() * 4
+
+    def step():
+        for k, t in host_in.items():
+            s[k].copy_(t, non_blocking=True)
+        fq.qk_norm_rope_quant(s["qk"], s["wq"], s["wk"], s["cos"], s["sin"], case.Hq, case.Hk,
+                              q_out=s["q"], scale=s["scale"])
+        host_q.copy_(s["q"], non_blocking=True)
+        host_s.copy_(s["scale"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(steps):
+            step()
+        end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end)
+    return {"value": round(case.bytes_per_step() * steps / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "steps": steps, "ms_per_step": round(ms / steps, 4), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+def cpu_oracle_sample(budget_s: float = 12.0):
+    """The oracle on bounded samples of the prologue workload (whole batches, repeated until the time
+    budget is spent): GB/s of the same ledger, single thread."""
+    import oracle
+    from fp8_quant_memory_gb300 import ledger
+    from fp8_quant_memory_gb300 import workloads as wl
+
+    d = wl.qk_inputs(T_TOK, HQ, HK, D, "bf16", "fp32", seed=20261202 + 2, std=2.0)
+    oracle.lib()
+    bytes_per = ledger.qk_prologue_bytes(T_TOK, HQ, HK, D)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], HQ, HK)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": round(bytes_per * reps / el / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full batches of {T_TOK} tokens x {HQ + HK} heads x {D} in {el:.1f} s"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from fp8_quant_memory_gb300 import ledger
+    from fp8_quant_memory_gb300 import workloads as wl
+
+    d = wl.qk_inputs(T_TOK, HQ, HK, D, "bf16", "fp32", seed=20261202 + 2, std=2.0)
+    oracle.lib()
+    # size each step so the whole run stays within about a minute
+    t0 = time.perf_counter()
+    oracle.qk_norm_rope_quant(d["qk"][:64].contiguous(), d["wq"], d["wk"], d["cos"][:64].contiguous(),
+                              d["sin"][:64].contiguous(), HQ, HK)
+    per_token = (time.perf_counter() - t0) / 64
+    total = max(args.steps + args.warmup, 1)
+    tok = int(max(1, min(T_TOK, 60.0 / (total * per_token))))
+    sl = {k: d[k][:tok].contiguous() for k in ("qk", "cos", "sin")}
+    bytes_per = ledger.qk_prologue_bytes(tok, HQ, HK, D)
+    for _ in range(args.warmup):
+        oracle.qk_norm_rope_quant(sl["qk"], d["wq"], d["wk"], sl["cos"], sl["sin"], HQ, HK)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.qk_norm_rope_quant(sl["qk"], d["wq"], d["wk"], sl["cos"], sl["sin"], HQ, HK)
+    el = time.perf_counter() - t0
+    val = bytes_per * args.steps / el / 1e9
+    sample = f"each step: the first {tok} of {T_TOK} tokens x {HQ + HK} heads x {D}"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / max(args.steps, 1), 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": tok},
+        "cpu_baseline": {"value": round(val, 4), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(val, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100000)
+    ap.add_argument("--warmup", type=int, default=1024)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+
+    global _PG
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        _PG = dist.group.WORLD
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    import fp8_quant_memory_gb300 as fq
+    from fp8_quant_memory_gb300 import _capi
+
+    _capi.load()
+    stream = torch.cuda.Stream(dev)
+
+    case = PrologueCase(dev)
+    sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
+                           if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
+    sampler.start()
+    ms, warm_done = time_case(case, args.steps, args.warmup, stream)
+    clocks = sampler.stop()
+    ms = max_over_ranks(ms)
+    status = fq.device_status(clear=True)
+
+    per_launch_us = ms * 1e3 / args.steps
+    bytes_step = case.bytes_per_step()
+    value = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
+    achieved = bytes_step / (per_launch_us * 1e-6) / 1e9
+    peak, peak_kind = peaks()
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": warm_done, "ms_per_step": round(ms / args.steps, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens": T_TOK, "q_heads": HQ, "kv_heads": HK, "head_dim": D,
+                   "rope_dim": D, "bytes_per_step": bytes_step, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2: 8 rotating input/output sets, 525 MB per rotation",
+                   "launch": "CUDA graphs of up to 256 launches, replayed"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "traffic": profiled_traffic(), "kernel": "rows_vec_kernel<bf16,float,QK,8,0,1>",
+                     "us_per_launch": round(per_launch_us, 3)},
+        "gpu_launches": args.steps * case.kernels_per_step,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    if rank == 0:
+        line["e2e"] = e2e_prologue(case, min(args.steps, 200), stream)
+        if not args.no_extras:
+            extras = []
+            for mk in (lambda: RmsnormFwdCase(dev), lambda: RmsnormBwdCase(dev), lambda: RopeCase(dev),
+                       lambda: RopeQuantTinyCase(dev),
+                       lambda: PrologueCase(dev, T=32768, Hq=64, Hk=8, std=1.0, theta=1e6, positions="uniform",
+                                            outlier_frac=0.01, n_sets=2, seed=20261202 + 4)):
+                c = mk()
+                k = 2000 if c.bytes_per_step() < 3e8 else 400
+                m2, _ = time_case(c, k, 16, stream)
+                us = m2 * 1e3 / k
+                gbs = c.bytes_per_step() / (us * 1e-6) / 1e9
+                extras.append({"workload": c.name, "us_per_step": round(us, 3), "GB/s": round(gbs, 1),
+                               "frac": round(gbs / peak, 4), "bytes_per_step": c.bytes_per_step(),
+                               "kernels_per_step": c.kernels_per_step})
+                del c
+                torch.cuda.empty_cache()
+            eager = TorchEagerPrologueCase(case)
+            m3, _ = time_case(eager, 50, 5, stream, use_graph=False)
+            us = m3 * 1e3 / 50
+            extras.append({"workload": eager.name, "us_per_step": round(us, 3),
+                           "GB/s_of_fused_ledger": round(bytes_step / (us * 1e-6) / 1e9, 1)})
+            line["also"] = extras
+        if world == 1 and not args.no_cpu:
+            line["cpu_baseline"] = cpu_oracle_sample()
+        print(json.dumps(line), flush=True)
+    if _PG is not None:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

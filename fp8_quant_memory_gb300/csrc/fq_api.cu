@@ -1,0 +1,263 @@
+// fq_api.cu -- the extern "C" entry points declared in include/fq.h: argument validation on the
+// host (before any CUDA call), choice between the vectorised and the scalar kernels, launch, and
+// error reporting through fq_last_error().
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "fq.h"
+#include "fq_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return code;
+}
+
+int ok() {
+  g_err.clear();
+  return FQ_OK;
+}
+
+bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_launch(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+int check_common(const char* fn, int dtype, float eps) {
+  if (dtype != FQ_BF16 && dtype != FQ_FP16)
+    return fail(FQ_ERR_UNSUPPORTED, "%s: dtype %d is not FQ_BF16 or FQ_FP16", fn, dtype);
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(FQ_ERR_INVALID_ARG, "%s: eps must be finite and >= 0", fn);
+  return FQ_OK;
+}
+
+int check_fp8_max(const char* fn, float fp8_max) {
+  if (!(fp8_max > 0.0f && fp8_max <= 448.0f))
+    return fail(FQ_ERR_INVALID_ARG, "%s: fp8_max must be in (0, 448], got %g", fn, static_cast<double>(fp8_max));
+  return FQ_OK;
+}
+
+int check_rope(const char* fn, int64_t N, int64_t R, const void* cos, const void* sin, int table_dtype) {
+  if (R < 0 || R % 2 != 0 || R > N)
+    return fail(FQ_ERR_INVALID_ARG, "%s: rope_dim must be even and in [0, %lld], got %lld", fn,
+                static_cast<long long>(N), static_cast<long long>(R));
+  if (R > 0 && (cos == nullptr || sin == nullptr)) return fail(FQ_ERR_INVALID_ARG, "%s: cos/sin are null", fn);
+  if (table_dtype != FQ_BF16 && table_dtype != FQ_FP16 && table_dtype != FQ_FP32)
+    return fail(FQ_ERR_UNSUPPORTED, "%s: table dtype %d is not FQ_BF16, FQ_FP16 or FQ_FP32", fn, table_dtype);
+  return FQ_OK;
+}
+
+// Rows are indexed with 32-bit integers inside the kernels; element offsets are 64-bit.
+constexpr int64_t kMaxRows = 0x7fffffffLL;
+constexpr int64_t kMaxWidth = 1LL << 24;
+
+// Launch a row problem on the vectorised kernel when layout permits, else on the scalar kernel.
+int launch_rows(const char* fn, const fq::RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s) {
+  cudaGetLastError();  // drop a stale non-sticky error from an unrelated earlier call
+  const int64_t tsize = (table_dtype == FQ_FP32) ? 4 : 2;
+  bool vec = (a.N % 8 == 0) && (a.R % 16 == 0) && aligned(a.x, 16) && aligned(a.wq, 16) &&
+             aligned(a.wk, 16) && (a.token_stride * 2) % 16 == 0;
+  if (a.R > 0) vec = vec && aligned(a.cos, 16) && aligned(a.sin, 16) && ((a.R / 2) * tsize) % 16 == 0;
+  if (a.y != nullptr) vec = vec && aligned(a.y, 16);
+  if (a.q != nullptr) vec = vec && aligned(a.q, 8);
+  if (a.scale != nullptr) vec = vec && aligned(a.scale, 4);
+  if (!(vec && fq::launch_rows_vector(a, mode, dtype, table_dtype, s)))
+    fq::launch_rows_scalar(a, mode, dtype, table_dtype, s);
+  return check_launch(fn);
+}
+
+}  // namespace
+
+namespace fq {
+
+int sm_count() {
+  static int cache[128] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+}  // namespace fq
+
+extern "C" {
+
+const char* fq_last_error(void) { return g_err.c_str(); }
+
+int fq_version(void) { return 1; }
+
+int fq_device_status(unsigned int* word, int clear, cudaStream_t stream) {
+  if (word == nullptr) return fail(FQ_ERR_INVALID_ARG, "fq_device_status: word is null");
+  const cudaError_t e = fq::read_device_status(word, clear, stream);
+  if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "fq_device_status: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, int dtype, float eps,
+                   cudaStream_t stream) {
+  const char* fn = "fq_rmsnorm_fwd";
+  if (int rc = check_common(fn, dtype, eps)) return rc;
+  if (x == nullptr || w == nullptr || y == nullptr) return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
+    return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
+  if (M == 0) return ok();
+  fq::RowArgs a{};
+  a.x = x;
+  a.wq = a.wk = w;
+  a.y = y;
+  a.rows = M;
+  a.token_stride = N;
+  a.H = a.Hq = 1;
+  a.N = static_cast<int32_t>(N);
+  a.R = 0;
+  a.eps = eps;
+  a.fp8_max = 448.0f;
+  return launch_rows(fn, a, fq::MODE_FWD, dtype, dtype, stream);
+}
+
+int fq_rmsnorm_rope(const void* x, const void* w, const void* cos, const void* sin, void* y, int64_t M,
+                    int64_t N, int64_t rope_dim, int dtype, int table_dtype, float eps,
+                    cudaStream_t stream) {
+  const char* fn = "fq_rmsnorm_rope";
+  if (int rc = check_common(fn, dtype, eps)) return rc;
+  if (x == nullptr || w == nullptr || y == nullptr) return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
+    return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
+  if (int rc = check_rope(fn, N, rope_dim, cos, sin, table_dtype)) return rc;
+  if (M == 0) return ok();
+  fq::RowArgs a{};
+  a.x = x;
+  a.wq = a.wk = w;
+  a.cos = cos;
+  a.sin = sin;
+  a.y = y;
+  a.rows = M;
+  a.token_stride = N;
+  a.H = a.Hq = 1;
+  a.N = static_cast<int32_t>(N);
+  a.R = static_cast<int32_t>(rope_dim);
+  a.eps = eps;
+  a.fp8_max = 448.0f;
+  return launch_rows(fn, a, fq::MODE_ROPE, dtype, table_dtype, stream);
+}
+
+int fq_rmsnorm_rope_quant(const void* x, const void* w, const void* cos, const void* sin, void* y,
+                          uint8_t* q, float* scale, int64_t M, int64_t N, int64_t rope_dim, int dtype,
+                          int table_dtype, float eps, float fp8_max, cudaStream_t stream) {
+  const char* fn = "fq_rmsnorm_rope_quant";
+  if (int rc = check_common(fn, dtype, eps)) return rc;
+  if (int rc = check_fp8_max(fn, fp8_max)) return rc;
+  if (x == nullptr || w == nullptr || q == nullptr || scale == nullptr)
+    return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
+    return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
+  if (int rc = check_rope(fn, N, rope_dim, cos, sin, table_dtype)) return rc;
+  if (M == 0) return ok();
+  fq::RowArgs a{};
+  a.x = x;
+  a.wq = a.wk = w;
+  a.cos = cos;
+  a.sin = sin;
+  a.y = y;
+  a.q = q;
+  a.scale = scale;
+  a.rows = M;
+  a.token_stride = N;
+  a.H = a.Hq = 1;
+  a.N = static_cast<int32_t>(N);
+  a.R = static_cast<int32_t>(rope_dim);
+  a.eps = eps;
+  a.fp8_max = fp8_max;
+  return launch_rows(fn, a, fq::MODE_ROPE_QUANT, dtype, table_dtype, stream);
+}
+
+int fq_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, const void* wk,
+                          const void* cos, const void* sin, uint8_t* q_out, float* scale, int64_t T,
+                          int64_t Hq, int64_t Hk, int64_t D, int64_t rope_dim, int dtype,
+                          int table_dtype, float eps, float fp8_max, cudaStream_t stream) {
+  const char* fn = "fq_qk_norm_rope_quant";
+  if (int rc = check_common(fn, dtype, eps)) return rc;
+  if (int rc = check_fp8_max(fn, fp8_max)) return rc;
+  if (qk == nullptr || wq == nullptr || wk == nullptr || q_out == nullptr || scale == nullptr)
+    return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (T < 0 || Hq < 0 || Hk < 0 || Hq + Hk < 1 || D < 1 || D > kMaxWidth || Hq + Hk > kMaxWidth)
+    return fail(FQ_ERR_INVALID_ARG, "%s: need T >= 0, Hq, Hk >= 0, Hq + Hk >= 1, D >= 1", fn);
+  const int64_t H = Hq + Hk;
+  if (token_stride < H * D)
+    return fail(FQ_ERR_INVALID_ARG, "%s: token_stride %lld < (Hq+Hk)*D = %lld", fn,
+                static_cast<long long>(token_stride), static_cast<long long>(H * D));
+  if (T > kMaxRows / H) return fail(FQ_ERR_INVALID_ARG, "%s: T*(Hq+Hk) must be < 2^31", fn);
+  if (int rc = check_rope(fn, D, rope_dim, cos, sin, table_dtype)) return rc;
+  if (T == 0) return ok();
+  fq::RowArgs a{};
+  a.x = qk;
+  a.wq = wq;
+  a.wk = wk;
+  a.cos = cos;
+  a.sin = sin;
+  a.y = nullptr;
+  a.q = q_out;
+  a.scale = scale;
+  a.rows = T * H;
+  a.token_stride = token_stride;
+  a.H = static_cast<int32_t>(H);
+  a.Hq = static_cast<int32_t>(Hq);
+  a.N = static_cast<int32_t>(D);
+  a.R = static_cast<int32_t>(rope_dim);
+  a.eps = eps;
+  a.fp8_max = fp8_max;
+  return launch_rows(fn, a, fq::MODE_QK, dtype, table_dtype, stream);
+}
+
+size_t fq_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N) {
+  if (M <= 0 || N <= 0) return 0;
+  return fq::bwd_workspace_bytes(M, N);
+}
+
+int fq_rmsnorm_bwd(const void* x, const void* w, const void* grad_y, void* dx, void* dw, float* dw_f32,
+                   void* workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype, float eps,
+                   cudaStream_t stream) {
+  const char* fn = "fq_rmsnorm_bwd";
+  if (int rc = check_common(fn, dtype, eps)) return rc;
+  if (x == nullptr || w == nullptr || grad_y == nullptr || dx == nullptr || dw == nullptr)
+    return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
+  if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
+    return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
+  const size_t need = fq_rmsnorm_bwd_workspace_bytes(M, N);
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need))
+    return fail(FQ_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, need,
+                workspace == nullptr ? static_cast<size_t>(0) : workspace_bytes);
+  if (need > 0 && !aligned(workspace, 16)) return fail(FQ_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned", fn);
+  cudaGetLastError();
+  fq::BwdArgs a{};
+  a.x = x;
+  a.w = w;
+  a.g = grad_y;
+  a.dx = dx;
+  a.dw = dw;
+  a.dw_f32 = dw_f32;
+  a.partial = static_cast<float*>(workspace);
+  a.M = M;
+  a.N = static_cast<int32_t>(N);
+  a.eps = eps;
+  fq::launch_bwd(a, dtype, stream);
+  return check_launch(fn);
+}
+
+}  // extern "C"

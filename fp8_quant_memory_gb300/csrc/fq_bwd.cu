@@ -1,0 +1,314 @@
+// fq_bwd.cu -- RMSNorm backward ("rmsnorm_tl.py" (Ch.17), RMSNormTileLang.backward):
+//   rstd recomputed from x; xn = x*rstd; gw = g*w; c = mean(gw*xn);
+//   dx = dtype(rstd*(gw - xn*c));   dw = dtype(sum over rows of g*xn).
+//
+// dw is a column reduction over all M rows. It is done in two deterministic stages:
+//   stage 1: rows are cut into fixed chunks (a partition that depends on M only); one CTA owns a
+//            chunk, computes dx for its rows and writes the chunk's fp32 partial column sums;
+//   stage 2: every column adds its chunk partials in chunk order.
+// No atomics anywhere, so dw is bitwise reproducible run to run and independent of the grid.
+//
+// Stage 1 reads x and g once (16-byte streaming loads) and writes dx once. A row is owned by a
+// team of TPR threads (a lane group for narrow rows, several warps for wide rows); one reduction
+// per row yields both sum(x^2) and sum(gw*x), and c = rstd * sum(gw*x) / N (the same quantity as
+// mean(gw*xn) up to fp32 rounding order).
+#include "fq_device.cuh"
+#include "fq_internal.h"
+
+namespace fq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int64_t kMaxChunks = 256;
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+template <int TPR>
+__device__ __forceinline__ float team_sum_shfl(float v) {
+  return group_sum<(TPR < 32 ? TPR : 32)>(v);
+}
+
+template <typename T, int TPR, int VPT, int RB>
+__global__ void __launch_bounds__(kThreads) bwd_stage1_kernel(const BwdArgs a, int64_t rows_per_chunk) {
+  constexpr int G = kThreads / TPR;               // row teams per CTA
+  constexpr int WPT = TPR > 32 ? TPR / 32 : 1;    // warps per team
+  __shared__ float red[2][G][WPT][2 * RB];        // cross-warp row sums (TPR > 32), double buffered
+  extern __shared__ float comb[];                 // [G][VPT*TPR*8] team partials (G > 1)
+
+  const int tid = threadIdx.x;
+  const int g = tid / TPR;
+  const int l = tid % TPR;
+  const int N = a.N;
+  const int nv = N >> 3;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * rows_per_chunk;
+  const int64_t c1 = min(c0 + rows_per_chunk, a.M);
+  const float fN = static_cast<float>(N);
+
+  const T* wp = static_cast<const T*>(a.w);
+  float2 wf[VPT][4];
+  float2 acc[VPT][4];
+  bool ok[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = l + k * TPR;
+    ok[k] = v < nv;
+    const uint4 u = ok[k] ? ld_cached16(wp + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      wf[k][e] = Elem<T>::unpack(word(u, e));
+      acc[k][e] = make_float2(0.f, 0.f);
+    }
+  }
+
+  const int64_t nrows = c1 - c0;
+  const int64_t iters = (nrows + G * RB - 1) / (G * RB);
+  for (int64_t it = 0; it < iters; ++it) {
+    uint4 xv[RB][VPT], gv[RB][VPT];
+    int64_t row[RB];
+    bool rv[RB];
+#pragma unroll
+    for (int b = 0; b < RB; ++b) {
+      row[b] = c0 + (it * RB + b) * G + g;
+      rv[b] = row[b] < c1;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const bool live = rv[b] && ok[k];
+        const int64_t off = row[b] * N + 8 * (l + k * TPR);
+        xv[b][k] = live ? ld_stream16(static_cast<const T*>(a.x) + off) : make_uint4(0u, 0u, 0u, 0u);
+        gv[b][k] = live ? ld_stream16(static_cast<const T*>(a.g) + off) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    }
+    float ss[RB], sg[RB];
+#pragma unroll
+    for (int b = 0; b < RB; ++b) {
+      float2 s2 = make_float2(0.f, 0.f), g2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 xf = Elem<T>::unpack(word(xv[b][k], e));
+          const float2 gw = mul2(Elem<T>::unpack(word(gv[b][k], e)), wf[k][e]);
+          s2 = fma2(xf, xf, s2);
+          g2 = fma2(gw, xf, g2);
+        }
+      ss[b] = team_sum_shfl<TPR>(s2.x + s2.y);
+      sg[b] = team_sum_shfl<TPR>(g2.x + g2.y);
+    }
+    if constexpr (WPT > 1) {
+      const int buf = static_cast<int>(it & 1);
+      const int wi = l >> 5;
+      if ((l & 31) == 0) {
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+          red[buf][g][wi][2 * b] = ss[b];
+          red[buf][g][wi][2 * b + 1] = sg[b];
+        }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int b = 0; b < RB; ++b) {
+        float s = 0.f, q = 0.f;
+#pragma unroll
+        for (int j = 0; j < WPT; ++j) {  // fixed order
+          s += red[buf][g][j][2 * b];
+          q += red[buf][g][j][2 * b + 1];
+        }
+        ss[b] = s;
+        sg[b] = q;
+      }
+      // the other buffer is rewritten only after the next iteration's barrier
+    }
+#pragma unroll
+    for (int b = 0; b < RB; ++b) {
+      const float rstd = rstd_from_ss(ss[b], fN, a.eps);
+      const float c = __fdiv_rn(__fmul_rn(sg[b], rstd), fN);
+      const float2 rstd2 = splat2(rstd), c2 = splat2(c);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        uint4 out;
+        uint32_t pk[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 xn = mul2(Elem<T>::unpack(word(xv[b][k], e)), rstd2);
+          const float2 gf = Elem<T>::unpack(word(gv[b][k], e));
+          const float2 gw = mul2(gf, wf[k][e]);
+          const float2 d = add2(gw, neg2(mul2(xn, c2)));
+          pk[e] = Elem<T>::pack(mul2(rstd2, d));
+          acc[k][e] = fma2(gf, xn, acc[k][e]);
+        }
+        out = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        if (rv[b] && ok[k]) st_stream16(static_cast<T*>(a.dx) + row[b] * N + 8 * (l + k * TPR), out);
+      }
+    }
+  }
+
+  // Combine the G teams' column partials in team order and write this chunk's partial row.
+  float* prow = a.partial + static_cast<int64_t>(blockIdx.x) * N;
+  if constexpr (G == 1) {
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      if (!ok[k]) continue;
+      float* p = prow + 8 * (l + k * TPR);
+      reinterpret_cast<float4*>(p)[0] = make_float4(acc[k][0].x, acc[k][0].y, acc[k][1].x, acc[k][1].y);
+      reinterpret_cast<float4*>(p)[1] = make_float4(acc[k][2].x, acc[k][2].y, acc[k][3].x, acc[k][3].y);
+    }
+  } else {
+    constexpr int W = VPT * TPR * 8;  // padded row width held by one team
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 8 * (l + k * TPR) + 2 * e;
+        comb[g * W + j] = acc[k][e].x;
+        comb[g * W + j + 1] = acc[k][e].y;
+      }
+    __syncthreads();
+    for (int j = tid; j < N; j += kThreads) {
+      float s = 0.f;
+#pragma unroll
+      for (int t = 0; t < G; ++t) s += comb[t * W + j];
+      prow[j] = s;
+    }
+  }
+}
+
+// Stage 2: dw[j] = sum over chunks (in order) of partial[chunk, j]. One CTA per 32 columns; warp w
+// adds chunks w, w+8, ... in order, then warp 0 adds the 8 warp sums in order.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    bwd_stage2_kernel(const float* partial, int64_t chunks, int N, void* dw, float* dw_f32) {
+  __shared__ float part[kThreads / 32][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int j = blockIdx.x * 32 + lane;
+  float s = 0.f;
+  if (j < N) {
+    int64_t c = warp;
+    for (; c + 3 * 8 < chunks; c += 4 * 8) {
+      const float p0 = partial[c * N + j];
+      const float p1 = partial[(c + 8) * N + j];
+      const float p2 = partial[(c + 16) * N + j];
+      const float p3 = partial[(c + 24) * N + j];
+      s += p0;
+      s += p1;
+      s += p2;
+      s += p3;
+    }
+    for (; c < chunks; c += 8) s += partial[c * N + j];
+  }
+  part[warp][lane] = s;
+  __syncthreads();
+  if (warp == 0 && j < N) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) tot += part[w][lane];
+    if (dw_f32) dw_f32[j] = tot;
+    Elem<T>::store1(dw, j, tot);
+  }
+}
+
+// Scalar stage 1 for any N / alignment: one CTA per chunk walks its rows one at a time; thread i
+// owns columns i, i+256, ... and accumulates its chunk partials in the workspace row.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) bwd_stage1_scalar_kernel(const BwdArgs a, int64_t rows_per_chunk) {
+  __shared__ float red[kThreads / 32][2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int N = a.N;
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * rows_per_chunk;
+  const int64_t c1 = min(c0 + rows_per_chunk, a.M);
+  float* prow = a.partial + static_cast<int64_t>(blockIdx.x) * N;
+  for (int j = tid; j < N; j += kThreads) prow[j] = 0.f;
+  for (int64_t r = c0; r < c1; ++r) {
+    float ss = 0.f, sg = 0.f;
+    for (int j = tid; j < N; j += kThreads) {
+      const float x = Elem<T>::load1(a.x, r * N + j);
+      const float gw = __fmul_rn(Elem<T>::load1(a.g, r * N + j), Elem<T>::load1(a.w, j));
+      ss = __fmaf_rn(x, x, ss);
+      sg = __fmaf_rn(gw, x, sg);
+    }
+    ss = group_sum<32>(ss);
+    sg = group_sum<32>(sg);
+    if (lane == 0) {
+      red[warp][0] = ss;
+      red[warp][1] = sg;
+    }
+    __syncthreads();
+    ss = 0.f;
+    sg = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+      ss += red[w][0];
+      sg += red[w][1];
+    }
+    __syncthreads();
+    const float rstd = rstd_from_ss(ss, static_cast<float>(N), a.eps);
+    const float c = __fdiv_rn(__fmul_rn(sg, rstd), static_cast<float>(N));
+    for (int j = tid; j < N; j += kThreads) {
+      const float gf = Elem<T>::load1(a.g, r * N + j);
+      const float xn = __fmul_rn(Elem<T>::load1(a.x, r * N + j), rstd);
+      const float gw = __fmul_rn(gf, Elem<T>::load1(a.w, j));
+      Elem<T>::store1(a.dx, r * N + j, __fmul_rn(rstd, __fsub_rn(gw, __fmul_rn(xn, c))));
+      prow[j] = __fmaf_rn(gf, xn, prow[j]);
+    }
+  }
+}
+
+template <typename T, int TPR, int VPT, int RB>
+void launch_stage1(const BwdArgs& a, const BwdPlan& p, cudaStream_t s) {
+  constexpr int G = kThreads / TPR;
+  const size_t smem = (G > 1) ? static_cast<size_t>(G) * VPT * TPR * 8 * sizeof(float) : 0;
+  auto kern = bwd_stage1_kernel<T, TPR, VPT, RB>;
+  if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  kern<<<static_cast<unsigned>(p.chunks), kThreads, smem, s>>>(a, p.rows_per_chunk);
+}
+
+bool vector_ok(const BwdArgs& a, int dtype_size) {
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  return (a.N % 8 == 0) && al(a.x) && al(a.w) && al(a.g) && al(a.dx) && al(a.partial) && dtype_size == 2;
+}
+
+template <typename T>
+void launch_bwd_t(const BwdArgs& a, cudaStream_t s) {
+  const BwdPlan p = bwd_plan(a.M);
+  if (a.M > 0) {
+    const int nv = a.N / 8;
+    const bool vec = vector_ok(a, sizeof(T));
+    if (vec && nv <= 16) launch_stage1<T, 16, 1, 2>(a, p, s);
+    else if (vec && nv <= 32) launch_stage1<T, 32, 1, 2>(a, p, s);
+    else if (vec && nv <= 64) launch_stage1<T, 64, 1, 2>(a, p, s);
+    else if (vec && nv <= 128) launch_stage1<T, 128, 1, 2>(a, p, s);
+    else if (vec && nv <= 256) launch_stage1<T, 256, 1, 2>(a, p, s);
+    else if (vec && nv <= 512) launch_stage1<T, 256, 2, 2>(a, p, s);
+    else if (vec && nv <= 1024) launch_stage1<T, 256, 4, 1>(a, p, s);
+    else bwd_stage1_scalar_kernel<T><<<static_cast<unsigned>(p.chunks), kThreads, 0, s>>>(a, p.rows_per_chunk);
+  }
+  const unsigned grid2 = static_cast<unsigned>((a.N + 31) / 32);
+  bwd_stage2_kernel<T><<<grid2, kThreads, 0, s>>>(a.partial, p.chunks, a.N, a.dw, a.dw_f32);
+}
+
+}  // namespace
+
+BwdPlan bwd_plan(int64_t M) {
+  BwdPlan p;
+  if (M <= 0) {
+    p.chunks = 0;
+    p.rows_per_chunk = 1;
+    return p;
+  }
+  p.rows_per_chunk = (M + kMaxChunks - 1) / kMaxChunks;
+  p.chunks = (M + p.rows_per_chunk - 1) / p.rows_per_chunk;
+  return p;
+}
+
+size_t bwd_workspace_bytes(int64_t M, int64_t N) {
+  const BwdPlan p = bwd_plan(M);
+  return static_cast<size_t>(p.chunks) * static_cast<size_t>(N) * sizeof(float);
+}
+
+void launch_bwd(const BwdArgs& a, int dtype, cudaStream_t s) {
+  if (dtype == DT_BF16) launch_bwd_t<__nv_bfloat16>(a, s);
+  else launch_bwd_t<__half>(a, s);
+}
+
+}  // namespace fq

@@ -1,0 +1,166 @@
+// fq_device.cuh -- device-side building blocks of the sm_103a kernels: storage-format traits,
+// cache-hinted 16/8-byte memory access, packed f32x2 arithmetic, e4m3fn packing, group reductions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fq {
+
+// ------------------------------------------------------------------------------------------------
+// Storage element traits: two packed 16-bit elements (lower address in the low half) <-> float2.
+// Conversions to float are exact; conversions from float round to nearest even.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<__nv_bfloat16> {
+  static __device__ __forceinline__ float2 unpack(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+  }
+  static __device__ __forceinline__ uint32_t pack(float2 v) {
+    __nv_bfloat162 h = __float22bfloat162_rn(v);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ float load1(const void* p, int64_t i) {
+    const uint16_t b = static_cast<const uint16_t*>(p)[i];
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+  static __device__ __forceinline__ void store1(void* p, int64_t i, float v) {
+    __nv_bfloat16 h = __float2bfloat16_rn(v);
+    static_cast<__nv_bfloat16*>(p)[i] = h;
+  }
+};
+
+template <>
+struct Elem<__half> {
+  static __device__ __forceinline__ float2 unpack(uint32_t u) {
+    return __half22float2(*reinterpret_cast<__half2*>(&u));
+  }
+  static __device__ __forceinline__ uint32_t pack(float2 v) {
+    __half2 h = __float22half2_rn(v);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  static __device__ __forceinline__ float load1(const void* p, int64_t i) {
+    return __half2float(static_cast<const __half*>(p)[i]);
+  }
+  static __device__ __forceinline__ void store1(void* p, int64_t i, float v) {
+    static_cast<__half*>(p)[i] = __float2half_rn(v);
+  }
+};
+
+template <>
+struct Elem<float> {
+  static __device__ __forceinline__ float load1(const void* p, int64_t i) {
+    return static_cast<const float*>(p)[i];
+  }
+};
+
+// Round a float2 to the storage format and back (the `.to(dtype)` cast of the definition).
+template <typename T>
+__device__ __forceinline__ float2 round_trip(float2 v) {
+  return Elem<T>::unpack(Elem<T>::pack(v));
+}
+
+// ------------------------------------------------------------------------------------------------
+// Memory access. Streamed data (x, grad_y) bypasses L1 allocation; outputs use evict-first stores.
+// Small reused data (weights, rotary tables) goes through the default cached path.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream16(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+__device__ __forceinline__ uint4 ld_cached16(const void* p) {
+  return __ldg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ float4 ld_cached16f(const void* p) {
+  return __ldg(reinterpret_cast<const float4*>(p));
+}
+
+__device__ __forceinline__ void st_stream16(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_stream8(void* p, uint2 v) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+// ------------------------------------------------------------------------------------------------
+// Packed fp32 pairs (one FFMA2/FMUL2/FADD2 instruction per pair on sm_100-class SMs).
+// Each component is rounded exactly like the scalar IEEE operation.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a, b); }
+__device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+__device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
+
+// Quotient y / s rounded to nearest, given r = RN(1/s) (correctly rounded reciprocal):
+// q0 = RN(y*r) is within one ulp of y/s, the residual y - q0*s is exact in one FMA, and
+// RN(q0 + residual*r) is the correctly rounded quotient (Markstein's correction, IBM J. Res.
+// Dev. 34(1), 1990; Muller et al., Handbook of Floating-Point Arithmetic, ch. 4).
+__device__ __forceinline__ float2 div2_by(float2 y, float s, float r) {
+  const float2 q0 = mul2(y, splat2(r));
+  const float2 e = fma2(neg2(q0), splat2(s), y);
+  return fma2(e, splat2(r), q0);
+}
+
+// ------------------------------------------------------------------------------------------------
+// e4m3fn: cvt.rn.satfinite rounds to nearest even and saturates at +-448 (the format's largest
+// finite value), which is the clamp-then-round of the definition when fp8_max = 448.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t e4m3x2(float2 v) {  // v.x -> low byte, v.y -> high byte
+  uint16_t d;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(v.y), "f"(v.x));
+  return d;
+}
+
+// 8 quotients -> 8 codes (element 0 at the lowest address).
+__device__ __forceinline__ uint2 pack_e4m3x8(float2 a, float2 b, float2 c, float2 d) {
+  return make_uint2(e4m3x2(a) | (e4m3x2(b) << 16), e4m3x2(c) | (e4m3x2(d) << 16));
+}
+
+__device__ __forceinline__ float clamp_abs(float v, float m) { return fminf(fmaxf(v, -m), m); }
+
+// ------------------------------------------------------------------------------------------------
+// Reductions over a group of G consecutive lanes (G a power of two <= 32). Every lane of the warp
+// must call these (full-mask shuffles); each lane receives its own group's result.
+// ------------------------------------------------------------------------------------------------
+template <int G>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+template <int G>
+__device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+  for (int o = G / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float absmax4(float m, float2 a, float2 b) {
+  // three-input max.f32 (sm_100+): two instructions for four values
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(m), "f"(fabsf(a.x)), "f"(fabsf(a.y)));
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(r), "f"(fabsf(b.x)), "f"(fabsf(b.y)));
+  return r;
+}
+
+// rstd from the row's sum of squares: 1/sqrt(ss/N + eps), every step correctly rounded in fp32.
+__device__ __forceinline__ float rstd_from_ss(float ss, float n, float eps) {
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n), eps)));
+}
+
+}  // namespace fq

@@ -1,0 +1,77 @@
+// fq_internal.h -- host-side launch interface shared by the translation units of libfq.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace fq {
+
+enum Mode : int {
+  MODE_FWD = 0,         // y = dtype(x*rstd*w)
+  MODE_ROPE = 1,        // y = dtype(rope(dtype(x*rstd*w)))
+  MODE_ROPE_QUANT = 2,  // as MODE_ROPE, then q/scale from the rounded y; y optional
+  MODE_QK = 3,          // prologue: fp32 from load to quantiser, per-head weight, per-token table
+};
+
+enum Dtype : int { DT_BF16 = 0, DT_FP16 = 1, DT_FP32 = 2 };
+
+// One launch over `rows` rows of width N. Row r belongs to token t = r / H and head h = r % H;
+// its input starts at x + t*token_stride + h*N and it uses weight (h < Hq ? wq : wk) and table
+// row t. Outputs are contiguous: y/q row r at r*N, scale at r. The rmsnorm_* entry points use
+// H = Hq = 1 and token_stride = N.
+struct RowArgs {
+  const void* x;
+  const void* wq;
+  const void* wk;
+  const void* cos;
+  const void* sin;
+  void* y;         // nullable (MODE_ROPE_QUANT), unused in MODE_QK
+  uint8_t* q;      // quant modes
+  float* scale;    // quant modes
+  int64_t rows;
+  int64_t token_stride;  // elements
+  int32_t H, Hq;
+  int32_t N, R;
+  float eps;
+  float fp8_max;
+};
+
+// Vectorised path: needs N % 8 == 0, R % 16 == 0, 16-byte aligned x/w/y/cos/sin and token stride,
+// 8-byte aligned q, table dtype equal to the storage dtype or fp32, and a supported width.
+// Returns false (launching nothing) when the shape has no instantiation.
+bool launch_rows_vector(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s);
+
+// Scalar path: any N >= 1, even R, any alignment, any dtype combination.
+void launch_rows_scalar(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s);
+
+// Backward. Partition of rows into dw chunks (depends on M only).
+struct BwdPlan {
+  int64_t chunks;
+  int64_t rows_per_chunk;
+};
+BwdPlan bwd_plan(int64_t M);
+size_t bwd_workspace_bytes(int64_t M, int64_t N);
+
+struct BwdArgs {
+  const void* x;
+  const void* w;
+  const void* g;
+  void* dx;
+  void* dw;
+  float* dw_f32;  // nullable
+  float* partial;  // [chunks, N] fp32 workspace
+  int64_t M;
+  int32_t N;
+  float eps;
+};
+void launch_bwd(const BwdArgs& a, int dtype, cudaStream_t s);
+
+// Device status word (bit 0: a bounded wait gave up). device_status_ptr() is its device address,
+// passed to kernels in other translation units.
+cudaError_t read_device_status(unsigned int* word, int clear, cudaStream_t s);
+unsigned int* device_status_ptr();
+
+int sm_count();
+
+}  // namespace fq

@@ -1,0 +1,57 @@
+"""Ideal (algorithmic) byte ledger of each entry point: every input read once, every output written
+once, the norm weight(s) and the rotary table counted once per call.
+
+This follows the accounting rule of "ledger.py" (Ch.13 ledger: one read per input, one write per
+output, intermediates not free) and the prologue ledger of "case_norm_rope_quant.py" (Ch.28,
+``Design.payload_bytes`` + ``Design.ideal_lookup_bytes``), with one correction: the tables here are
+half width ([rows, rope_dim/2] per cos and sin), so the table term is ``2 * T * (R/2) * table_bytes``
+instead of the page's ``2 * T * head_dim * table_bytes``.
+"""
+from __future__ import annotations
+
+ELEM_BYTES = {"fp32": 4, "fp16": 2, "bf16": 2, "e4m3": 1}
+
+
+def qk_prologue_bytes(T: int, Hq: int, Hk: int, D: int, R: int | None = None, dtype: str = "bf16",
+                      table_dtype: str = "fp32") -> int:
+    R = D if R is None else R
+    rows = T * (Hq + Hk)
+    x = rows * D * ELEM_BYTES[dtype]
+    q = rows * D * ELEM_BYTES["e4m3"]
+    scale = rows * 4
+    table = 2 * T * (R // 2) * ELEM_BYTES[table_dtype]
+    weights = 2 * D * ELEM_BYTES[dtype]
+    return x + q + scale + table + weights
+
+
+def rope_quant_bytes(M: int, N: int, R: int, dtype: str = "bf16", table_dtype: str = "bf16",
+                     write_y: bool = True) -> int:
+    e = ELEM_BYTES[dtype]
+    return (M * N * e + N * e + 2 * M * (R // 2) * ELEM_BYTES[table_dtype] + (M * N * e if write_y else 0)
+            + M * N + M * 4)
+
+
+def rope_bytes(M: int, N: int, R: int, dtype: str = "fp16", table_dtype: str = "fp16") -> int:
+    e = ELEM_BYTES[dtype]
+    return 2 * M * N * e + N * e + 2 * M * (R // 2) * ELEM_BYTES[table_dtype]
+
+
+def rmsnorm_fwd_bytes(M: int, N: int, dtype: str = "bf16") -> int:
+    e = ELEM_BYTES[dtype]
+    return 2 * M * N * e + N * e
+
+
+def rmsnorm_bwd_bytes(M: int, N: int, dtype: str = "bf16") -> int:
+    """x, grad_y read; dx written; w read; dw written (the fp32 partial workspace is extra)."""
+    e = ELEM_BYTES[dtype]
+    return 3 * M * N * e + 2 * N * e
+
+
+def page_prologue_ideal_bytes(T: int, Hq: int, Hk: int, D: int, in_bytes: int = 2, out_bytes: int = 1,
+                              table_bytes: int = 4) -> int:
+    """The Ch.28 page's own ideal ledger (payload + ideal lookup), table counted at full head_dim width."""
+    rows = T * (Hq + Hk)
+    elems = rows * D
+    payload = elems * in_bytes + elems * out_bytes + rows * 4
+    lookup = 2 * D * in_bytes + 2 * T * D * table_bytes
+    return payload + lookup

@@ -1,8 +1,9 @@
 """Seeded synthetic inputs for the fused RMSNorm / RoPE / FP8 path.
 
 This module builds inputs only; it holds none of the method's arithmetic. Both the CUDA path and the
-reference oracle are fed from it. Every array is drawn in fp64 from ``numpy.random.Generator(PCG64)``
-with an explicit seed and then converted to its storage dtype by torch.
+reference oracle are fed from it. Every array is drawn from ``numpy.random.Generator(PCG64)`` with an
+explicit seed -- the large activation arrays as fp32 standard normals scaled by their std, weights and
+tables in fp64 -- and then converted to its storage dtype by torch.
 
 The rotary tables are inputs too: ``angle[row, p] = pos[row] * theta ** (-2p / rope_dim)`` for
 ``p < rope_dim / 2`` in fp64, ``cos``/``sin`` of that in fp64, then rounded to the table dtype. The
@@ -49,6 +50,22 @@ def _to(a: np.ndarray, dtype: str) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(a)).to(_TORCH_DTYPES[dtype])
 
 
+def _normal32(rng: np.random.Generator, std: float, size) -> np.ndarray:
+    """N(0, std) activations drawn in fp32 (they are stored in bf16/fp16 anyway)."""
+    v = rng.standard_normal(size=size, dtype=np.float32)
+    if std != 1.0:
+        v *= np.float32(std)
+    return v
+
+
+def _distinct_indices(rng: np.random.Generator, n: int, k: int) -> np.ndarray:
+    """k distinct indices in [0, n), uniform without replacement (oversample, dedupe, subsample)."""
+    cand = np.unique(rng.integers(0, n, size=int(k * 1.02) + 1024, dtype=np.int64))
+    while cand.size < k:
+        cand = np.unique(np.concatenate([cand, rng.integers(0, n, size=k, dtype=np.int64)]))
+    return cand[rng.permutation(cand.size)[:k]]
+
+
 def rope_table(positions: np.ndarray, rope_dim: int, theta: float, dtype: str):
     """(cos, sin), each [len(positions), rope_dim // 2] in ``dtype``."""
     half = rope_dim // 2
@@ -70,7 +87,7 @@ def rows_inputs(M: int, N: int, rope_dim: int, dtype: str = "bf16", table_dtype:
     Row r takes the position of its token, ``r // heads_per_token`` (1: pos = row index).
     """
     rng = _rng(seed)
-    x = _to(rng.normal(0.0, std, size=(M, N)), dtype)
+    x = _to(_normal32(rng, std, (M, N)), dtype)
     w = _to(rng.normal(1.0, 0.1, size=N), dtype)
     pos = np.arange(M, dtype=np.int64) // max(heads_per_token, 1)
     cos, sin = rope_table(pos, max(rope_dim, 2), theta, table_dtype)
@@ -82,8 +99,8 @@ def rows_inputs(M: int, N: int, rope_dim: int, dtype: str = "bf16", table_dtype:
 def rmsnorm_inputs(M: int, N: int, dtype: str = "bf16", seed: int = BASE_SEED, std: float = 1.0):
     """x, grad_y [M, N] ~N(0, std), w [N] ~N(1, 0.1)."""
     rng = _rng(seed)
-    x = _to(rng.normal(0.0, std, size=(M, N)), dtype)
-    g = _to(rng.normal(0.0, 1.0, size=(M, N)), dtype)
+    x = _to(_normal32(rng, std, (M, N)), dtype)
+    g = _to(_normal32(rng, 1.0, (M, N)), dtype)
     w = _to(rng.normal(1.0, 0.1, size=N), dtype)
     return {"x": x, "g": g, "w": w}
 
@@ -101,11 +118,10 @@ def qk_inputs(T: int, Hq: int, Hk: int, D: int, dtype: str = "bf16", table_dtype
     H = Hq + Hk
     R = D if rope_dim is None else rope_dim
     rng = _rng(seed)
-    vals = rng.normal(0.0, std, size=T * H * D)
+    vals = _normal32(rng, std, T * H * D)
     if outlier_frac > 0.0:
         k = int(round(outlier_frac * vals.size))
-        idx = rng.choice(vals.size, size=k, replace=False)
-        vals[idx] *= outlier_mult
+        vals[_distinct_indices(rng, vals.size, k)] *= np.float32(outlier_mult)
     wq = _to(rng.normal(1.0, 0.1, size=D), dtype)
     wk = _to(rng.normal(1.0, 0.1, size=D), dtype)
     if positions == "arange":
@@ -122,7 +138,7 @@ def qk_inputs(T: int, Hq: int, Hk: int, D: int, dtype: str = "bf16", table_dtype
     else:
         if token_stride < H * D:
             raise ValueError("token_stride must be >= (Hq+Hk)*D")
-        full = rng.normal(0.0, std, size=(T, token_stride))
+        full = _normal32(rng, std, (T, token_stride))
         full[:, : H * D] = vals.reshape(T, H * D)
         qk = _to(full, dtype)
     return {"qk": qk, "wq": wq, "wk": wk, "cos": cos, "sin": sin, "positions": pos,

@@ -1,0 +1,145 @@
+/*
+ * fq.h -- C ABI of libfq: fused RMSNorm -> NeoX partial RoPE -> per-row FP8 (e4m3fn) quantisation
+ * on GB300 (sm_103a), plus the standalone RMSNorm forward and backward.
+ *
+ * Conventions shared by every entry point
+ *   - Every tensor pointer is a DEVICE pointer owned by the caller. The library never allocates,
+ *     frees or retains any of them; it does not keep pointers past the call.
+ *   - Work is enqueued on `stream` (0 = the legacy default stream) and runs asynchronously: outputs
+ *     are valid once the stream reaches that point. No entry point synchronises.
+ *   - Shapes are element counts. All tensors are row-major and contiguous unless a stride argument
+ *     says otherwise. Output buffers must not overlap input buffers.
+ *   - Storage dtypes: FQ_BF16 (bfloat16) or FQ_FP16 (IEEE binary16) for x, w, y, grad_y, dx, dw.
+ *     Rotary tables: FQ_BF16, FQ_FP16 or FQ_FP32. FP8 outputs are uint8 codes in OCP E4M3 "fn"
+ *     encoding (bias 7, max +-448, no infinities, NaN = S.1111.111).
+ *   - Return value: FQ_OK, or an fq_status error code. On error nothing was launched and a
+ *     message is available from fq_last_error() (per thread). Argument checks happen on the host
+ *     before any CUDA call, so an invalid call never touches the device.
+ *   - Rows of 16-byte aligned, 8-element multiples take the vectorised kernels; anything else
+ *     (odd widths, unaligned pointers, rope_dim not a multiple of 16, other table dtypes) takes a
+ *     scalar kernel with the same results. No combination falls back to the host.
+ *
+ * Sources of the definitions (tutorial pages, cited by title and function):
+ *   "rmsnorm_rope_quant.py" (Ch.13 operators I, fusion capstone): torch_reference_fused,
+ *       _torch_rope_neox, rms_norm_rope_fused, rms_norm_rope_quant_fused.
+ *   "rmsnorm_tl.py" (Ch.17 end-to-end training): _rmsnorm_fwd, RMSNormTileLang.backward.
+ *   "case_norm_rope_quant.py" (Ch.28 operator design methodology): the QK-Norm + RoPE + FP8
+ *       attention prologue (module docstring) and design C (one token's rows share the lookups).
+ */
+#ifndef FQ_H_
+#define FQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes. */
+enum fq_status {
+  FQ_OK = 0,
+  FQ_ERR_INVALID_ARG = 1, /* null pointer, non-positive or inconsistent shape, odd rope_dim,
+                             rope_dim > row width, fp8_max outside (0, 448], eps < 0 or not finite */
+  FQ_ERR_UNSUPPORTED = 2, /* dtype code not accepted by this entry point */
+  FQ_ERR_MISALIGNED = 3,  /* reserved: misaligned inputs take the scalar path instead */
+  FQ_ERR_CUDA = 4,        /* a CUDA call failed (launch error, no device); see fq_last_error() */
+  FQ_ERR_DEVICE = 5       /* a kernel reported a failure through the device status word */
+};
+
+/* Storage dtype codes. */
+enum fq_dtype { FQ_BF16 = 0, FQ_FP16 = 1, FQ_FP32 = 2 };
+
+/* Message describing the last error returned on the calling thread ("" if none). The string is
+ * owned by the library and stays valid until the next call on the same thread. */
+const char* fq_last_error(void);
+
+/* Library ABI version (incremented on any signature change). */
+int fq_version(void);
+
+/* Reads the device status word of the current device after synchronising `stream`, optionally
+ * clearing it. Bit 0 (value 1): a pipelined kernel gave up on a bounded wait and skipped its
+ * remaining work. `*word` receives the bits. Returns FQ_OK or FQ_ERR_CUDA. */
+int fq_device_status(unsigned int* word, int clear, cudaStream_t stream);
+
+/*
+ * RMSNorm forward ("rmsnorm_tl.py", _rmsnorm_fwd):
+ *   rstd_i = 1 / sqrt(sum_j x_ij^2 / N + eps)   (fp32)
+ *   y_ij   = dtype((x_ij * rstd_i) * w_j)        (fp32 products, one rounding to dtype)
+ * x, y: [M, N] dtype; w: [N] dtype. M >= 0 (M = 0 is a no-op), N >= 1.
+ */
+int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, int dtype, float eps,
+                   cudaStream_t stream);
+
+/*
+ * RMSNorm + NeoX partial RoPE ("rmsnorm_rope_quant.py", rms_norm_rope_fused and the first two
+ * steps of torch_reference_fused):
+ *   normed_ij = dtype((x_ij * rstd_i) * w_j)
+ *   for p < R/2, lo = normed[i, N-R+p], hi = normed[i, N-R+R/2+p], c = cos[i,p], s = sin[i,p]:
+ *     y[i, N-R+p]     = dtype(lo*c - hi*s)
+ *     y[i, N-R+R/2+p] = dtype(hi*c + lo*s)
+ *   the first N-R columns of y are normed unchanged.
+ * x, y: [M, N] dtype; w: [N]; cos, sin: [M, R/2] table_dtype (one table row per x row).
+ * R = rope_dim: even, 0 <= R <= N (R = 0: no rotation; cos/sin may then be null).
+ */
+int fq_rmsnorm_rope(const void* x, const void* w, const void* cos, const void* sin, void* y, int64_t M,
+                    int64_t N, int64_t rope_dim, int dtype, int table_dtype, float eps,
+                    cudaStream_t stream);
+
+/*
+ * RMSNorm + NeoX partial RoPE + per-row FP8 ("rmsnorm_rope_quant.py", torch_reference_fused):
+ *   y as in fq_rmsnorm_rope (rounded to dtype);
+ *   scale_i = max(max_j |y_ij|, 1e-4) / fp8_max                       (fp32)
+ *   q_ij    = e4m3fn_round_to_nearest_even(clamp(y_ij / scale_i, -fp8_max, fp8_max))
+ * y: [M, N] dtype, or null to skip writing it (q and scale are unchanged by that choice);
+ * q: [M, N] uint8 e4m3fn codes; scale: [M] fp32. fp8_max in (0, 448] (448 = e4m3fn max).
+ */
+int fq_rmsnorm_rope_quant(const void* x, const void* w, const void* cos, const void* sin, void* y,
+                          uint8_t* q, float* scale, int64_t M, int64_t N, int64_t rope_dim, int dtype,
+                          int table_dtype, float eps, float fp8_max, cudaStream_t stream);
+
+/*
+ * QK-Norm + RoPE + FP8 attention prologue ("case_norm_rope_quant.py", module docstring; design C):
+ *   for every token t < T and head h < H = Hq + Hk, the row x = qk[t*token_stride + h*D + (0..D-1)]
+ *   is normalised with wq (h < Hq) or wk (h >= Hq), its last R columns are rotated with table row t
+ *   (shared by every head of the token), and it is quantised with one fp32 scale per row:
+ *     n_j = (x_j * rstd) * w_j;  y = rope(n) as above;  all in fp32 (no rounding to dtype);
+ *     scale[t,h] = max(max_j |y_j|, 1e-4) / fp8_max;  q[t,h,j] = e4m3fn(clamp(y_j / scale, +-fp8_max))
+ * qk: dtype, token_stride >= H*D elements between consecutive tokens (H*D when packed; larger for
+ *     the q/k slice of a fused QKV projection row).
+ * wq, wk: [D] dtype. cos, sin: [T, R/2] table_dtype. q_out: [T, H, D] uint8. scale: [T, H] fp32.
+ * R = rope_dim: even, 0 <= R <= D. T = 0 is a no-op.
+ */
+int fq_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, const void* wk,
+                          const void* cos, const void* sin, uint8_t* q_out, float* scale, int64_t T,
+                          int64_t Hq, int64_t Hk, int64_t D, int64_t rope_dim, int dtype,
+                          int table_dtype, float eps, float fp8_max, cudaStream_t stream);
+
+/*
+ * Bytes of caller-provided device workspace fq_rmsnorm_bwd needs for an [M, N] problem: the fp32
+ * per-chunk partial column sums of the two-stage dw reduction. 0 when M == 0.
+ */
+size_t fq_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N);
+
+/*
+ * RMSNorm backward ("rmsnorm_tl.py", RMSNormTileLang.backward), rstd recomputed from x:
+ *   xn = x * rstd;  gw = g * w;  c = mean_j(gw_j * xn_j)
+ *   dx = dtype(rstd * (gw - xn * c))                  [M, N]
+ *   dw = dtype(sum_i g_ij * xn_ij)                    [N]  (fp32 sums)
+ * dw is reduced in two deterministic stages: fixed row chunks (a partition that depends only on M)
+ * write fp32 partial column sums to `workspace`, then each column sums its chunks in order. The
+ * result is bitwise reproducible run to run. dw_f32 (nullable) receives the fp32 sums before the
+ * final rounding. workspace: at least fq_rmsnorm_bwd_workspace_bytes(M, N) bytes, 16-byte aligned,
+ * no initial contents required. M = 0 writes dw = 0.
+ */
+int fq_rmsnorm_bwd(const void* x, const void* w, const void* grad_y, void* dx, void* dw, float* dw_f32,
+                   void* workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype, float eps,
+                   cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FQ_H_ */

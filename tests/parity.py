@@ -1,0 +1,69 @@
+"""Tolerance rules shared by the parity tests (CUDA path vs the oracle).
+
+- bf16 outputs: |gpu - ref| <= max(2^-7 |ref|, 1e-3)   (the stated bf16 tolerance)
+- fp16 outputs: |gpu - ref| <= max(2^-9 |ref|, 1e-3)   (two fp16 ulps; fp16 has 3 more bits)
+- fp32 scales:  relative difference <= 1e-5
+- fp8 codes:    identical, or one e4m3 step apart on at most 0.1% of the elements
+- dw (fp32 sums): |gpu - ref| <= 1e-3 * max(|ref|, rms(ref)); bf16/fp16 dw within one ulp
+"""
+from __future__ import annotations
+
+import torch
+
+
+def storage_tol(dtype):
+    return (2.0 ** -7, 1e-3) if dtype == torch.bfloat16 else (2.0 ** -9, 1e-3)
+
+
+def assert_storage_close(gpu: torch.Tensor, ref: torch.Tensor, what: str = "y"):
+    rel, abs_ = storage_tol(ref.dtype)
+    a = gpu.detach().cpu().double()
+    b = ref.double()
+    err = (a - b).abs()
+    bound = torch.clamp(b.abs() * rel, min=abs_)
+    bad = err > bound
+    assert not bool(bad.any()), (
+        f"{what}: {int(bad.sum())} of {bad.numel()} elements outside the tolerance; worst err "
+        f"{float(err.max()):.3g} at ref {float(b.flatten()[int(err.flatten().argmax())]):.5g}")
+
+
+def code_order(q: torch.Tensor) -> torch.Tensor:
+    """Signed position of each e4m3fn code on the number line (adjacent finite values differ by 1)."""
+    q = q.to(torch.int32)
+    mag = q & 0x7F
+    return torch.where((q & 0x80) != 0, -mag, mag)
+
+
+def assert_codes_close(gpu_q: torch.Tensor, ref_q: torch.Tensor, what: str = "q", max_frac: float = 1e-3):
+    a = code_order(gpu_q.detach().cpu())
+    b = code_order(ref_q)
+    d = (a - b).abs()
+    assert int(d.max()) <= 1 if d.numel() else True, f"{what}: codes differ by {int(d.max())} steps"
+    frac = float((d != 0).float().mean()) if d.numel() else 0.0
+    assert frac <= max_frac, f"{what}: {frac:.2%} of codes differ (limit {max_frac:.2%})"
+    return frac
+
+
+def assert_scale_close(gpu_s: torch.Tensor, ref_s: torch.Tensor, rel: float = 1e-5, what: str = "scale"):
+    a = gpu_s.detach().cpu().double()
+    b = ref_s.double()
+    r = ((a - b).abs() / b.abs()).max() if b.numel() else torch.tensor(0.0)
+    assert float(r) <= rel, f"{what}: relative difference {float(r):.3g} > {rel}"
+
+
+def assert_dw_close(gpu_f32: torch.Tensor, ref_f32: torch.Tensor, rel: float = 1e-3):
+    a = gpu_f32.detach().cpu().double()
+    b = ref_f32.double()
+    rms = b.pow(2).mean().sqrt()
+    bound = rel * torch.maximum(b.abs(), rms)
+    bad = (a - b).abs() > bound
+    assert not bool(bad.any()), f"dw_f32: {int(bad.sum())} columns outside 1e-3 * max(|ref|, rms)"
+
+
+def assert_within_one_ulp(gpu: torch.Tensor, ref: torch.Tensor, what: str = "dw"):
+    a = gpu.detach().cpu().view(torch.int16).to(torch.int32)
+    b = ref.view(torch.int16).to(torch.int32)
+    # same-sign patterns are ordered like integers; treat +-0 as equal
+    ord_a = torch.where(a < 0, -(a & 0x7FFF), a)
+    ord_b = torch.where(b < 0, -(b & 0x7FFF), b)
+    assert int((ord_a - ord_b).abs().max()) <= 1, f"{what}: more than one ulp apart"

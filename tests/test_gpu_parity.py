@@ -1,0 +1,225 @@
+"""GPU parity: every libfq entry point against the oracle on the same seeded inputs, at sizes the
+oracle finishes in seconds that span many CTAs and a ragged tail, plus edge cases (one row, an
+empty batch, odd widths and misaligned views that take the scalar kernel, a token stride, a
+non-default fp8_max, partial rope). Tolerances: tests/parity.py.
+"""
+import pytest
+import torch
+
+import fp8_quant_memory_gb300 as fq
+from fp8_quant_memory_gb300 import workloads as wl
+from parity import (assert_codes_close, assert_dw_close, assert_scale_close, assert_storage_close,
+                    assert_within_one_ulp)
+
+pytestmark = pytest.mark.gpu
+
+DT = {"bf16": torch.bfloat16, "fp16": torch.float16, "fp32": torch.float32}
+
+
+def cuda(d):
+    return {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+
+def misalign(t: torch.Tensor) -> torch.Tensor:
+    """Same values at an address that is 2 bytes past a 16-byte boundary (forces the scalar path)."""
+    flat = torch.empty(t.numel() + 8, dtype=t.dtype, device=t.device)
+    view = flat[1: 1 + t.numel()].view(t.shape)
+    view.copy_(t)
+    return view
+
+
+# ----------------------------------------------------------------------------------- prologue
+PROLOGUE_CASES = [
+    # T, Hq, Hk, D, R, dtype, table, std, stride_extra, fp8_max
+    (37, 32, 8, 128, 128, "bf16", "fp32", 2.0, 0, 448.0),
+    (1, 32, 8, 128, 128, "bf16", "fp32", 2.0, 0, 448.0),
+    (129, 4, 2, 128, 128, "fp16", "fp32", 1.0, 0, 448.0),
+    (50, 6, 2, 128, 128, "bf16", "bf16", 1.0, 0, 448.0),
+    (33, 3, 1, 128, 128, "bf16", "fp32", 1.0, 3 * 128, 448.0),   # q/k slice of a QKV row
+    (17, 8, 0, 64, 64, "bf16", "fp32", 1.0, 0, 448.0),           # q only, D = 64
+    (21, 0, 4, 128, 64, "bf16", "fp32", 1.0, 0, 448.0),          # k only, partial rope
+    (19, 5, 3, 256, 128, "fp16", "fp16", 1.0, 0, 448.0),         # D = 256
+    (23, 4, 4, 128, 128, "bf16", "fp32", 1.0, 0, 240.0),         # fp8_max < 448
+    (13, 3, 2, 96, 40, "bf16", "fp32", 1.0, 0, 448.0),           # rope_dim not a multiple of 16
+    (11, 2, 2, 100, 50, "bf16", "bf16", 1.0, 0, 448.0),          # odd-ish width: scalar path
+    (9, 2, 1, 128, 0, "bf16", "fp32", 1.0, 0, 448.0),            # no rotation
+    (7, 40, 8, 128, 128, "bf16", "fp16", 1.0, 0, 448.0),         # table dtype != storage dtype
+]
+
+
+def _run_prologue(orc, case, seed=100, force_scalar=False):
+    T, Hq, Hk, D, R, dt, tdt, std, extra, fmax = case
+    H = Hq + Hk
+    ts = None if extra == 0 else H * D + extra
+    d = wl.qk_inputs(T, Hq, Hk, D, dt, tdt, seed=seed, std=std, rope_dim=R, token_stride=ts)
+    q_ref, s_ref = orc.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], Hq, Hk,
+                                          fp8_max=fmax, rope_dim=R)
+    g = cuda(d)
+    qk = misalign(g["qk"]) if force_scalar else g["qk"]
+    q, s = fq.qk_norm_rope_quant(qk, g["wq"], g["wk"], g["cos"], g["sin"], Hq, Hk, fp8_max=fmax, rope_dim=R)
+    torch.cuda.synchronize()
+    assert_scale_close(s, s_ref)
+    assert_codes_close(q, q_ref)
+
+
+@pytest.mark.parametrize("case", PROLOGUE_CASES, ids=lambda c: "T%d-%d+%d-D%d-R%d-%s-%s-x%d-m%g" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], c[6], c[8], c[9]))
+def test_prologue_parity(orc, cuda_ok, case):
+    _run_prologue(orc, case)
+
+
+@pytest.mark.parametrize("case", PROLOGUE_CASES[:4], ids=lambda c: "T%d-%d+%d-%s" % (c[0], c[1], c[2], c[5]))
+def test_prologue_parity_scalar_path(orc, cuda_ok, case):
+    _run_prologue(orc, case, seed=101, force_scalar=True)
+
+
+def test_prologue_empty_batch(cuda_ok):
+    d = cuda(wl.qk_inputs(1, 2, 2, 128, seed=1))
+    q, s = fq.qk_norm_rope_quant(d["qk"][:0], d["wq"], d["wk"], d["cos"][:0], d["sin"][:0], 2, 2)
+    torch.cuda.synchronize()
+    assert q.shape == (0, 4, 128) and s.shape == (0, 4)
+
+
+def test_prologue_outliers_and_huge_positions(orc, cuda_ok):
+    """Config-5-like statistics (1% outliers x50, positions up to 131072, theta 1e6), small T."""
+    d = wl.qk_inputs(64, 16, 4, 128, "bf16", "fp32", seed=102, std=1.0, theta=1e6, positions="uniform",
+                     outlier_frac=0.01)
+    q_ref, s_ref = orc.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], 16, 4)
+    g = cuda(d)
+    q, s = fq.qk_norm_rope_quant(g["qk"], g["wq"], g["wk"], g["cos"], g["sin"], 16, 4)
+    assert_scale_close(s, s_ref)
+    assert_codes_close(q, q_ref)
+
+
+def test_prologue_zero_rows(orc, cuda_ok):
+    """All-zero rows: scale = 1e-4/448 and every code +0."""
+    d = wl.qk_inputs(4, 2, 2, 128, seed=103)
+    d["qk"][1:3] = 0
+    q_ref, s_ref = orc.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], 2, 2)
+    g = cuda(d)
+    q, s = fq.qk_norm_rope_quant(g["qk"], g["wq"], g["wk"], g["cos"], g["sin"], 2, 2)
+    assert torch.equal(q.cpu()[1:3], torch.zeros_like(q.cpu()[1:3]))
+    assert torch.equal(s.cpu()[1:3], s_ref[1:3])
+    assert_codes_close(q, q_ref)
+
+
+# ----------------------------------------------------------------------------------- rmsnorm_rope_quant
+ROPE_QUANT_CASES = [
+    # M, N, R, dtype, table
+    (256, 512, 64, "bf16", "bf16"),    # the tiny workload
+    (1, 512, 64, "bf16", "bf16"),
+    (37, 192, 64, "fp16", "fp16"),
+    (300, 128, 128, "bf16", "fp32"),
+    (64, 4096, 128, "fp16", "fp16"),   # the fusion page's own demo width
+    (45, 1024, 256, "bf16", "bf16"),
+    (33, 100, 20, "bf16", "bf16"),     # scalar path
+    (29, 256, 0, "bf16", "bf16"),      # no rotation
+    (31, 512, 64, "bf16", "fp16"),     # mixed table dtype: scalar path
+]
+
+
+@pytest.mark.parametrize("want_y", [True, False])
+@pytest.mark.parametrize("case", ROPE_QUANT_CASES, ids=lambda c: "M%d-N%d-R%d-%s-%s" % c)
+def test_rmsnorm_rope_quant_parity(orc, cuda_ok, case, want_y):
+    M, N, R, dt, tdt = case
+    d = wl.rows_inputs(M, N, R, dt, tdt, seed=200 + M)
+    y_ref, q_ref, s_ref = orc.rmsnorm_rope_quant(d["x"], d["w"], d["cos"], d["sin"])
+    g = cuda(d)
+    y, q, s = fq.rmsnorm_rope_quant(g["x"], g["w"], g["cos"], g["sin"], want_y=True)
+    torch.cuda.synchronize()
+    assert_storage_close(y, y_ref)
+    # The codes and scales are the quantiser applied to the kernel's own y: exact.
+    q_own, s_own = orc.quant_rows(y.cpu())
+    assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
+    assert_codes_close(q, q_ref)
+    if not want_y:
+        _, q2, s2 = fq.rmsnorm_rope_quant(g["x"], g["w"], g["cos"], g["sin"], want_y=False)
+        assert torch.equal(q2, q) and torch.equal(s2, s)
+
+
+def test_rmsnorm_rope_quant_scalar_path_matches(orc, cuda_ok):
+    d = wl.rows_inputs(77, 512, 64, "bf16", "bf16", seed=250)
+    y_ref, q_ref, _ = orc.rmsnorm_rope_quant(d["x"], d["w"], d["cos"], d["sin"])
+    g = cuda(d)
+    y, q, s = fq.rmsnorm_rope_quant(misalign(g["x"]), g["w"], g["cos"], g["sin"])
+    assert_storage_close(y, y_ref)
+    q_own, s_own = orc.quant_rows(y.cpu())
+    assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
+
+
+# ----------------------------------------------------------------------------------- rmsnorm_rope
+@pytest.mark.parametrize("case", [(4096, 192, 64, "fp16", "fp16", 32), (100, 192, 64, "bf16", "fp32", 1),
+                                  (64, 256, 32, "bf16", "bf16", 1), (10, 70, 14, "fp16", "fp16", 1)],
+                         ids=lambda c: "M%d-N%d-R%d-%s-%s-h%d" % c)
+def test_rmsnorm_rope_parity(orc, cuda_ok, case):
+    M, N, R, dt, tdt, hpt = case
+    d = wl.rows_inputs(M, N, R, dt, tdt, seed=300 + M, heads_per_token=hpt)
+    y_ref = orc.rmsnorm_rope(d["x"], d["w"], d["cos"], d["sin"])
+    g = cuda(d)
+    y = fq.rmsnorm_rope(g["x"], g["w"], g["cos"], g["sin"])
+    assert_storage_close(y, y_ref)
+
+
+# ----------------------------------------------------------------------------------- rmsnorm fwd
+@pytest.mark.parametrize("case", [(64, 4096, "bf16"), (513, 128, "bf16"), (33, 2048, "fp16"), (1, 8, "bf16"),
+                                  (17, 100, "bf16"), (5, 5000, "fp16")], ids=lambda c: "M%d-N%d-%s" % c)
+def test_rmsnorm_fwd_parity(orc, cuda_ok, case):
+    M, N, dt = case
+    d = wl.rmsnorm_inputs(M, N, dt, seed=400 + M)
+    y_ref = orc.rmsnorm_fwd(d["x"], d["w"])
+    g = cuda(d)
+    y = fq.rmsnorm_fwd(g["x"], g["w"])
+    assert_storage_close(y, y_ref)
+
+
+def test_rmsnorm_fwd_empty(cuda_ok):
+    x = torch.empty((0, 64), dtype=torch.bfloat16, device="cuda")
+    y = fq.rmsnorm_fwd(x, torch.ones(64, dtype=torch.bfloat16, device="cuda"))
+    assert y.shape == (0, 64)
+
+
+# ----------------------------------------------------------------------------------- backward
+@pytest.mark.parametrize("case", [(257, 4096, "bf16"), (300, 128, "bf16"), (70, 1024, "fp16"),
+                                  (1, 512, "bf16"), (41, 100, "bf16"), (9, 8192, "bf16"), (600, 2048, "fp16")],
+                         ids=lambda c: "M%d-N%d-%s" % c)
+def test_rmsnorm_bwd_parity(orc, cuda_ok, case):
+    M, N, dt = case
+    d = wl.rmsnorm_inputs(M, N, dt, seed=500 + M)
+    dx_ref, dw_ref, dw32_ref = orc.rmsnorm_bwd(d["x"], d["w"], d["g"])
+    g = cuda(d)
+    dx, dw, dw32 = fq.rmsnorm_bwd(g["x"], g["w"], g["g"])
+    assert_storage_close(dx, dx_ref, "dx")
+    assert_dw_close(dw32, dw32_ref)
+    assert_within_one_ulp(dw, dw_ref)
+    assert torch.equal(dw.cpu(), dw32.cpu().to(dw.dtype))
+
+
+def test_rmsnorm_bwd_deterministic(cuda_ok):
+    d = cuda(wl.rmsnorm_inputs(1000, 4096, "bf16", seed=550))
+    a = fq.rmsnorm_bwd(d["x"], d["w"], d["g"])
+    b = fq.rmsnorm_bwd(d["x"], d["w"], d["g"])
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+def test_rmsnorm_bwd_empty_gives_zero_dw(cuda_ok):
+    x = torch.empty((0, 256), dtype=torch.bfloat16, device="cuda")
+    w = torch.ones(256, dtype=torch.bfloat16, device="cuda")
+    dx, dw, dw32 = fq.rmsnorm_bwd(x, w, x)
+    assert dx.shape == (0, 256) and torch.equal(dw32.cpu(), torch.zeros(256))
+
+
+def test_autograd_wrapper(orc, cuda_ok):
+    d = wl.rmsnorm_inputs(48, 256, "bf16", seed=560)
+    x = d["x"].cuda().requires_grad_(True)
+    w = d["w"].cuda().requires_grad_(True)
+    y = fq.rmsnorm(x, w)
+    y.backward(d["g"].cuda())
+    dx_ref, dw_ref, _ = orc.rmsnorm_bwd(d["x"], d["w"], d["g"])
+    assert_storage_close(y.detach(), orc.rmsnorm_fwd(d["x"], d["w"]))
+    assert_storage_close(x.grad, dx_ref, "dx")
+    assert_within_one_ulp(w.grad, dw_ref)
+
+
+def test_device_status_clean_after_runs(cuda_ok):
+    assert fq.device_status(clear=True) == 0
