@@ -49,11 +49,14 @@ int check_fp8_max(const char* fn, float fp8_max) {
   return FQ_OK;
 }
 
-int check_rope(const char* fn, int64_t N, int64_t R, const void* cos, const void* sin, int table_dtype) {
+// `empty`: the batch has no rows, so the tables are never read and may be null.
+int check_rope(const char* fn, int64_t N, int64_t R, const void* cos, const void* sin, int table_dtype,
+               bool empty) {
   if (R < 0 || R % 2 != 0 || R > N)
     return fail(FQ_ERR_INVALID_ARG, "%s: rope_dim must be even and in [0, %lld], got %lld", fn,
                 static_cast<long long>(N), static_cast<long long>(R));
-  if (R > 0 && (cos == nullptr || sin == nullptr)) return fail(FQ_ERR_INVALID_ARG, "%s: cos/sin are null", fn);
+  if (!empty && R > 0 && (cos == nullptr || sin == nullptr))
+    return fail(FQ_ERR_INVALID_ARG, "%s: cos/sin are null", fn);
   if (table_dtype != FQ_BF16 && table_dtype != FQ_FP16 && table_dtype != FQ_FP32)
     return fail(FQ_ERR_UNSUPPORTED, "%s: table dtype %d is not FQ_BF16, FQ_FP16 or FQ_FP32", fn, table_dtype);
   return FQ_OK;
@@ -113,10 +116,10 @@ int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, 
                    cudaStream_t stream) {
   const char* fn = "fq_rmsnorm_fwd";
   if (int rc = check_common(fn, dtype, eps)) return rc;
-  if (x == nullptr || w == nullptr || y == nullptr) return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
     return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
   if (M == 0) return ok();
+  if (x == nullptr || w == nullptr || y == nullptr) return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
   fq::RowArgs a{};
   a.x = x;
   a.wq = a.wk = w;
@@ -136,11 +139,11 @@ int fq_rmsnorm_rope(const void* x, const void* w, const void* cos, const void* s
                     cudaStream_t stream) {
   const char* fn = "fq_rmsnorm_rope";
   if (int rc = check_common(fn, dtype, eps)) return rc;
-  if (x == nullptr || w == nullptr || y == nullptr) return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
     return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
-  if (int rc = check_rope(fn, N, rope_dim, cos, sin, table_dtype)) return rc;
+  if (int rc = check_rope(fn, N, rope_dim, cos, sin, table_dtype, M == 0)) return rc;
   if (M == 0) return ok();
+  if (x == nullptr || w == nullptr || y == nullptr) return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
   fq::RowArgs a{};
   a.x = x;
   a.wq = a.wk = w;
@@ -163,12 +166,12 @@ int fq_rmsnorm_rope_quant(const void* x, const void* w, const void* cos, const v
   const char* fn = "fq_rmsnorm_rope_quant";
   if (int rc = check_common(fn, dtype, eps)) return rc;
   if (int rc = check_fp8_max(fn, fp8_max)) return rc;
-  if (x == nullptr || w == nullptr || q == nullptr || scale == nullptr)
-    return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
     return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
-  if (int rc = check_rope(fn, N, rope_dim, cos, sin, table_dtype)) return rc;
+  if (int rc = check_rope(fn, N, rope_dim, cos, sin, table_dtype, M == 0)) return rc;
   if (M == 0) return ok();
+  if (x == nullptr || w == nullptr || q == nullptr || scale == nullptr)
+    return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
   fq::RowArgs a{};
   a.x = x;
   a.wq = a.wk = w;
@@ -194,8 +197,6 @@ int fq_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, 
   const char* fn = "fq_qk_norm_rope_quant";
   if (int rc = check_common(fn, dtype, eps)) return rc;
   if (int rc = check_fp8_max(fn, fp8_max)) return rc;
-  if (qk == nullptr || wq == nullptr || wk == nullptr || q_out == nullptr || scale == nullptr)
-    return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (T < 0 || Hq < 0 || Hk < 0 || Hq + Hk < 1 || D < 1 || D > kMaxWidth || Hq + Hk > kMaxWidth)
     return fail(FQ_ERR_INVALID_ARG, "%s: need T >= 0, Hq, Hk >= 0, Hq + Hk >= 1, D >= 1", fn);
   const int64_t H = Hq + Hk;
@@ -203,8 +204,10 @@ int fq_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, 
     return fail(FQ_ERR_INVALID_ARG, "%s: token_stride %lld < (Hq+Hk)*D = %lld", fn,
                 static_cast<long long>(token_stride), static_cast<long long>(H * D));
   if (T > kMaxRows / H) return fail(FQ_ERR_INVALID_ARG, "%s: T*(Hq+Hk) must be < 2^31", fn);
-  if (int rc = check_rope(fn, D, rope_dim, cos, sin, table_dtype)) return rc;
+  if (int rc = check_rope(fn, D, rope_dim, cos, sin, table_dtype, T == 0)) return rc;
   if (T == 0) return ok();
+  if (qk == nullptr || wq == nullptr || wk == nullptr || q_out == nullptr || scale == nullptr)
+    return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
   fq::RowArgs a{};
   a.x = qk;
   a.wq = wq;
@@ -235,10 +238,10 @@ int fq_rmsnorm_bwd(const void* x, const void* w, const void* grad_y, void* dx, v
                    cudaStream_t stream) {
   const char* fn = "fq_rmsnorm_bwd";
   if (int rc = check_common(fn, dtype, eps)) return rc;
-  if (x == nullptr || w == nullptr || grad_y == nullptr || dx == nullptr || dw == nullptr)
-    return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
   if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
     return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
+  if (w == nullptr || dw == nullptr || (M > 0 && (x == nullptr || grad_y == nullptr || dx == nullptr)))
+    return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
   const size_t need = fq_rmsnorm_bwd_workspace_bytes(M, N);
   if (need > 0 && (workspace == nullptr || workspace_bytes < need))
     return fail(FQ_ERR_INVALID_ARG, "%s: workspace of %zu bytes needed, %zu given", fn, need,

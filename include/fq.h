@@ -110,7 +110,7 @@ int fq_rmsnorm_rope_quant(const void* x, const void* w, const void* cos, const v
  * qk: dtype, token_stride >= H*D elements between consecutive tokens (H*D when packed; larger for
  *     the q/k slice of a fused QKV projection row).
  * wq, wk: [D] dtype. cos, sin: [T, R/2] table_dtype. q_out: [T, H, D] uint8. scale: [T, H] fp32.
- * R = rope_dim: even, 0 <= R <= D. T = 0 is a no-op.
+ * R = rope_dim: even, 0 <= R <= D. T = 0 is a no-op (pointers may then be null).
  */
 int fq_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, const void* wk,
                           const void* cos, const void* sin, uint8_t* q_out, float* scale, int64_t T,
