@@ -29,6 +29,7 @@ SIGNATURES = {
                                      _int, _int, _f32, _f32, _vp]),
     "fq_rmsnorm_bwd_workspace_bytes": (_sz, [_i64, _i64]),
     "fq_rmsnorm_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _int, _f32, _vp]),
+    "fq_rmsnorm_bwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _f32, _vp]),
 }
 
 _lib = None

@@ -13,14 +13,19 @@ namespace {
 
 thread_local std::string g_err;
 
-int fail(int code, const char* fmt, ...) {
+int vfail(int code, const char* fmt, va_list ap) {
   char buf[512];
-  va_list ap;
-  va_start(ap, fmt);
   vsnprintf(buf, sizeof(buf), fmt, ap);
-  va_end(ap);
   g_err = buf;
   return code;
+}
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  const int rc = vfail(code, fmt, ap);
+  va_end(ap);
+  return rc;
 }
 
 int ok() {
@@ -84,6 +89,14 @@ int launch_rows(const char* fn, const fq::RowArgs& a, int mode, int dtype, int t
 }  // namespace
 
 namespace fq {
+
+int set_error(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  const int rc = vfail(code, fmt, ap);
+  va_end(ap);
+  return rc;
+}
 
 int sm_count() {
   static int cache[128] = {0};

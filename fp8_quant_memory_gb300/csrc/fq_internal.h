@@ -74,4 +74,7 @@ unsigned int* device_status_ptr();
 
 int sm_count();
 
+// Records a printf-style message for fq_last_error() on this thread and returns `code`.
+int set_error(int code, const char* fmt, ...);
+
 }  // namespace fq

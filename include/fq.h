@@ -138,6 +138,30 @@ int fq_rmsnorm_bwd(const void* x, const void* w, const void* grad_y, void* dx, v
                    void* workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype, float eps,
                    cudaStream_t stream);
 
+/* Size of the library's built-in scratch used by fq_rmsnorm_bwd_noalloc (4 MiB of device memory per
+ * GPU that loads the library). It fits fq_rmsnorm_bwd_workspace_bytes(M, N) for N <= 4096 at any M,
+ * and for wider rows while M is small enough (at most FQ_NOALLOC_SCRATCH_BYTES / (4 * N) chunks). */
+#define FQ_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+
+/*
+ * RMSNorm backward that allocates nothing and takes no workspace. The tutorial pages have no
+ * counterpart; it exists for callers that cannot allocate device memory or pass a workspace: for
+ * example a plugin inside a framework that owns all device buffers through its own pool and hands
+ * the plugin only its tensors, or a latency-critical loop that must never call cudaMalloc (which
+ * can synchronise the whole device).
+ * Same arguments, results and error rules as fq_rmsnorm_bwd, minus the workspace: the dw partial
+ * sums go to a fixed array in the library's own device memory (FQ_NOALLOC_SCRATCH_BYTES per device,
+ * held until the process exits). Problems whose fq_rmsnorm_bwd_workspace_bytes(M, N) exceeds that
+ * size are rejected with FQ_ERR_INVALID_ARG.
+ * The first call on each device looks up that array's device address (with the device current);
+ * make that first call before any stream capture. Every call shares the one array and leaves its
+ * contents behind (nothing in it needs clearing: each call overwrites what it reads), so calls
+ * that may overlap on the GPU -- on different streams, or from different threads -- race on it and
+ * must be serialised by the caller.
+ */
+int fq_rmsnorm_bwd_noalloc(const void* x, const void* w, const void* grad_y, void* dx, void* dw,
+                           float* dw_f32, int64_t M, int64_t N, int dtype, float eps, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
