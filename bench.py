@@ -41,7 +41,7 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 T_TOK, HQ, HK, D = 4096, 32, 8, 128
 WORKLOAD = "qk_norm_rope_quant T=4096 Hq=32 Hk=8 D=128 rope_dim=128 bf16->e4m3 fp32-tables"
-KERNEL_SOURCES = ["fp8_quant_memory_gb300/csrc/fq_rows.cu", "fp8_quant_memory_gb300/csrc/fq_device.cuh"]
+KERNEL_SOURCES = ["fp8_quant_memory_gb300/csrc/fq_prologue.cu", "fp8_quant_memory_gb300/csrc/fq_device.cuh"]
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "qk_norm_rope_quant_4k.md")
 
 
@@ -554,7 +554,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
-                     "traffic": profiled_traffic(), "kernel": "rows_vec_kernel<bf16,float,QK,8,0,1>",
+                     "traffic": profiled_traffic(), "kernel": "prologue_tma_kernel<bf16,float>",
                      "us_per_launch": round(per_launch_us, 3)},
         "gpu_launches": args.steps * case.kernels_per_step,
         "clocks": clocks,

@@ -4,6 +4,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <string>
 
 #include "fq.h"
@@ -81,6 +82,12 @@ int launch_rows(const char* fn, const fq::RowArgs& a, int mode, int dtype, int t
   if (a.y != nullptr) vec = vec && aligned(a.y, 16);
   if (a.q != nullptr) vec = vec && aligned(a.q, 8);
   if (a.scale != nullptr) vec = vec && aligned(a.scale, 4);
+  // FQ_PROLOGUE_KERNEL=generic selects the generic vectorised kernel for the prologue instead of the
+  // TMA-fed one (a diagnostic switch: both compute the same result).
+  const char* pick = std::getenv("FQ_PROLOGUE_KERNEL");
+  const bool tma_ok = !(pick != nullptr && std::string(pick) == "generic");
+  if (vec && mode == fq::MODE_QK && tma_ok && fq::launch_prologue_tma(a, dtype, table_dtype, s))
+    return check_launch(fn);
   if (!(vec && fq::launch_rows_vector(a, mode, dtype, table_dtype, s)))
     fq::launch_rows_scalar(a, mode, dtype, table_dtype, s);
   return check_launch(fn);

@@ -42,6 +42,10 @@ struct RowArgs {
 // Returns false (launching nothing) when the shape has no instantiation.
 bool launch_rows_vector(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s);
 
+// TMA-fed persistent prologue kernel (MODE_QK, N == R == 128, 16-byte aligned token stride, table
+// dtype fp32 or the storage dtype). Returns false (launching nothing) when it does not apply.
+bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s);
+
 // Scalar path: any N >= 1, even R, any alignment, any dtype combination.
 void launch_rows_scalar(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s);
 

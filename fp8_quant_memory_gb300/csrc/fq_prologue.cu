@@ -1,0 +1,459 @@
+// fq_prologue.cu -- the QK-Norm + RoPE + FP8 attention prologue ("case_norm_rope_quant.py" (Ch.28),
+// module docstring) for head_dim 128 with the whole head rotated, as a TMA-fed persistent kernel.
+//
+// Data movement. Every CTA owns one contiguous range of (token, head) rows, balanced to the row.
+// One producer lane streams that range through a ring of shared-memory stages of 64 rows: two 2-D
+// tensor TMA loads (cp.async.bulk.tensor, 128-byte swizzle) bring the first and second halves of the
+// 64 rows (the NeoX "lo" and "hi" halves, 8 KB each in bf16) and two 1-D bulk copies bring the cos
+// and sin rows of the tokens those rows belong to; an mbarrier counts the bytes. Bytes in flight do
+// not depend on registers or occupancy. x is read from HBM once; each table row once per stage that
+// needs it (L2 serves repeats); the two norm weights once per CTA (shared memory, fp32, in a
+// lane-permuted layout). Codes and scales go straight to global memory with evict-first stores.
+//
+// Work layout. Eight consumer warps, four lanes per row (eight rows per warp, one row per lane group
+// per stage). Lane j of a row holds the NeoX pairs 16j..16j+15 of both halves, so every pair
+// (p, p+64) sits in one thread: no shuffle and no shared-memory round trip for the rotation. The
+// swizzle makes the four lanes' 16-byte reads of two neighbouring rows hit disjoint banks. Each
+// lane stores its 16 contiguous codes of each half with one 16-byte store.
+//
+// Arithmetic (same cast points and roundings as the oracle and the generic row kernel):
+//   ss = sum x^2 (fp32) -> rstd = 1/sqrt(ss/128 + eps)  (ss/128 is exact as ss * 2^-7; the square
+//   root and the reciprocal are correctly rounded); n = (x*rstd)*w; lo' = lo*c - hi*s,
+//   hi' = hi*c + lo*s; amax -> scale = max(amax, 1e-4)/fp8_max (correctly rounded);
+//   q = e4m3(RN(y/scale)) from the correctly rounded reciprocal and one Markstein correction.
+//
+// Waits are bounded: a wait that has not completed after ~1 s of %globaltimer time sets bit 0 of
+// the device status word and the kernel stops issuing and consuming work (waiting, again bounded,
+// for the copies it has in flight) instead of trapping.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "fq_device.cuh"
+#include "fq_internal.h"
+
+namespace fq {
+namespace {
+
+constexpr int kD = 128;                                  // head_dim handled here
+constexpr int kLPR = 4;                                  // lanes per row
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;      // + one producer warp
+constexpr int kStageRows = kConsumerWarps * (32 / kLPR); // 64
+constexpr int kHalfTile = kStageRows * (kD / 2) * 2;     // one half of 64 rows in a 16-bit dtype: 8 KB
+constexpr uint64_t kWaitLimitNs = 1000000000ull;         // 1 s
+
+struct PrologueArgs {
+  const void* wq;
+  const void* wk;
+  const void* cos;
+  const void* sin;
+  uint8_t* q;
+  float* scale;
+  unsigned int* status;
+  uint64_t magic;        // t = (r * magic) >> shift == r / H for r < 2^31
+  int32_t shift;
+  int32_t rows;          // T * H
+  int32_t H, Hq;
+  float inv_h;           // RN(1/H), for floor(x / H) with x < 2^21
+  float eps, fp8_max, rcp_fp8_max;
+  int32_t stages;        // ring depth
+  int32_t stage_bytes;   // 2 half tiles + 2 table blocks, multiple of 1024
+  int32_t tab_block;     // bytes of one table block (cos or sin)
+};
+
+// ------------------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity to complete; false if ~1 s passed first.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1; i != 0; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds16(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ float4 lds16f(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint32_t word(const uint4& v, int k) {
+  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+}
+
+// Table entries 8m..8m+7 of the lane's 16 (pairs 16j+8m..16j+8m+7 of one table row) -> 4 float2.
+template <typename TT>
+__device__ __forceinline__ void lds_table8(uint32_t addr, int m, float2 (&v)[4]) {
+  if constexpr (sizeof(TT) == 4) {
+    const float4 f0 = lds16f(addr + 32 * m), f1 = lds16f(addr + 32 * m + 16);
+    v[0] = make_float2(f0.x, f0.y);
+    v[1] = make_float2(f0.z, f0.w);
+    v[2] = make_float2(f1.x, f1.y);
+    v[3] = make_float2(f1.z, f1.w);
+  } else {
+    const uint4 u = lds16(addr + 16 * m);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) v[e] = Elem<TT>::unpack(word(u, e));
+  }
+}
+
+__device__ __forceinline__ void flag_failure(unsigned int* status) {
+  if (status != nullptr) atomicOr(status, 1u);
+}
+
+// ------------------------------------------------------------------------------ the kernel
+template <typename T, typename TT>
+__global__ void __launch_bounds__(kThreads, 2)
+    prologue_tma_kernel(const __grid_constant__ CUtensorMap xmap, const PrologueArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  // The 128-byte swizzle repeats every 1024 bytes: align the ring to 1024.
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  const int S = a.stages;
+  float* wsm = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * a.stage_bytes);  // 2 x 128 floats
+  uint64_t* full = reinterpret_cast<uint64_t*>(wsm + 2 * kD);
+  uint64_t* empty = full + S;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int32_t r0 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x) * a.rows) / gridDim.x);
+  const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x + 1) * a.rows) / gridDim.x);
+  const int nst = (r1 - r0 + kStageRows - 1) / kStageRows;
+  constexpr int kTabRow = (kD / 2) * static_cast<int>(sizeof(TT));  // bytes of one table row
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  // Programmatic dependent launch: let the next kernel in the stream start its own set-up now, and
+  // wait for the previous one to finish (and its writes to be visible) before touching global memory.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (warp == kConsumerWarps) {
+    // ---------------------------------------------------------------- producer (one lane)
+    if (lane != 0) return;
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
+    int k = 0;
+    bool ok = true;
+    for (; k < nst; ++k) {
+      const int slot = k % S;
+      if (k >= S && !mbar_wait(&empty[slot], static_cast<uint32_t>((k / S) - 1) & 1u)) {
+        ok = false;
+        break;
+      }
+      const int32_t rs = r0 + k * kStageRows;
+      const int32_t re = min(rs + kStageRows, r1);
+      const int32_t tf = static_cast<int32_t>((static_cast<uint64_t>(rs) * a.magic) >> a.shift);
+      const int32_t tl = static_cast<int32_t>((static_cast<uint64_t>(re - 1) * a.magic) >> a.shift);
+      const uint32_t tbytes = static_cast<uint32_t>(tl - tf + 1) * kTabRow;
+      unsigned char* st = smem + static_cast<size_t>(slot) * a.stage_bytes;
+      // Rows past the end of the tensor are zero-filled and still counted in full.
+      mbar_arrive_expect_tx(&full[slot], 2u * kHalfTile + 2u * tbytes);
+      tma_load_2d(st, &xmap, 0, rs, &full[slot]);
+      tma_load_2d(st + kHalfTile, &xmap, kD / 2, rs, &full[slot]);
+      bulk_g2s(st + 2 * kHalfTile, static_cast<const unsigned char*>(a.cos) + static_cast<int64_t>(tf) * kTabRow,
+               tbytes, &full[slot]);
+      bulk_g2s(st + 2 * kHalfTile + a.tab_block,
+               static_cast<const unsigned char*>(a.sin) + static_cast<int64_t>(tf) * kTabRow, tbytes, &full[slot]);
+    }
+    if (!ok) {
+      flag_failure(a.status);
+      // Let the copies already issued land before this CTA's shared memory goes away.
+      for (int j = max(0, k - S); j < k; ++j)
+        if (!mbar_wait(&full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  // Weights as fp32, permuted so that lane j's k-th float4 of a half sits at ((set*2+half)*4+k)*4+j:
+  // the four lanes of a row read 64 contiguous bytes per load. Loaded while the first stages are in
+  // flight; only the consumer warps synchronise on it.
+  for (int i = threadIdx.x; i < 2 * kD; i += kConsumerWarps * 32) {
+    const int set = i / kD, c = i % kD;
+    const int half = c / 64, within = c % 64;
+    const int jj = within / 16, kk = (within % 16) / 4, comp = within % 4;
+    wsm[((((set * 2 + half) * 4 + kk) * 4 + jj) * 4) + comp] = Elem<T>::load1(set ? a.wk : a.wq, c);
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+  const int grp = lane >> 2;         // row within the warp's eight
+  const int j = lane & 3;            // pairs 16j..16j+15 of each half
+  const int l = warp * 8 + grp;      // row within the stage
+  const int sw = l & 7;              // 128-byte swizzle phase of this row
+  const uint32_t xoff0 = l * 128 + (((2 * j) ^ sw) << 4);
+  const uint32_t xoff1 = l * 128 + (((2 * j + 1) ^ sw) << 4);
+  const uint32_t wbase = smem_addr(wsm) + j * 16;
+  const bool clamp = a.fp8_max != 448.0f;
+
+  for (int k = 0; k < nst; ++k) {
+    const int slot = k % S;
+    if (!mbar_wait(&full[slot], static_cast<uint32_t>(k / S) & 1u)) {
+      flag_failure(a.status);
+      return;
+    }
+    const uint32_t st = smem_addr(smem + static_cast<size_t>(slot) * a.stage_bytes);
+    const int32_t rs = r0 + k * kStageRows;
+    const bool live = l < r1 - rs;
+    const int32_t tf = static_cast<int32_t>((static_cast<uint64_t>(rs) * a.magic) >> a.shift);
+    const int32_t xh = (rs - tf * a.H) + l;                    // head index counted from token tf
+    const int32_t dt = static_cast<int32_t>((static_cast<float>(xh) + 0.5f) * a.inv_h);  // floor(xh / H)
+    const int32_t h = xh - dt * a.H;
+    const int32_t r = rs + l;
+
+    const uint4 xl0 = lds16(st + xoff0), xl1 = lds16(st + xoff1);
+    const uint4 xh0 = lds16(st + kHalfTile + xoff0), xh1 = lds16(st + kHalfTile + xoff1);
+    const uint32_t tcos = st + 2 * kHalfTile + dt * kTabRow + j * (16 * static_cast<int>(sizeof(TT)));
+    const uint32_t wa = wbase + (h >= a.Hq ? 512u : 0u);  // the k weights follow the q weights
+
+    float2 lo[8], hi[8];
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      lo[e] = Elem<T>::unpack(word(xl0, e));
+      lo[4 + e] = Elem<T>::unpack(word(xl1, e));
+      hi[e] = Elem<T>::unpack(word(xh0, e));
+      hi[4 + e] = Elem<T>::unpack(word(xh1, e));
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      acc0 = fma2(lo[i], lo[i], acc0);
+      acc1 = fma2(hi[i], hi[i], acc1);
+    }
+    const float2 acc = add2(acc0, acc1);
+    const float ss = group_sum<kLPR>(acc.x + acc.y);
+    // ss/128 is exact as a multiplication by 2^-7; sqrt and reciprocal correctly rounded.
+    const float rstd = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, 0.0078125f), a.eps)));
+    const float2 rstd2 = splat2(rstd);
+    float amax = 0.f;
+    // Normalise and rotate eight pairs at a time (weights and table entries loaded per half-chunk).
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      float2 wl[4], wh[4], c[4], s[4];
+#pragma unroll
+      for (int q4 = 0; q4 < 2; ++q4) {
+        const float4 fl = lds16f(wa + (2 * m + q4) * 64);
+        const float4 fh = lds16f(wa + 256 + (2 * m + q4) * 64);
+        wl[2 * q4] = make_float2(fl.x, fl.y);
+        wl[2 * q4 + 1] = make_float2(fl.z, fl.w);
+        wh[2 * q4] = make_float2(fh.x, fh.y);
+        wh[2 * q4 + 1] = make_float2(fh.z, fh.w);
+      }
+      lds_table8<TT>(tcos, m, c);
+      lds_table8<TT>(tcos + a.tab_block, m, s);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int i = 4 * m + e;
+        const float2 nl = mul2(mul2(lo[i], rstd2), wl[e]);
+        const float2 nh = mul2(mul2(hi[i], rstd2), wh[e]);
+        lo[i] = add2(mul2(nl, c[e]), neg2(mul2(nh, s[e])));
+        hi[i] = add2(mul2(nh, c[e]), mul2(nl, s[e]));
+        amax = absmax4(amax, lo[i], hi[i]);
+      }
+    }
+    amax = fmaxf(group_max<kLPR>(amax), 1e-4f);
+    // scale = RN(amax / fp8_max) via the correctly rounded reciprocal and one correction.
+    const float s0 = __fmul_rn(amax, a.rcp_fp8_max);
+    const float sc = __fmaf_rn(__fmaf_rn(-s0, a.fp8_max, amax), a.rcp_fp8_max, s0);
+    const float rc = __frcp_rn(sc);
+    uint32_t ql[4], qh[4];
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      float2 a0 = div2_by(lo[i], sc, rc), a1 = div2_by(lo[i + 1], sc, rc);
+      float2 b0 = div2_by(hi[i], sc, rc), b1 = div2_by(hi[i + 1], sc, rc);
+      if (clamp) {
+        a0 = make_float2(clamp_abs(a0.x, a.fp8_max), clamp_abs(a0.y, a.fp8_max));
+        a1 = make_float2(clamp_abs(a1.x, a.fp8_max), clamp_abs(a1.y, a.fp8_max));
+        b0 = make_float2(clamp_abs(b0.x, a.fp8_max), clamp_abs(b0.y, a.fp8_max));
+        b1 = make_float2(clamp_abs(b1.x, a.fp8_max), clamp_abs(b1.y, a.fp8_max));
+      }
+      ql[i / 2] = e4m3x2(a0) | (e4m3x2(a1) << 16);
+      qh[i / 2] = e4m3x2(b0) | (e4m3x2(b1) << 16);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the stage's shared memory
+    if (live) {
+      uint8_t* qrow = a.q + static_cast<int64_t>(r) * kD;
+      st_stream16(qrow + 16 * j, make_uint4(ql[0], ql[1], ql[2], ql[3]));
+      st_stream16(qrow + 64 + 16 * j, make_uint4(qh[0], qh[1], qh[2], qh[3]));
+      if (j == 0) a.scale[r] = sc;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
+  if (a.N != kD || a.R != kD) return false;
+  if (a.rows <= 0 || a.rows > 0x7fffffffLL) return false;
+  if (a.token_stride != static_cast<int64_t>(a.H) * kD) return false;  // packed [T, H, 128] only
+  if (a.H + kStageRows >= (1 << 21)) return false;
+  if (!(table_dtype == DT_FP32 || table_dtype == dtype)) return false;
+  if ((reinterpret_cast<uintptr_t>(a.q) & 15u) != 0) return false;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+  if (encode == nullptr) return false;
+  const int tsz = (table_dtype == DT_FP32) ? 4 : 2;
+
+  CUtensorMap xmap;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(a.rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box[2] = {kD / 2, kStageRows};
+  const cuuint32_t estr[2] = {1, 1};
+  if (encode(&xmap, dtype == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+             const_cast<void*>(a.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+
+  PrologueArgs p{};
+  p.wq = a.wq;
+  p.wk = a.wk;
+  p.cos = a.cos;
+  p.sin = a.sin;
+  p.q = a.q;
+  p.scale = a.scale;
+  p.status = device_status_ptr();
+  p.rows = static_cast<int32_t>(a.rows);
+  p.H = a.H;
+  p.Hq = a.Hq;
+  p.inv_h = 1.0f / static_cast<float>(a.H);
+  p.eps = a.eps;
+  p.fp8_max = a.fp8_max;
+  p.rcp_fp8_max = static_cast<float>(1.0 / static_cast<double>(a.fp8_max));
+  // r / H as (r * magic) >> shift for every r < 2^31: shift = 31 + ceil(log2 H), magic = ceil(2^shift / H).
+  int lg = 0;
+  while ((1LL << lg) < a.H) ++lg;
+  p.shift = 31 + lg;
+  p.magic = static_cast<uint64_t>(((static_cast<unsigned __int128>(1) << p.shift) + a.H - 1) / a.H);
+  const int tab_rows = (kStageRows - 1) / a.H + 2;  // tokens one 64-row stage can touch
+  p.tab_block = ((tab_rows * (kD / 2) * tsz) + 127) & ~127;
+  p.stage_bytes = ((2 * kHalfTile + 2 * p.tab_block) + 1023) & ~1023;
+  // Ring depth: as many stages (up to 6) as fit two CTAs per SM in GB300's 228 KB of shared memory.
+  const int fixed = 1024 + 2 * kD * static_cast<int>(sizeof(float)) + 2 * 8 * static_cast<int>(sizeof(uint64_t));
+  p.stages = (110 * 1024 - fixed) / p.stage_bytes;
+  if (p.stages > 6) p.stages = 6;
+  if (p.stages < 2) p.stages = 2;
+  const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + 2 * kD * sizeof(float) +
+                      2 * p.stages * sizeof(uint64_t);
+  if (smem > 227 * 1024) return false;
+
+  void (*kern)(const CUtensorMap, const PrologueArgs);
+  if (dtype == DT_BF16)
+    kern = (tsz == 4) ? prologue_tma_kernel<__nv_bfloat16, float> : prologue_tma_kernel<__nv_bfloat16, __nv_bfloat16>;
+  else
+    kern = (tsz == 4) ? prologue_tma_kernel<__half, float> : prologue_tma_kernel<__half, __half>;
+  static int configured[4] = {0, 0, 0, 0};
+  const int key = (dtype == DT_BF16 ? 0 : 2) + (tsz == 4 ? 0 : 1);
+  if (configured[key] < static_cast<int>(smem)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+      return false;
+    configured[key] = static_cast<int>(smem);
+  }
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  const int64_t want = (a.rows + kStageRows - 1) / kStageRows;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
+  const int grid = static_cast<int>(want < cap ? want : cap);
+  // Programmatic stream serialisation: this grid may be scheduled while the previous kernel in the
+  // stream drains; griddepcontrol.wait inside the kernel orders every global access after it.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, xmap, p) == cudaSuccess;
+}
+
+}  // namespace fq

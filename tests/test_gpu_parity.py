@@ -223,3 +223,48 @@ def test_autograd_wrapper(orc, cuda_ok):
 
 def test_device_status_clean_after_runs(cuda_ok):
     assert fq.device_status(clear=True) == 0
+
+
+# ----------------------------------------------------------------------------------- TMA prologue kernel
+TMA_CASES = [
+    # T, Hq, Hk, dtype, table, stride_extra
+    (4096, 32, 8, "bf16", "fp32", 0),     # the measured workload
+    (1, 1, 0, "bf16", "fp32", 0),         # a single row
+    (3, 1, 0, "fp16", "fp32", 0),         # H = 1: every row of a stage is a different token
+    (97, 1, 1, "bf16", "bf16", 0),        # H = 2, 16-bit tables
+    (50, 64, 8, "bf16", "fp32", 0),       # large H, stages span token boundaries
+    (211, 5, 3, "fp16", "fp16", 0),       # rows not a multiple of the 64-row stage
+    (65, 3, 1, "bf16", "fp32", 2 * 128),  # q/k slice of a wider row: one copy per token segment
+    (300, 6, 2, "bf16", "fp32", 8),       # odd token stride (still 16-byte aligned)
+]
+
+
+@pytest.mark.parametrize("kernel", ["tma", "generic"])
+@pytest.mark.parametrize("case", TMA_CASES, ids=lambda c: "T%d-%d+%d-%s-%s-x%d" % c)
+def test_prologue_tma_kernel_parity(orc, cuda_ok, monkeypatch, case, kernel):
+    T, Hq, Hk, dt, tdt, extra = case
+    if kernel == "generic":
+        monkeypatch.setenv("FQ_PROLOGUE_KERNEL", "generic")
+    else:
+        monkeypatch.delenv("FQ_PROLOGUE_KERNEL", raising=False)
+    H = Hq + Hk
+    ts = None if extra == 0 else H * 128 + extra
+    d = wl.qk_inputs(T, Hq, Hk, 128, dt, tdt, seed=700 + T, std=2.0, token_stride=ts)
+    q_ref, s_ref = orc.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], Hq, Hk)
+    g = cuda(d)
+    q, s = fq.qk_norm_rope_quant(g["qk"], g["wq"], g["wk"], g["cos"], g["sin"], Hq, Hk)
+    torch.cuda.synchronize()
+    assert_scale_close(s, s_ref)
+    assert_codes_close(q, q_ref)
+    assert fq.device_status(clear=True) == 0
+
+
+def test_prologue_tma_matches_generic_kernel(cuda_ok, monkeypatch):
+    """Both kernels on identical inputs: scales within 1e-6 relative, codes at most one step apart."""
+    d = cuda(wl.qk_inputs(777, 32, 8, 128, "bf16", "fp32", seed=790, std=2.0))
+    monkeypatch.delenv("FQ_PROLOGUE_KERNEL", raising=False)
+    q1, s1 = fq.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], 32, 8)
+    monkeypatch.setenv("FQ_PROLOGUE_KERNEL", "generic")
+    q2, s2 = fq.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], 32, 8)
+    assert_scale_close(s1, s2.cpu(), rel=1e-6)
+    assert_codes_close(q1, q2.cpu())
