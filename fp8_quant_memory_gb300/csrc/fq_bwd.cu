@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(kThreads) bwd_stage1_kernel(const BwdArgs a, i
           const float2 xn = mul2(Elem<T>::unpack(word(xv[b][k], e)), rstd2);
           const float2 gf = Elem<T>::unpack(word(gv[b][k], e));
           const float2 gw = mul2(gf, wf[k][e]);
-          const float2 d = add2(gw, neg2(mul2(xn, c2)));
+          const float2 d = sub2(gw, mul2(xn, c2));
           pk[e] = Elem<T>::pack(mul2(rstd2, d));
           acc[k][e] = fma2(gf, xn, acc[k][e]);
         }

@@ -103,6 +103,18 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) { return __fmul2_rn(a
 __device__ __forceinline__ float2 add2(float2 a, float2 b) { return __fadd2_rn(a, b); }
 __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
 __device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+// a - b per component (sub.rn.f32x2: one instruction, no separate negation).
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "sub.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
 __device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
 
 // Quotient y / s rounded to nearest, given r = RN(1/s) (correctly rounded reciprocal):
@@ -111,7 +123,7 @@ __device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
 // Dev. 34(1), 1990; Muller et al., Handbook of Floating-Point Arithmetic, ch. 4).
 __device__ __forceinline__ float2 div2_by(float2 y, float s, float r) {
   const float2 q0 = mul2(y, splat2(r));
-  const float2 e = fma2(neg2(q0), splat2(s), y);
+  const float2 e = fma2(q0, splat2(-s), y);  // y - q0*s, exact: (-q0)*s == q0*(-s)
   return fma2(e, splat2(r), q0);
 }
 

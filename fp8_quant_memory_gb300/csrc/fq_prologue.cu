@@ -61,6 +61,7 @@ struct PrologueArgs {
   int32_t stages;        // ring depth
   int32_t stage_bytes;   // 2 half tiles + 2 table blocks, multiple of 1024
   int32_t tab_block;     // bytes of one table block (cos or sin)
+  int32_t depth;         // the producer keeps at most this many stages in flight
 };
 
 // ------------------------------------------------------------------------------ PTX wrappers
@@ -167,6 +168,109 @@ __device__ __forceinline__ void flag_failure(unsigned int* status) {
   if (status != nullptr) atomicOr(status, 1u);
 }
 
+// One (token, head) row of a stage, by the four lanes of a lane group: shared-memory x, table and
+// weight entries in, e4m3 codes and the fp32 scale out. `l` is the row within the stage.
+template <typename T, typename TT>
+__device__ __forceinline__ void prologue_row(const PrologueArgs& a, uint32_t st, int l, int j, int rev,
+                                             uint32_t wbase, int32_t rs, int32_t r1, int32_t tf, bool clamp) {
+  constexpr int kTabRow = (kD / 2) * static_cast<int>(sizeof(TT));
+  const int sw = l & 7;  // 128-byte swizzle phase of this row
+  const bool live = l < r1 - rs;
+  const int32_t xh = (rs - tf * a.H) + l;                                             // head index from token tf
+  const int32_t dt = static_cast<int32_t>((static_cast<float>(xh) + 0.5f) * a.inv_h);  // floor(xh / H)
+  const int32_t h = xh - dt * a.H;
+  const int32_t r = rs + l;
+  const uint32_t xrow = st + l * 128;
+  const uint4 xl0 = lds16(xrow + (((2 * j + rev) ^ sw) << 4));
+  const uint4 xl1 = lds16(xrow + (((2 * j + (rev ^ 1)) ^ sw) << 4));
+  const uint4 xh0 = lds16(xrow + kHalfTile + (((2 * j + rev) ^ sw) << 4));
+  const uint4 xh1 = lds16(xrow + kHalfTile + (((2 * j + (rev ^ 1)) ^ sw) << 4));
+  const uint32_t tcos = st + 2 * kHalfTile + dt * kTabRow + j * (16 * static_cast<int>(sizeof(TT)));
+  const uint32_t wa = wbase + (h >= a.Hq ? 512u : 0u);  // the k weights follow the q weights
+
+  float2 lo[8], hi[8];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    lo[e] = Elem<T>::unpack(word(xl0, e));
+    lo[4 + e] = Elem<T>::unpack(word(xl1, e));
+    hi[e] = Elem<T>::unpack(word(xh0, e));
+    hi[4 + e] = Elem<T>::unpack(word(xh1, e));
+  }
+  // Sum of squares with four independent accumulators (short dependency chains).
+  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    acc[0] = fma2(lo[i], lo[i], acc[0]);
+    acc[1] = fma2(lo[i + 1], lo[i + 1], acc[1]);
+    acc[2] = fma2(hi[i], hi[i], acc[2]);
+    acc[3] = fma2(hi[i + 1], hi[i + 1], acc[3]);
+  }
+  const float2 acc2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+  const float ss = group_sum<kLPR>(acc2.x + acc2.y);
+  // ss/128 is exact as a multiplication by 2^-7; sqrt and reciprocal correctly rounded.
+  const float rstd = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, 0.0078125f), a.eps)));
+  const float2 rstd2 = splat2(rstd);
+  float pm[4];  // partial |y| maxima (four independent chains)
+  // Normalise and rotate eight pairs at a time (weights and table entries loaded per sub-chunk).
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int sm = m ^ rev;  // the sub-chunk this step works on
+    float2 wl[4], wh[4], c[4], s[4];
+#pragma unroll
+    for (int q4 = 0; q4 < 2; ++q4) {
+      const float4 fl = lds16f(wa + (2 * sm + q4) * 64);
+      const float4 fh = lds16f(wa + 256 + (2 * sm + q4) * 64);
+      wl[2 * q4] = make_float2(fl.x, fl.y);
+      wl[2 * q4 + 1] = make_float2(fl.z, fl.w);
+      wh[2 * q4] = make_float2(fh.x, fh.y);
+      wh[2 * q4 + 1] = make_float2(fh.z, fh.w);
+    }
+    lds_table8<TT>(tcos, sm, c);
+    lds_table8<TT>(tcos + a.tab_block, sm, s);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = 4 * m + e;
+      const float2 nl = mul2(mul2(lo[i], rstd2), wl[e]);
+      const float2 nh = mul2(mul2(hi[i], rstd2), wh[e]);
+      lo[i] = sub2(mul2(nl, c[e]), mul2(nh, s[e]));
+      hi[i] = add2(mul2(nh, c[e]), mul2(nl, s[e]));
+    }
+    pm[2 * m] = absmax4(absmax4(0.f, lo[4 * m], hi[4 * m]), lo[4 * m + 1], hi[4 * m + 1]);
+    pm[2 * m + 1] = absmax4(absmax4(0.f, lo[4 * m + 2], hi[4 * m + 2]), lo[4 * m + 3], hi[4 * m + 3]);
+  }
+  float amax;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(amax) : "f"(pm[0]), "f"(pm[1]), "f"(pm[2]));
+  amax = fmaxf(amax, pm[3]);
+  amax = fmaxf(group_max<kLPR>(amax), 1e-4f);
+  // scale = RN(amax / fp8_max) via the correctly rounded reciprocal and one correction.
+  const float s0 = __fmul_rn(amax, a.rcp_fp8_max);
+  const float sc = __fmaf_rn(__fmaf_rn(-s0, a.fp8_max, amax), a.rcp_fp8_max, s0);
+  const float rc = __frcp_rn(sc);
+  uint32_t ql[4], qh[4];
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    float2 a0 = div2_by(lo[i], sc, rc), a1 = div2_by(lo[i + 1], sc, rc);
+    float2 b0 = div2_by(hi[i], sc, rc), b1 = div2_by(hi[i + 1], sc, rc);
+    if (clamp) {
+      a0 = make_float2(clamp_abs(a0.x, a.fp8_max), clamp_abs(a0.y, a.fp8_max));
+      a1 = make_float2(clamp_abs(a1.x, a.fp8_max), clamp_abs(a1.y, a.fp8_max));
+      b0 = make_float2(clamp_abs(b0.x, a.fp8_max), clamp_abs(b0.y, a.fp8_max));
+      b1 = make_float2(clamp_abs(b1.x, a.fp8_max), clamp_abs(b1.y, a.fp8_max));
+    }
+    ql[i / 2] = e4m3x2(a0) | (e4m3x2(a1) << 16);
+    qh[i / 2] = e4m3x2(b0) | (e4m3x2(b1) << 16);
+  }
+  if (live) {
+    // ql/qh[0..1] hold sub-chunk rev, [2..3] the other one (8 codes each)
+    uint8_t* qrow = a.q + static_cast<int64_t>(r) * kD + 16 * j;
+    st_stream8(qrow + 8 * rev, make_uint2(ql[0], ql[1]));
+    st_stream8(qrow + 8 * (rev ^ 1), make_uint2(ql[2], ql[3]));
+    st_stream8(qrow + 64 + 8 * rev, make_uint2(qh[0], qh[1]));
+    st_stream8(qrow + 64 + 8 * (rev ^ 1), make_uint2(qh[2], qh[3]));
+    if (j == 0) a.scale[r] = sc;
+  }
+}
+
 // ------------------------------------------------------------------------------ the kernel
 template <typename T, typename TT>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -190,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
+      mbar_init(&empty[s], kConsumerWarps / 2);  // each stage is consumed by one half of the warps
     }
     fence_barrier_init();
   }
@@ -206,11 +310,26 @@ __global__ void __launch_bounds__(kThreads, 2)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
     int k = 0;
     bool ok = true;
+    int slot = 0;
+    uint32_t phase = 0;  // parity of the slot's current use; its release completes phase ^ 1
+    int dslot = 0;       // slot and parity of stage k - depth
+    uint32_t dphase = 0;
     for (; k < nst; ++k) {
-      const int slot = k % S;
-      if (k >= S && !mbar_wait(&empty[slot], static_cast<uint32_t>((k / S) - 1) & 1u)) {
+      if (k >= S && !mbar_wait(&empty[slot], phase ^ 1u)) {
         ok = false;
         break;
+      }
+      // Keep at most `depth` stages in flight: every CTA's next stage then queues behind few
+      // others, which evens out when the CTAs' data arrives (the last CTA sets the kernel's end).
+      if (k >= a.depth) {
+        if (!mbar_wait(&full[dslot], dphase)) {
+          ok = false;
+          break;
+        }
+        if (++dslot == S) {
+          dslot = 0;
+          dphase ^= 1u;
+        }
       }
       const int32_t rs = r0 + k * kStageRows;
       const int32_t re = min(rs + kStageRows, r1);
@@ -226,6 +345,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                tbytes, &full[slot]);
       bulk_g2s(st + 2 * kHalfTile + a.tab_block,
                static_cast<const unsigned char*>(a.sin) + static_cast<int64_t>(tf) * kTabRow, tbytes, &full[slot]);
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
     }
     if (!ok) {
       flag_failure(a.status);
@@ -247,106 +370,39 @@ __global__ void __launch_bounds__(kThreads, 2)
     wsm[((((set * 2 + half) * 4 + kk) * 4 + jj) * 4) + comp] = Elem<T>::load1(set ? a.wk : a.wq, c);
   }
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-  const int grp = lane >> 2;         // row within the warp's eight
-  const int j = lane & 3;            // pairs 16j..16j+15 of each half
-  const int l = warp * 8 + grp;      // row within the stage
-  const int sw = l & 7;              // 128-byte swizzle phase of this row
-  const uint32_t xoff0 = l * 128 + (((2 * j) ^ sw) << 4);
-  const uint32_t xoff1 = l * 128 + (((2 * j + 1) ^ sw) << 4);
+  const int grp = lane >> 2;  // row group within the warp
+  const int j = lane & 3;     // pairs 16j..16j+15 of each half
+  // A lane's 16 pairs are two sub-chunks of 8. Lanes 2 and 3 walk them in the opposite order, so
+  // that in every shared-memory load the four lanes of a row touch disjoint banks (their fp32 table
+  // and weight entries would otherwise sit 128 bytes apart).
+  const int rev = j >> 1;
   const uint32_t wbase = smem_addr(wsm) + j * 16;
   const bool clamp = a.fp8_max != 448.0f;
+  // The consumer warps work in two halves on alternate stages (even / odd), so that at any moment
+  // the warps of a scheduler are at different points of their row (the serial parts -- reductions,
+  // square root, reciprocals -- then overlap with the other half's arithmetic). A lane group takes
+  // rows l0 and l0 + 32 of its half's stages.
+  const int half = warp / (kConsumerWarps / 2);
+  const int l0 = (warp % (kConsumerWarps / 2)) * 8 + grp;
 
-  for (int k = 0; k < nst; ++k) {
-    const int slot = k % S;
-    if (!mbar_wait(&full[slot], static_cast<uint32_t>(k / S) & 1u)) {
+  int slot = half;  // stage k lives in slot k % S; S >= 2
+  uint32_t phase = 0;
+  for (int k = half; k < nst; k += 2) {
+    if (!mbar_wait(&full[slot], phase)) {
       flag_failure(a.status);
       return;
     }
     const uint32_t st = smem_addr(smem + static_cast<size_t>(slot) * a.stage_bytes);
     const int32_t rs = r0 + k * kStageRows;
-    const bool live = l < r1 - rs;
     const int32_t tf = static_cast<int32_t>((static_cast<uint64_t>(rs) * a.magic) >> a.shift);
-    const int32_t xh = (rs - tf * a.H) + l;                    // head index counted from token tf
-    const int32_t dt = static_cast<int32_t>((static_cast<float>(xh) + 0.5f) * a.inv_h);  // floor(xh / H)
-    const int32_t h = xh - dt * a.H;
-    const int32_t r = rs + l;
-
-    const uint4 xl0 = lds16(st + xoff0), xl1 = lds16(st + xoff1);
-    const uint4 xh0 = lds16(st + kHalfTile + xoff0), xh1 = lds16(st + kHalfTile + xoff1);
-    const uint32_t tcos = st + 2 * kHalfTile + dt * kTabRow + j * (16 * static_cast<int>(sizeof(TT)));
-    const uint32_t wa = wbase + (h >= a.Hq ? 512u : 0u);  // the k weights follow the q weights
-
-    float2 lo[8], hi[8];
-    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      lo[e] = Elem<T>::unpack(word(xl0, e));
-      lo[4 + e] = Elem<T>::unpack(word(xl1, e));
-      hi[e] = Elem<T>::unpack(word(xh0, e));
-      hi[4 + e] = Elem<T>::unpack(word(xh1, e));
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      acc0 = fma2(lo[i], lo[i], acc0);
-      acc1 = fma2(hi[i], hi[i], acc1);
-    }
-    const float2 acc = add2(acc0, acc1);
-    const float ss = group_sum<kLPR>(acc.x + acc.y);
-    // ss/128 is exact as a multiplication by 2^-7; sqrt and reciprocal correctly rounded.
-    const float rstd = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, 0.0078125f), a.eps)));
-    const float2 rstd2 = splat2(rstd);
-    float amax = 0.f;
-    // Normalise and rotate eight pairs at a time (weights and table entries loaded per half-chunk).
-#pragma unroll
-    for (int m = 0; m < 2; ++m) {
-      float2 wl[4], wh[4], c[4], s[4];
-#pragma unroll
-      for (int q4 = 0; q4 < 2; ++q4) {
-        const float4 fl = lds16f(wa + (2 * m + q4) * 64);
-        const float4 fh = lds16f(wa + 256 + (2 * m + q4) * 64);
-        wl[2 * q4] = make_float2(fl.x, fl.y);
-        wl[2 * q4 + 1] = make_float2(fl.z, fl.w);
-        wh[2 * q4] = make_float2(fh.x, fh.y);
-        wh[2 * q4 + 1] = make_float2(fh.z, fh.w);
-      }
-      lds_table8<TT>(tcos, m, c);
-      lds_table8<TT>(tcos + a.tab_block, m, s);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = 4 * m + e;
-        const float2 nl = mul2(mul2(lo[i], rstd2), wl[e]);
-        const float2 nh = mul2(mul2(hi[i], rstd2), wh[e]);
-        lo[i] = add2(mul2(nl, c[e]), neg2(mul2(nh, s[e])));
-        hi[i] = add2(mul2(nh, c[e]), mul2(nl, s[e]));
-        amax = absmax4(amax, lo[i], hi[i]);
-      }
-    }
-    amax = fmaxf(group_max<kLPR>(amax), 1e-4f);
-    // scale = RN(amax / fp8_max) via the correctly rounded reciprocal and one correction.
-    const float s0 = __fmul_rn(amax, a.rcp_fp8_max);
-    const float sc = __fmaf_rn(__fmaf_rn(-s0, a.fp8_max, amax), a.rcp_fp8_max, s0);
-    const float rc = __frcp_rn(sc);
-    uint32_t ql[4], qh[4];
-#pragma unroll
-    for (int i = 0; i < 8; i += 2) {
-      float2 a0 = div2_by(lo[i], sc, rc), a1 = div2_by(lo[i + 1], sc, rc);
-      float2 b0 = div2_by(hi[i], sc, rc), b1 = div2_by(hi[i + 1], sc, rc);
-      if (clamp) {
-        a0 = make_float2(clamp_abs(a0.x, a.fp8_max), clamp_abs(a0.y, a.fp8_max));
-        a1 = make_float2(clamp_abs(a1.x, a.fp8_max), clamp_abs(a1.y, a.fp8_max));
-        b0 = make_float2(clamp_abs(b0.x, a.fp8_max), clamp_abs(b0.y, a.fp8_max));
-        b1 = make_float2(clamp_abs(b1.x, a.fp8_max), clamp_abs(b1.y, a.fp8_max));
-      }
-      ql[i / 2] = e4m3x2(a0) | (e4m3x2(a1) << 16);
-      qh[i / 2] = e4m3x2(b0) | (e4m3x2(b1) << 16);
-    }
+    prologue_row<T, TT>(a, st, l0, j, rev, wbase, rs, r1, tf, clamp);
+    prologue_row<T, TT>(a, st, l0 + 32, j, rev, wbase, rs, r1, tf, clamp);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the stage's shared memory
-    if (live) {
-      uint8_t* qrow = a.q + static_cast<int64_t>(r) * kD;
-      st_stream16(qrow + 16 * j, make_uint4(ql[0], ql[1], ql[2], ql[3]));
-      st_stream16(qrow + 64 + 16 * j, make_uint4(qh[0], qh[1], qh[2], qh[3]));
-      if (j == 0) a.scale[r] = sc;
+    slot += 2;
+    if (slot >= S) {
+      slot -= S;
+      phase ^= 1u;
     }
   }
 }
@@ -418,6 +474,11 @@ bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStrea
   p.stages = (110 * 1024 - fixed) / p.stage_bytes;
   if (p.stages > 6) p.stages = 6;
   if (p.stages < 2) p.stages = 2;
+  // At most two stages in flight per CTA (measured best on the 4k and 32k prologues). The depth
+  // must not exceed the ring: the producer waits on the full barrier of stage k - depth, whose slot
+  // must not have been refilled yet.
+  p.depth = 2;
+  if (p.depth > p.stages) p.depth = p.stages;
   const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + 2 * kD * sizeof(float) +
                       2 * p.stages * sizeof(uint64_t);
   if (smem > 227 * 1024) return false;

@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kThreads) rows_vec_kernel(const RowArgs a) {
             lo = round_trip<T>(lo);
             hi = round_trip<T>(hi);
           }
-          float2 ylo = add2(mul2(lo, c[k]), neg2(mul2(hi, sn[k])));
+          float2 ylo = sub2(mul2(lo, c[k]), mul2(hi, sn[k]));
           float2 yhi = add2(mul2(hi, c[k]), mul2(lo, sn[k]));
           if constexpr (MODE == MODE_QK) {
             yf[slo][k] = ylo;
