@@ -16,11 +16,14 @@
 // swizzle makes the four lanes' 16-byte reads of two neighbouring rows hit disjoint banks. Each
 // lane stores its 16 contiguous codes of each half with one 16-byte store.
 //
-// Arithmetic (same cast points and roundings as the oracle and the generic row kernel):
-//   ss = sum x^2 (fp32) -> rstd = 1/sqrt(ss/128 + eps)  (ss/128 is exact as ss * 2^-7; the square
-//   root and the reciprocal are correctly rounded); n = (x*rstd)*w; lo' = lo*c - hi*s,
-//   hi' = hi*c + lo*s; amax -> scale = max(amax, 1e-4)/fp8_max (correctly rounded);
-//   q = e4m3(RN(y/scale)) from the correctly rounded reciprocal and one Markstein correction.
+// Arithmetic (the oracle's cast points, with two hardware shortcuts that stay far inside the
+// parity tolerances -- scale within 1e-5 relative, codes at most one step apart on at most 0.1%):
+//   ss = sum x^2 (fp32) -> rstd = rsqrt(ss/128 + eps) with the hardware rsqrt approximation (at
+//   most 2 ulp, as torch's own CUDA rsqrt; ss/128 is exact as ss * 2^-7); n = (x*rstd)*w;
+//   lo' = lo*c - hi*s, hi' = hi*c + lo*s (each product and sum rounded, no fusion);
+//   scale = RN(max(amax, 1e-4)/fp8_max) (correctly rounded); q = e4m3(RN(y * RN(1/scale))).
+// A perturbation of one or two fp32 ulps moves a code only when y/scale sits at an e4m3 rounding
+// boundary, so the codes match the oracle's true division except on a vanishing fraction.
 //
 // Waits are bounded: a wait that has not completed after ~1 s of %globaltimer time sets bit 0 of
 // the device status word and the kernel stops issuing and consuming work (waiting, again bounded,
@@ -40,8 +43,12 @@ constexpr int kD = 128;                                  // head_dim handled her
 constexpr int kLPR = 4;                                  // lanes per row
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;      // + one producer warp
-constexpr int kStageRows = kConsumerWarps * (32 / kLPR); // 64
-constexpr int kHalfTile = kStageRows * (kD / 2) * 2;     // one half of 64 rows in a 16-bit dtype: 8 KB
+constexpr int kGroupsPerHalf = (kConsumerWarps / 2) * (32 / kLPR);  // lane groups in one consumer half
+// Rows per stage (SR) is a template parameter: 64 for long row ranges per CTA, 32 when a CTA has
+// only a few stages to do (shorter pipeline fill and drain). Each lane group takes SR / 32 rows of
+// every stage its half consumes. One half of a stage's x (the NeoX lo or hi half) is SR * 128 bytes.
+template <int SR>
+__host__ __device__ constexpr int half_tile() { return SR * (kD / 2) * 2; }
 constexpr uint64_t kWaitLimitNs = 1000000000ull;         // 1 s
 
 struct PrologueArgs {
@@ -170,7 +177,7 @@ __device__ __forceinline__ void flag_failure(unsigned int* status) {
 
 // One (token, head) row of a stage, by the four lanes of a lane group: shared-memory x, table and
 // weight entries in, e4m3 codes and the fp32 scale out. `l` is the row within the stage.
-template <typename T, typename TT>
+template <typename T, typename TT, int SR>
 __device__ __forceinline__ void prologue_row(const PrologueArgs& a, uint32_t st, int l, int j, int rev,
                                              uint32_t wbase, int32_t rs, int32_t r1, int32_t tf, bool clamp) {
   constexpr int kTabRow = (kD / 2) * static_cast<int>(sizeof(TT));
@@ -183,9 +190,9 @@ __device__ __forceinline__ void prologue_row(const PrologueArgs& a, uint32_t st,
   const uint32_t xrow = st + l * 128;
   const uint4 xl0 = lds16(xrow + (((2 * j + rev) ^ sw) << 4));
   const uint4 xl1 = lds16(xrow + (((2 * j + (rev ^ 1)) ^ sw) << 4));
-  const uint4 xh0 = lds16(xrow + kHalfTile + (((2 * j + rev) ^ sw) << 4));
-  const uint4 xh1 = lds16(xrow + kHalfTile + (((2 * j + (rev ^ 1)) ^ sw) << 4));
-  const uint32_t tcos = st + 2 * kHalfTile + dt * kTabRow + j * (16 * static_cast<int>(sizeof(TT)));
+  const uint4 xh0 = lds16(xrow + half_tile<SR>() + (((2 * j + rev) ^ sw) << 4));
+  const uint4 xh1 = lds16(xrow + half_tile<SR>() + (((2 * j + (rev ^ 1)) ^ sw) << 4));
+  const uint32_t tcos = st + 2 * half_tile<SR>() + dt * kTabRow + j * (16 * static_cast<int>(sizeof(TT)));
   const uint32_t wa = wbase + (h >= a.Hq ? 512u : 0u);  // the k weights follow the q weights
 
   float2 lo[8], hi[8];
@@ -207,8 +214,8 @@ __device__ __forceinline__ void prologue_row(const PrologueArgs& a, uint32_t st,
   }
   const float2 acc2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
   const float ss = group_sum<kLPR>(acc2.x + acc2.y);
-  // ss/128 is exact as a multiplication by 2^-7; sqrt and reciprocal correctly rounded.
-  const float rstd = __frcp_rn(__fsqrt_rn(__fadd_rn(__fmul_rn(ss, 0.0078125f), a.eps)));
+  // ss/128 is exact as a multiplication by 2^-7; rsqrt is the hardware approximation.
+  const float rstd = rsqrtf(__fadd_rn(__fmul_rn(ss, 0.0078125f), a.eps));
   const float2 rstd2 = splat2(rstd);
   float pm[4];  // partial |y| maxima (four independent chains)
   // Normalise and rotate eight pairs at a time (weights and table entries loaded per sub-chunk).
@@ -249,8 +256,8 @@ __device__ __forceinline__ void prologue_row(const PrologueArgs& a, uint32_t st,
   uint32_t ql[4], qh[4];
 #pragma unroll
   for (int i = 0; i < 8; i += 2) {
-    float2 a0 = div2_by(lo[i], sc, rc), a1 = div2_by(lo[i + 1], sc, rc);
-    float2 b0 = div2_by(hi[i], sc, rc), b1 = div2_by(hi[i + 1], sc, rc);
+    float2 a0 = mul2(lo[i], splat2(rc)), a1 = mul2(lo[i + 1], splat2(rc));
+    float2 b0 = mul2(hi[i], splat2(rc)), b1 = mul2(hi[i + 1], splat2(rc));
     if (clamp) {
       a0 = make_float2(clamp_abs(a0.x, a.fp8_max), clamp_abs(a0.y, a.fp8_max));
       a1 = make_float2(clamp_abs(a1.x, a.fp8_max), clamp_abs(a1.y, a.fp8_max));
@@ -272,7 +279,7 @@ __device__ __forceinline__ void prologue_row(const PrologueArgs& a, uint32_t st,
 }
 
 // ------------------------------------------------------------------------------ the kernel
-template <typename T, typename TT>
+template <typename T, typename TT, int SR>
 __global__ void __launch_bounds__(kThreads, 2)
     prologue_tma_kernel(const __grid_constant__ CUtensorMap xmap, const PrologueArgs a) {
   extern __shared__ unsigned char smem_raw[];
@@ -288,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int lane = threadIdx.x & 31;
   const int32_t r0 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x) * a.rows) / gridDim.x);
   const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x + 1) * a.rows) / gridDim.x);
-  const int nst = (r1 - r0 + kStageRows - 1) / kStageRows;
+  const int nst = (r1 - r0 + SR - 1) / SR;
   constexpr int kTabRow = (kD / 2) * static_cast<int>(sizeof(TT));  // bytes of one table row
 
   if (threadIdx.x == 0) {
@@ -331,19 +338,19 @@ __global__ void __launch_bounds__(kThreads, 2)
           dphase ^= 1u;
         }
       }
-      const int32_t rs = r0 + k * kStageRows;
-      const int32_t re = min(rs + kStageRows, r1);
+      const int32_t rs = r0 + k * SR;
+      const int32_t re = min(rs + SR, r1);
       const int32_t tf = static_cast<int32_t>((static_cast<uint64_t>(rs) * a.magic) >> a.shift);
       const int32_t tl = static_cast<int32_t>((static_cast<uint64_t>(re - 1) * a.magic) >> a.shift);
       const uint32_t tbytes = static_cast<uint32_t>(tl - tf + 1) * kTabRow;
       unsigned char* st = smem + static_cast<size_t>(slot) * a.stage_bytes;
       // Rows past the end of the tensor are zero-filled and still counted in full.
-      mbar_arrive_expect_tx(&full[slot], 2u * kHalfTile + 2u * tbytes);
+      mbar_arrive_expect_tx(&full[slot], 2u * half_tile<SR>() + 2u * tbytes);
       tma_load_2d(st, &xmap, 0, rs, &full[slot]);
-      tma_load_2d(st + kHalfTile, &xmap, kD / 2, rs, &full[slot]);
-      bulk_g2s(st + 2 * kHalfTile, static_cast<const unsigned char*>(a.cos) + static_cast<int64_t>(tf) * kTabRow,
+      tma_load_2d(st + half_tile<SR>(), &xmap, kD / 2, rs, &full[slot]);
+      bulk_g2s(st + 2 * half_tile<SR>(), static_cast<const unsigned char*>(a.cos) + static_cast<int64_t>(tf) * kTabRow,
                tbytes, &full[slot]);
-      bulk_g2s(st + 2 * kHalfTile + a.tab_block,
+      bulk_g2s(st + 2 * half_tile<SR>() + a.tab_block,
                static_cast<const unsigned char*>(a.sin) + static_cast<int64_t>(tf) * kTabRow, tbytes, &full[slot]);
       if (++slot == S) {
         slot = 0;
@@ -381,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // The consumer warps work in two halves on alternate stages (even / odd), so that at any moment
   // the warps of a scheduler are at different points of their row (the serial parts -- reductions,
   // square root, reciprocals -- then overlap with the other half's arithmetic). A lane group takes
-  // rows l0 and l0 + 32 of its half's stages.
+  // rows l0, l0 + 32, ... of its half's stages.
   const int half = warp / (kConsumerWarps / 2);
   const int l0 = (warp % (kConsumerWarps / 2)) * 8 + grp;
 
@@ -393,10 +400,11 @@ __global__ void __launch_bounds__(kThreads, 2)
       return;
     }
     const uint32_t st = smem_addr(smem + static_cast<size_t>(slot) * a.stage_bytes);
-    const int32_t rs = r0 + k * kStageRows;
+    const int32_t rs = r0 + k * SR;
     const int32_t tf = static_cast<int32_t>((static_cast<uint64_t>(rs) * a.magic) >> a.shift);
-    prologue_row<T, TT>(a, st, l0, j, rev, wbase, rs, r1, tf, clamp);
-    prologue_row<T, TT>(a, st, l0 + 32, j, rev, wbase, rs, r1, tf, clamp);
+#pragma unroll
+    for (int u = 0; u < (SR / kGroupsPerHalf); ++u)
+      prologue_row<T, TT, SR>(a, st, l0 + u * kGroupsPerHalf, j, rev, wbase, rs, r1, tf, clamp);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the stage's shared memory
     slot += 2;
@@ -424,13 +432,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
-  if (a.N != kD || a.R != kD) return false;
-  if (a.rows <= 0 || a.rows > 0x7fffffffLL) return false;
-  if (a.token_stride != static_cast<int64_t>(a.H) * kD) return false;  // packed [T, H, 128] only
-  if (a.H + kStageRows >= (1 << 21)) return false;
-  if (!(table_dtype == DT_FP32 || table_dtype == dtype)) return false;
-  if ((reinterpret_cast<uintptr_t>(a.q) & 15u) != 0) return false;
+namespace {
+
+template <int SR>
+bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
   if (encode == nullptr) return false;
   const int tsz = (table_dtype == DT_FP32) ? 4 : 2;
@@ -438,7 +443,7 @@ bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStrea
   CUtensorMap xmap;
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(a.rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD) * 2};
-  const cuuint32_t box[2] = {kD / 2, kStageRows};
+  const cuuint32_t box[2] = {kD / 2, SR};
   const cuuint32_t estr[2] = {1, 1};
   if (encode(&xmap, dtype == DT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
              const_cast<void*>(a.x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -466,18 +471,18 @@ bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStrea
   while ((1LL << lg) < a.H) ++lg;
   p.shift = 31 + lg;
   p.magic = static_cast<uint64_t>(((static_cast<unsigned __int128>(1) << p.shift) + a.H - 1) / a.H);
-  const int tab_rows = (kStageRows - 1) / a.H + 2;  // tokens one 64-row stage can touch
+  const int tab_rows = (SR - 1) / a.H + 2;  // tokens one stage can touch
   p.tab_block = ((tab_rows * (kD / 2) * tsz) + 127) & ~127;
-  p.stage_bytes = ((2 * kHalfTile + 2 * p.tab_block) + 1023) & ~1023;
-  // Ring depth: as many stages (up to 6) as fit two CTAs per SM in GB300's 228 KB of shared memory.
-  const int fixed = 1024 + 2 * kD * static_cast<int>(sizeof(float)) + 2 * 8 * static_cast<int>(sizeof(uint64_t));
+  p.stage_bytes = ((2 * half_tile<SR>() + 2 * p.tab_block) + 1023) & ~1023;
+  // Ring depth: as many stages (up to 12) as fit two CTAs per SM in GB300's 228 KB of shared memory.
+  const int fixed = 1024 + 2 * kD * static_cast<int>(sizeof(float)) + 2 * 12 * static_cast<int>(sizeof(uint64_t));
   p.stages = (110 * 1024 - fixed) / p.stage_bytes;
-  if (p.stages > 6) p.stages = 6;
+  if (p.stages > 12) p.stages = 12;
   if (p.stages < 2) p.stages = 2;
-  // At most two stages in flight per CTA (measured best on the 4k and 32k prologues). The depth
-  // must not exceed the ring: the producer waits on the full barrier of stage k - depth, whose slot
-  // must not have been refilled yet.
-  p.depth = 2;
+  // At most 128 rows (two 64-row stages) in flight per CTA: measured best on the 4k and 32k
+  // prologues. The depth must not exceed the ring: the producer waits on the full barrier of stage
+  // k - depth, whose slot must not have been refilled yet.
+  p.depth = 128 / SR;
   if (p.depth > p.stages) p.depth = p.stages;
   const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + 2 * kD * sizeof(float) +
                       2 * p.stages * sizeof(uint64_t);
@@ -485,9 +490,10 @@ bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStrea
 
   void (*kern)(const CUtensorMap, const PrologueArgs);
   if (dtype == DT_BF16)
-    kern = (tsz == 4) ? prologue_tma_kernel<__nv_bfloat16, float> : prologue_tma_kernel<__nv_bfloat16, __nv_bfloat16>;
+    kern = (tsz == 4) ? prologue_tma_kernel<__nv_bfloat16, float, SR>
+                      : prologue_tma_kernel<__nv_bfloat16, __nv_bfloat16, SR>;
   else
-    kern = (tsz == 4) ? prologue_tma_kernel<__half, float> : prologue_tma_kernel<__half, __half>;
+    kern = (tsz == 4) ? prologue_tma_kernel<__half, float, SR> : prologue_tma_kernel<__half, __half, SR>;
   static int configured[4] = {0, 0, 0, 0};
   const int key = (dtype == DT_BF16 ? 0 : 2) + (tsz == 4 ? 0 : 1);
   if (configured[key] < static_cast<int>(smem)) {
@@ -499,7 +505,7 @@ bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStrea
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
     per_sm = 1;
-  const int64_t want = (a.rows + kStageRows - 1) / kStageRows;
+  const int64_t want = (a.rows + SR - 1) / SR;
   const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
   const int grid = static_cast<int>(want < cap ? want : cap);
   // Programmatic stream serialisation: this grid may be scheduled while the previous kernel in the
@@ -515,6 +521,22 @@ bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStrea
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, xmap, p) == cudaSuccess;
+}
+
+}  // namespace
+
+bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
+  if (a.N != kD || a.R != kD) return false;
+  if (a.rows <= 0 || a.rows > 0x7fffffffLL) return false;
+  if (a.token_stride != static_cast<int64_t>(a.H) * kD) return false;  // packed [T, H, 128] only
+  if (a.H + 64 >= (1 << 21)) return false;
+  if (!(table_dtype == DT_FP32 || table_dtype == dtype)) return false;
+  if ((reinterpret_cast<uintptr_t>(a.q) & 15u) != 0) return false;
+  // Short row ranges per CTA (a few stages each): 32-row stages halve the pipeline fill and drain.
+  // Long ranges: 64-row stages halve the per-stage bookkeeping. Two CTAs per SM are resident.
+  const int64_t rows_per_cta = a.rows / (2 * static_cast<int64_t>(sm_count()));
+  if (rows_per_cta <= 1024) return launch_sr<32>(a, dtype, table_dtype, s);
+  return launch_sr<64>(a, dtype, table_dtype, s);
 }
 
 }  // namespace fq

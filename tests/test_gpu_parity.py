@@ -92,13 +92,14 @@ def test_prologue_outliers_and_huge_positions(orc, cuda_ok):
 
 
 def test_prologue_zero_rows(orc, cuda_ok):
-    """All-zero rows: scale = 1e-4/448 and every code +0."""
+    """All-zero rows: scale = 1e-4/448 and every code decodes to zero. The rotation can give -0
+    (0*c - 0*s with c < 0 < s), which e4m3fn encodes as 0x80, so the sign bit is not checked."""
     d = wl.qk_inputs(4, 2, 2, 128, seed=103)
     d["qk"][1:3] = 0
     q_ref, s_ref = orc.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], 2, 2)
     g = cuda(d)
     q, s = fq.qk_norm_rope_quant(g["qk"], g["wq"], g["wk"], g["cos"], g["sin"], 2, 2)
-    assert torch.equal(q.cpu()[1:3], torch.zeros_like(q.cpu()[1:3]))
+    assert int((q.cpu()[1:3] & 0x7F).max()) == 0
     assert torch.equal(s.cpu()[1:3], s_ref[1:3])
     assert_codes_close(q, q_ref)
 
