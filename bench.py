@@ -554,7 +554,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
-                     "traffic": profiled_traffic(), "kernel": "prologue_tma_kernel<bf16,float>",
+                     "traffic": profiled_traffic(), "kernel": "prologue_tma_kernel<bf16,float,32>",
                      "us_per_launch": round(per_launch_us, 3)},
         "gpu_launches": args.steps * case.kernels_per_step,
         "clocks": clocks,
