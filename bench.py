@@ -378,6 +378,7 @@ def time_case(case: Case, steps: int, warmup: int, stream, use_graph=True, graph
 
 
 _PG = None
+_PG_DEVICE = "cpu"
 
 
 def barrier():
@@ -388,14 +389,21 @@ def barrier():
 
 
 def max_over_ranks(v: float) -> float:
+    """Largest value of `v` over all ranks (the job's time is its slowest rank's)."""
     if _PG is None:
         return v
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=_PG_DEVICE)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput_gbs(bytes_per_step: int, steps: int, max_ms: float, world: int) -> float:
+    """Whole-job GB/s: every rank processed `steps` batches of `bytes_per_step` (weak scaling) in
+    the slowest rank's time."""
+    return world * bytes_per_step * steps / (max_ms * 1e-3) / 1e9
 
 
 def e2e_prologue(case: PrologueCase, steps: int, stream):
@@ -512,7 +520,7 @@ def main():
 
     import torch
 
-    global _PG
+    global _PG, _PG_DEVICE
     rank, local_rank, world = dist_env()
     if world > 1:
         import torch.distributed as dist
@@ -520,6 +528,7 @@ def main():
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
         _PG = dist.group.WORLD
+        _PG_DEVICE = f"cuda:{local_rank}"
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     import fp8_quant_memory_gb300 as fq
@@ -539,7 +548,7 @@ def main():
 
     per_launch_us = ms * 1e3 / args.steps
     bytes_step = case.bytes_per_step()
-    value = world * bytes_step * args.steps / (ms * 1e-3) / 1e9
+    value = job_throughput_gbs(bytes_step, args.steps, ms, world)
     achieved = bytes_step / (per_launch_us * 1e-6) / 1e9
     peak, peak_kind = peaks()
 

@@ -23,7 +23,8 @@ import torch
 from . import _capi
 
 __all__ = ["rmsnorm_fwd", "rmsnorm_rope", "rmsnorm_rope_quant", "qk_norm_rope_quant", "rmsnorm_bwd",
-           "rmsnorm_bwd_workspace_bytes", "rmsnorm", "RMSNormFunction", "device_status", "FqError"]
+           "rmsnorm_bwd_workspace_bytes", "rmsnorm", "RMSNormFunction", "device_status", "check_bounded_wait",
+           "FqError"]
 
 FqError = _capi.FqError
 
@@ -174,6 +175,15 @@ def device_status(clear: bool = True, device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     _capi.call("fq_device_status", ctypes.byref(word), 1 if clear else 0, _stream(dev))
     return int(word.value)
+
+
+def check_bounded_wait(limit_ms: int = 50, device=None) -> int:
+    """Run the bounded-wait diagnostic (a wait that can only give up after limit_ms) and return the
+    device status word it leaves (bit 0 set means the wait gave up as designed); clears it."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    device_status(clear=True, device=dev)
+    _capi.call("fq_check_bounded_wait", ctypes.c_uint(limit_ms), _stream(dev))
+    return device_status(clear=True, device=dev)
 
 
 class RMSNormFunction(torch.autograd.Function):

@@ -132,6 +132,15 @@ int fq_device_status(unsigned int* word, int clear, cudaStream_t stream) {
   return ok();
 }
 
+int fq_check_bounded_wait(unsigned int limit_ms, cudaStream_t stream) {
+  if (limit_ms < 1 || limit_ms > 10000)
+    return fail(FQ_ERR_INVALID_ARG, "fq_check_bounded_wait: limit_ms must be in [1, 10000], got %u", limit_ms);
+  cudaGetLastError();
+  const cudaError_t e = fq::launch_wait_probe(limit_ms, stream);
+  if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "fq_check_bounded_wait: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, int dtype, float eps,
                    cudaStream_t stream) {
   const char* fn = "fq_rmsnorm_fwd";

@@ -75,6 +75,8 @@ void launch_bwd(const BwdArgs& a, int dtype, cudaStream_t s);
 // passed to kernels in other translation units.
 cudaError_t read_device_status(unsigned int* word, int clear, cudaStream_t s);
 unsigned int* device_status_ptr();
+// Launches the bounded-wait probe (one block, one wait that can only give up after limit_ms).
+cudaError_t launch_wait_probe(unsigned int limit_ms, cudaStream_t s);
 
 int sm_count();
 

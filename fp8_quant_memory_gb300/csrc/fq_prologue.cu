@@ -35,6 +35,7 @@
 
 #include "fq_device.cuh"
 #include "fq_internal.h"
+#include "fq_sync.cuh"
 
 namespace fq {
 namespace {
@@ -49,7 +50,6 @@ constexpr int kGroupsPerHalf = (kConsumerWarps / 2) * (32 / kLPR);  // lane grou
 // every stage its half consumes. One half of a stage's x (the NeoX lo or hi half) is SR * 128 bytes.
 template <int SR>
 __host__ __device__ constexpr int half_tile() { return SR * (kD / 2) * 2; }
-constexpr uint64_t kWaitLimitNs = 1000000000ull;         // 1 s
 
 struct PrologueArgs {
   const void* wq;
@@ -70,74 +70,6 @@ struct PrologueArgs {
   int32_t tab_block;     // bytes of one table block (cos or sin)
   int32_t depth;         // the producer keeps at most this many stages in flight
 };
-
-// ------------------------------------------------------------------------------ PTX wrappers
-__device__ __forceinline__ uint32_t smem_addr(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
-               : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(done)
-      : "r"(smem_addr(bar)), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-// Wait for the phase with the given parity to complete; false if ~1 s passed first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1; i != 0; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
-  }
-  return false;
-}
-
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
-      "[%4];" ::"r"(smem_addr(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void fence_barrier_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
 
 __device__ __forceinline__ uint4 lds16(uint32_t addr) {
   uint4 v;
@@ -169,10 +101,6 @@ __device__ __forceinline__ void lds_table8(uint32_t addr, int m, float2 (&v)[4])
 #pragma unroll
     for (int e = 0; e < 4; ++e) v[e] = Elem<TT>::unpack(word(u, e));
   }
-}
-
-__device__ __forceinline__ void flag_failure(unsigned int* status) {
-  if (status != nullptr) atomicOr(status, 1u);
 }
 
 // One (token, head) row of a stage, by the four lanes of a lane group: shared-memory x, table and
@@ -322,14 +250,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     int dslot = 0;       // slot and parity of stage k - depth
     uint32_t dphase = 0;
     for (; k < nst; ++k) {
-      if (k >= S && !mbar_wait(&empty[slot], phase ^ 1u)) {
+      if (k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) {
         ok = false;
         break;
       }
       // Keep at most `depth` stages in flight: every CTA's next stage then queues behind few
       // others, which evens out when the CTAs' data arrives (the last CTA sets the kernel's end).
       if (k >= a.depth) {
-        if (!mbar_wait(&full[dslot], dphase)) {
+        if (!mbar_wait(kWaitLimitNs, &full[dslot], dphase)) {
           ok = false;
           break;
         }
@@ -361,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       flag_failure(a.status);
       // Let the copies already issued land before this CTA's shared memory goes away.
       for (int j = max(0, k - S); j < k; ++j)
-        if (!mbar_wait(&full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
+        if (!mbar_wait(kWaitLimitNs, &full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
     }
     return;
   }
@@ -395,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   int slot = half;  // stage k lives in slot k % S; S >= 2
   uint32_t phase = 0;
   for (int k = half; k < nst; k += 2) {
-    if (!mbar_wait(&full[slot], phase)) {
+    if (!mbar_wait(kWaitLimitNs, &full[slot], phase)) {
       flag_failure(a.status);
       return;
     }

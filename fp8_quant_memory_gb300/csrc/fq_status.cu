@@ -2,6 +2,7 @@
 // in a pipelined kernel) set bit 0 here instead of trapping when a wait gives up, so the context
 // stays usable and the host can read the failure with fq_device_status().
 #include "fq_internal.h"
+#include "fq_sync.cuh"
 
 namespace fq {
 
@@ -23,6 +24,25 @@ cudaError_t read_device_status(unsigned int* word, int clear, cudaStream_t s) {
   e = cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(unsigned int), 0, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return e;
   return cudaStreamSynchronize(s);
+}
+
+// One block whose only mbarrier wait can never complete (nothing arrives on the barrier): the wait
+// ends by giving up after `limit_ns` and reports through the status word, the same path a stalled
+// pipeline stage takes in the production kernels.
+__global__ void wait_probe_kernel(unsigned int* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    if (!mbar_wait(limit_ns, &bar, 0u)) flag_failure(status);
+  }
+}
+
+cudaError_t launch_wait_probe(unsigned int limit_ms, cudaStream_t s) {
+  unsigned int* status = device_status_ptr();
+  if (status == nullptr) return cudaErrorInvalidSymbol;
+  wait_probe_kernel<<<1, 32, 0, s>>>(status, static_cast<uint64_t>(limit_ms) * 1000000ull);
+  return cudaGetLastError();
 }
 
 }  // namespace fq

@@ -64,6 +64,14 @@ int fq_version(void);
  * remaining work. `*word` receives the bits. Returns FQ_OK or FQ_ERR_CUDA. */
 int fq_device_status(unsigned int* word, int clear, cudaStream_t stream);
 
+/* Diagnostic for the bounded waits of the pipelined kernels: enqueues one block whose single
+ * mbarrier wait can never complete (nothing arrives on the barrier). The wait gives up after
+ * limit_ms milliseconds (1..10000) and sets bit 0 of the device status word -- the path a stalled
+ * pipeline stage takes -- instead of hanging or trapping; the context stays usable. After the
+ * stream reaches it, fq_device_status reports bit 0 set. Returns FQ_OK, FQ_ERR_INVALID_ARG or
+ * FQ_ERR_CUDA. The tutorial pages have no counterpart (they have no pipelined kernel). */
+int fq_check_bounded_wait(unsigned int limit_ms, cudaStream_t stream);
+
 /*
  * RMSNorm forward ("rmsnorm_tl.py", _rmsnorm_fwd):
  *   rstd_i = 1 / sqrt(sum_j x_ij^2 / N + eps)   (fp32)

@@ -269,3 +269,24 @@ def test_prologue_tma_matches_generic_kernel(cuda_ok, monkeypatch):
     q2, s2 = fq.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], 32, 8)
     assert_scale_close(s1, s2.cpu(), rel=1e-6)
     assert_codes_close(q1, q2.cpu())
+
+
+# ----------------------------------------------------------------------------------- failure detection
+def test_bounded_wait_gives_up_and_context_stays_usable(orc, cuda_ok):
+    """A wait that nothing completes ends after its limit and reports through the status word; the
+    next calls on the same context run and are correct."""
+    import time
+
+    t0 = time.perf_counter()
+    word = fq.check_bounded_wait(50)
+    elapsed = time.perf_counter() - t0
+    assert word & 1
+    assert 0.04 <= elapsed < 5.0
+    assert fq.device_status(clear=True) == 0
+    d = wl.qk_inputs(64, 8, 2, 128, seed=880)
+    q_ref, s_ref = orc.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], 8, 2)
+    g = cuda(d)
+    q, s = fq.qk_norm_rope_quant(g["qk"], g["wq"], g["wk"], g["cos"], g["sin"], 8, 2)
+    assert_scale_close(s, s_ref)
+    assert_codes_close(q, q_ref)
+    assert fq.device_status(clear=True) == 0
