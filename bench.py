@@ -504,6 +504,24 @@ def run_reference(args):
     return 0
 
 
+SECONDARY = {
+    "rmsnorm_fwd_8k_4k": lambda dev: RmsnormFwdCase(dev),
+    "rmsnorm_bwd_8k_4k": lambda dev: RmsnormBwdCase(dev),
+    "rope_fp16_64k": lambda dev: RopeCase(dev),
+    "rope_quant_tiny": lambda dev: RopeQuantTinyCase(dev),
+    "qk_prologue_32k": lambda dev: PrologueCase(dev, T=32768, Hq=64, Hk=8, std=1.0, theta=1e6, positions="uniform",
+                                                outlier_frac=0.01, n_sets=2, seed=20261202 + 4),
+}
+
+
+def time_secondary(c: Case, steps: int, warmup: int, stream, peak: float) -> dict:
+    ms, _ = time_case(c, steps, warmup, stream)
+    us = ms * 1e3 / steps
+    gbs = c.bytes_per_step() / (us * 1e-6) / 1e9
+    return {"workload": c.name, "us_per_step": round(us, 3), "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "bytes_per_step": c.bytes_per_step(), "kernels_per_step": c.kernels_per_step}
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -512,6 +530,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--workload", choices=["qk_prologue_4k", *SECONDARY], default="qk_prologue_4k",
+                    help="time one secondary workload alone (for profiling) instead of the benchmark step")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -536,6 +556,11 @@ def main():
 
     _capi.load()
     stream = torch.cuda.Stream(dev)
+    if args.workload != "qk_prologue_4k":
+        res = time_secondary(SECONDARY[args.workload](dev), args.steps, args.warmup, stream, peaks()[0])
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return 0
 
     case = PrologueCase(dev)
     sampler = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
@@ -573,18 +598,10 @@ def main():
         line["e2e"] = e2e_prologue(case, min(args.steps, 200), stream)
         if not args.no_extras:
             extras = []
-            for mk in (lambda: RmsnormFwdCase(dev), lambda: RmsnormBwdCase(dev), lambda: RopeCase(dev),
-                       lambda: RopeQuantTinyCase(dev),
-                       lambda: PrologueCase(dev, T=32768, Hq=64, Hk=8, std=1.0, theta=1e6, positions="uniform",
-                                            outlier_frac=0.01, n_sets=2, seed=20261202 + 4)):
-                c = mk()
+            for name, mk in SECONDARY.items():
+                c = mk(dev)
                 k = 2000 if c.bytes_per_step() < 3e8 else 400
-                m2, _ = time_case(c, k, 16, stream)
-                us = m2 * 1e3 / k
-                gbs = c.bytes_per_step() / (us * 1e-6) / 1e9
-                extras.append({"workload": c.name, "us_per_step": round(us, 3), "GB/s": round(gbs, 1),
-                               "frac": round(gbs / peak, 4), "bytes_per_step": c.bytes_per_step(),
-                               "kernels_per_step": c.kernels_per_step})
+                extras.append(time_secondary(c, k, 16, stream, peak))
                 del c
                 torch.cuda.empty_cache()
             eager = TorchEagerPrologueCase(case)

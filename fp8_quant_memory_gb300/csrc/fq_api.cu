@@ -88,6 +88,8 @@ int launch_rows(const char* fn, const fq::RowArgs& a, int mode, int dtype, int t
   const bool tma_ok = !(pick != nullptr && std::string(pick) == "generic");
   if (vec && mode == fq::MODE_QK && tma_ok && fq::launch_prologue_tma(a, dtype, table_dtype, s))
     return check_launch(fn);
+  if (vec && (mode == fq::MODE_FWD || mode == fq::MODE_ROPE) && fq::launch_rows_tma(a, mode, dtype, table_dtype, s))
+    return check_launch(fn);
   if (!(vec && fq::launch_rows_vector(a, mode, dtype, table_dtype, s)))
     fq::launch_rows_scalar(a, mode, dtype, table_dtype, s);
   return check_launch(fn);

@@ -30,8 +30,9 @@ __device__ __forceinline__ float team_sum_shfl(float v) {
   return group_sum<(TPR < 32 ? TPR : 32)>(v);
 }
 
+// Two CTAs per SM (at most 128 registers) keep all <= 256 chunk CTAs resident in one wave.
 template <typename T, int TPR, int VPT, int RB>
-__global__ void __launch_bounds__(kThreads) bwd_stage1_kernel(const BwdArgs a, int64_t rows_per_chunk) {
+__global__ void __launch_bounds__(kThreads, 2) bwd_stage1_kernel(const BwdArgs a, int64_t rows_per_chunk) {
   constexpr int G = kThreads / TPR;               // row teams per CTA
   constexpr int WPT = TPR > 32 ? TPR / 32 : 1;    // warps per team
   __shared__ float red[2][G][WPT][2 * RB];        // cross-warp row sums (TPR > 32), double buffered
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(kThreads) bwd_stage1_kernel(const BwdArgs a, i
         uint32_t pk[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float2 xn = mul2(Elem<T>::unpack(word(xv[b][k], e)), rstd2);
-          const float2 gf = Elem<T>::unpack(word(gv[b][k], e));
+          const float2 xn = mul2(unpack_again<T>(word(xv[b][k], e)), rstd2);
+          const float2 gf = unpack_again<T>(word(gv[b][k], e));
           const float2 gw = mul2(gf, wf[k][e]);
           const float2 d = sub2(gw, mul2(xn, c2));
           pk[e] = Elem<T>::pack(mul2(rstd2, d));
@@ -174,37 +175,66 @@ __global__ void __launch_bounds__(kThreads) bwd_stage1_kernel(const BwdArgs a, i
   }
 }
 
-// Stage 2: dw[j] = sum over chunks (in order) of partial[chunk, j]. One CTA per 32 columns; warp w
-// adds chunks w, w+8, ... in order, then warp 0 adds the 8 warp sums in order.
+// Stage 2: dw[j] = sum over chunks of partial[chunk, j] in a fixed order. One CTA per 32 columns:
+// thread (k, c4) with k in [0, 32) and c4 in [0, 8) adds chunks k, k+32, k+64, ... (in order, all
+// loads in flight) for columns 4*c4..4*c4+3 of the CTA's 32; the 32 partial sums per column are
+// then added in k order. The order depends on nothing but M and N: dw is reproducible bit for bit.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
     bwd_stage2_kernel(const float* partial, int64_t chunks, int N, void* dw, float* dw_f32) {
-  __shared__ float part[kThreads / 32][32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int j = blockIdx.x * 32 + lane;
-  float s = 0.f;
-  if (j < N) {
-    int64_t c = warp;
-    for (; c + 3 * 8 < chunks; c += 4 * 8) {
-      const float p0 = partial[c * N + j];
-      const float p1 = partial[(c + 8) * N + j];
-      const float p2 = partial[(c + 16) * N + j];
-      const float p3 = partial[(c + 24) * N + j];
-      s += p0;
-      s += p1;
-      s += p2;
-      s += p3;
-    }
-    for (; c < chunks; c += 8) s += partial[c * N + j];
-  }
-  part[warp][lane] = s;
-  __syncthreads();
-  if (warp == 0 && j < N) {
-    float tot = 0.f;
+  constexpr int kStreams = kThreads / 8;  // 32 chunk streams
+  __shared__ float part[kStreams][33];
+  const int c4 = threadIdx.x & 7;
+  const int k = threadIdx.x >> 3;
+  const int j0 = blockIdx.x * 32 + 4 * c4;
+  float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (j0 < N) {
+    const bool vec = (N % 4 == 0);
+    int64_t c = k;
+    for (; c + 7 * kStreams < chunks; c += 8 * kStreams) {
+      float4 p[8];
 #pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) tot += part[w][lane];
-    if (dw_f32) dw_f32[j] = tot;
-    Elem<T>::store1(dw, j, tot);
+      for (int u = 0; u < 8; ++u) {
+        const float* src = partial + (c + u * kStreams) * N + j0;
+        if (vec) {
+          p[u] = *reinterpret_cast<const float4*>(src);
+        } else {
+          p[u].x = src[0];
+          p[u].y = j0 + 1 < N ? src[1] : 0.f;
+          p[u].z = j0 + 2 < N ? src[2] : 0.f;
+          p[u].w = j0 + 3 < N ? src[3] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        sum.x += p[u].x;
+        sum.y += p[u].y;
+        sum.z += p[u].z;
+        sum.w += p[u].w;
+      }
+    }
+    for (; c < chunks; c += kStreams) {
+      const float* src = partial + c * N + j0;
+      sum.x += src[0];
+      sum.y += j0 + 1 < N ? src[1] : 0.f;
+      sum.z += j0 + 2 < N ? src[2] : 0.f;
+      sum.w += j0 + 3 < N ? src[3] : 0.f;
+    }
+  }
+  part[k][4 * c4 + 0] = sum.x;
+  part[k][4 * c4 + 1] = sum.y;
+  part[k][4 * c4 + 2] = sum.z;
+  part[k][4 * c4 + 3] = sum.w;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    const int j = blockIdx.x * 32 + threadIdx.x;
+    if (j < N) {
+      float tot = 0.f;
+#pragma unroll
+      for (int q = 0; q < kStreams; ++q) tot += part[q][threadIdx.x];
+      if (dw_f32) dw_f32[j] = tot;
+      Elem<T>::store1(dw, j, tot);
+    }
   }
 }
 

@@ -59,6 +59,28 @@ struct Elem<float> {
   }
 };
 
+// The same conversions as Elem<T>::unpack, written in PTX. A kernel that needs a packed vector
+// unpacked twice (before and after a reduction) uses this for the second time: the compiler cannot
+// merge it with the first, so the first set of floats dies early instead of occupying registers.
+template <typename T>
+__device__ __forceinline__ float2 unpack_again(uint32_t u);
+
+template <>
+__device__ __forceinline__ float2 unpack_again<__nv_bfloat16>(uint32_t u) {
+  float lo, hi;
+  asm("shl.b32 %0, %2, 16;\n\tand.b32 %1, %2, 0xffff0000;" : "=f"(lo), "=f"(hi) : "r"(u));
+  return make_float2(lo, hi);
+}
+
+template <>
+__device__ __forceinline__ float2 unpack_again<__half>(uint32_t u) {
+  float lo, hi;
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\tcvt.f32.f16 %0, l;\n\tcvt.f32.f16 %1, h;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(u));
+  return make_float2(lo, hi);
+}
+
 // Round a float2 to the storage format and back (the `.to(dtype)` cast of the definition).
 template <typename T>
 __device__ __forceinline__ float2 round_trip(float2 v) {

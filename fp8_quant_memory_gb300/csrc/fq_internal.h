@@ -46,6 +46,10 @@ bool launch_rows_vector(const RowArgs& a, int mode, int dtype, int table_dtype, 
 // dtype fp32 or the storage dtype). Returns false (launching nothing) when it does not apply.
 bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s);
 
+// TMA-fed row-stream kernels for MODE_FWD and MODE_ROPE over contiguous rows (>= 4096 rows, the
+// vectorised-path layout rules). Returns false (launching nothing) when they do not apply.
+bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s);
+
 // Scalar path: any N >= 1, even R, any alignment, any dtype combination.
 void launch_rows_scalar(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s);
 

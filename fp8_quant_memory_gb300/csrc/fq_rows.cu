@@ -16,49 +16,21 @@
 // Reductions (sum of squares, amax) are group shuffles.
 #include "fq_device.cuh"
 #include "fq_internal.h"
+#include "fq_rows.cuh"
 
 namespace fq {
 namespace {
 
+using namespace rows;
+
 constexpr int kThreads = 256;
 
-__device__ __forceinline__ uint32_t word(const uint4& v, int k) {
-  return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
-}
-
-__device__ __forceinline__ void set_word(uint4& v, int k, uint32_t u) {
-  if (k == 0) v.x = u;
-  else if (k == 1) v.y = u;
-  else if (k == 2) v.z = u;
-  else v.w = u;
-}
-
-// 8 consecutive table entries starting at element `off` -> 4 float2 (entries 2k, 2k+1 in [k]).
-template <typename TT>
-__device__ __forceinline__ void load_table8(const void* base, int64_t off, float2 (&v)[4]) {
-  if constexpr (sizeof(TT) == 4) {
-    const float* p = static_cast<const float*>(base) + off;
-    const float4 a = ld_cached16f(p);
-    const float4 b = ld_cached16f(p + 4);
-    v[0] = make_float2(a.x, a.y);
-    v[1] = make_float2(a.z, a.w);
-    v[2] = make_float2(b.x, b.y);
-    v[3] = make_float2(b.z, b.w);
-  } else {
-    const uint4 u = ld_cached16(static_cast<const TT*>(base) + off);
-    v[0] = Elem<TT>::unpack(u.x);
-    v[1] = Elem<TT>::unpack(u.y);
-    v[2] = Elem<TT>::unpack(u.z);
-    v[3] = Elem<TT>::unpack(u.w);
-  }
-}
-
-template <typename T, typename TT, int MODE, int LPR, int HS, int TS>
+// U rows per lane group per iteration: all U rows' loads are issued before any of them is used,
+// so a warp keeps U times the bytes in flight (narrow rows need it to cover HBM latency).
+template <typename T, typename TT, int MODE, int LPR, int HS, int TS, int U>
 __global__ void __launch_bounds__(kThreads) rows_vec_kernel(const RowArgs a) {
-  constexpr bool kQuant = (MODE == MODE_ROPE_QUANT) || (MODE == MODE_QK);
-  constexpr bool kRound = (MODE == MODE_ROPE) || (MODE == MODE_ROPE_QUANT);
   constexpr int kRowsPerCta = kThreads / LPR;
-  constexpr int kV = HS + 2 * TS;  // vector slots per lane: head..., tail-lo..., tail-hi...
+  constexpr int kV = HS + 2 * TS;
 
   const int lane = threadIdx.x & (LPR - 1);
   const int grp = threadIdx.x / LPR;
@@ -68,162 +40,114 @@ __global__ void __launch_bounds__(kThreads) rows_vec_kernel(const RowArgs a) {
   const int half = a.R >> 1;
   const float fN = static_cast<float>(N);
 
-  int col[kV];
-  bool ok[kV];
-#pragma unroll
-  for (int s = 0; s < HS; ++s) {
-    const int v = lane + s * LPR;
-    col[s] = 8 * v;
-    ok[s] = v < hv;
-  }
-#pragma unroll
-  for (int s = 0; s < TS; ++s) {
-    const int p = lane + s * LPR;
-    col[HS + s] = 8 * (hv + p);
-    col[HS + TS + s] = 8 * (hv + th + p);
-    ok[HS + s] = ok[HS + TS + s] = p < th;
-  }
-
   const int32_t rows = static_cast<int32_t>(a.rows);
-  for (int32_t base = blockIdx.x * kRowsPerCta; base < rows; base += gridDim.x * kRowsPerCta) {
-    const int32_t r = base + grp;
-    const bool rv = r < rows;
-    int32_t t = r, h = 0;
-    if constexpr (MODE == MODE_QK) {
-      t = r / a.H;
-      h = r - t * a.H;
-    }
-    const T* xrow = static_cast<const T*>(a.x) + (static_cast<int64_t>(t) * a.token_stride +
-                                                    static_cast<int64_t>(h) * N);
-    uint4 xv[kV];
+  for (int32_t base = blockIdx.x * (kRowsPerCta * U); base < rows; base += gridDim.x * (kRowsPerCta * U)) {
+    int32_t r[U], t[U], h[U];
+    bool rv[U];
+    uint4 xv[U][kV];
 #pragma unroll
-    for (int s = 0; s < kV; ++s)
-      xv[s] = (rv && ok[s]) ? ld_stream16(xrow + col[s]) : make_uint4(0u, 0u, 0u, 0u);
-
-    // a2: sum of squares -> rstd
-    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int s = 0; s < kV; ++s)
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = Elem<T>::unpack(word(xv[s], k));
-        acc = fma2(f, f, acc);
+    for (int u = 0; u < U; ++u) {
+      r[u] = base + u * kRowsPerCta + grp;
+      rv[u] = r[u] < rows;
+      t[u] = r[u];
+      h[u] = 0;
+      if constexpr (MODE == MODE_QK) {
+        t[u] = r[u] / a.H;
+        h[u] = r[u] - t[u] * a.H;
       }
-    const float ss = group_sum<LPR>(acc.x + acc.y);
-    const float rstd = rstd_from_ss(ss, fN, a.eps);
+      const T* xrow = static_cast<const T*>(a.x) + (static_cast<int64_t>(t[u]) * a.token_stride +
+                                                      static_cast<int64_t>(h[u]) * N);
+#pragma unroll
+      for (int s = 0; s < kV; ++s)
+        xv[u][s] = (rv[u] && slot_ok<LPR, HS, TS>(s, lane, hv, th))
+                       ? ld_stream16(xrow + slot_col<LPR, HS, TS>(s, lane, hv, th))
+                       : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      row_body<T, TT, MODE, LPR, HS, TS, false>(a, r[u], rv[u], h[u], xv[u], lane, hv, th, fN, a.cos, a.sin,
+                                                static_cast<int64_t>(t[u]) * half);
+  }
+}
+
+// Wide rows, RMSNorm forward: one warp per row in two passes. Pass 1 streams x (eight 16-byte
+// vectors per lane in flight) for the sum of squares; pass 2 reads the row again -- it was just
+// fetched, so it comes from L2, not HBM -- and writes y. Holding a 4096-wide row in registers
+// would cost ~150 registers per thread and one CTA per SM; this keeps a few dozen.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) rows_wide_fwd_kernel(const RowArgs a) {
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kBatch = 8;   // pass 1: vectors per lane in flight (HBM latency)
+  constexpr int kBatch2 = 4;  // pass 2: the row comes back from L2
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int N = a.N;
+  const int nv = N >> 3;
+  const float fN = static_cast<float>(N);
+  const T* w = static_cast<const T*>(a.wq);
+  const int32_t rows = static_cast<int32_t>(a.rows);
+  for (int32_t r = blockIdx.x * kWarps + warp; r < rows; r += gridDim.x * kWarps) {  // warp-uniform
+    const T* xrow = static_cast<const T*>(a.x) + static_cast<int64_t>(r) * N;
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    for (int v0 = lane; v0 < nv; v0 += 32 * kBatch) {
+      uint4 xv[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const int v = v0 + 32 * b;
+        xv[b] = v < nv ? __ldg(reinterpret_cast<const uint4*>(xrow + 8 * v)) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        const float2 f0 = Elem<T>::unpack(xv[b].x), f1 = Elem<T>::unpack(xv[b].y);
+        const float2 f2 = Elem<T>::unpack(xv[b].z), f3 = Elem<T>::unpack(xv[b].w);
+        acc0 = fma2(f0, f0, acc0);
+        acc1 = fma2(f1, f1, acc1);
+        acc0 = fma2(f2, f2, acc0);
+        acc1 = fma2(f3, f3, acc1);
+      }
+    }
+    const float2 acc = add2(acc0, acc1);
+    const float rstd = rstd_from_ss(group_sum<32>(acc.x + acc.y), fN, a.eps);
     const float2 rstd2 = splat2(rstd);
-    const T* wrow = static_cast<const T*>((MODE == MODE_QK && h >= a.Hq) ? a.wk : a.wq);
-
-    uint4 yp[kV];       // rounded y (storage dtype), kRound and MODE_FWD
-    float2 yf[kV][4];   // fp32 y, MODE_QK
-    float amax = 0.f;
-
-    // a3: head columns, normalised (and rounded unless MODE_QK)
+    T* yrow = static_cast<T*>(a.y) + static_cast<int64_t>(r) * N;
+    for (int v0 = lane; v0 < nv; v0 += 32 * kBatch2) {
+      uint4 xv[kBatch2], wv[kBatch2];
 #pragma unroll
-    for (int s = 0; s < HS; ++s) {
-      if (!ok[s]) {
-        yp[s] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) yf[s][k] = make_float2(0.f, 0.f);
-        continue;
-      }
-      const uint4 wv = ld_cached16(wrow + col[s]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 n = mul2(mul2(Elem<T>::unpack(word(xv[s], k)), rstd2), Elem<T>::unpack(word(wv, k)));
-        if constexpr (MODE == MODE_QK) {
-          yf[s][k] = n;
-        } else {
-          const uint32_t pk = Elem<T>::pack(n);
-          set_word(yp[s], k, pk);
-          if constexpr (kQuant) {
-            const float2 rn = Elem<T>::unpack(pk);
-            amax = absmax4(amax, rn, make_float2(0.f, 0.f));
-          }
+      for (int b = 0; b < kBatch2; ++b) {
+        const int v = v0 + 32 * b;
+        if (v < nv) {
+          xv[b] = ld_stream16(xrow + 8 * v);
+          wv[b] = ld_cached16(w + 8 * v);
         }
       }
-      if constexpr (MODE == MODE_QK) amax = absmax4(absmax4(amax, yf[s][0], yf[s][1]), yf[s][2], yf[s][3]);
-    }
-
-    // a4: rotary pairs
-    if constexpr (TS > 0) {
-      const int64_t trow = static_cast<int64_t>(t) * half;
 #pragma unroll
-      for (int s = 0; s < TS; ++s) {
-        const int slo = HS + s, shi = HS + TS + s;
-        if (!ok[slo]) {
-          yp[slo] = yp[shi] = make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) yf[slo][k] = yf[shi][k] = make_float2(0.f, 0.f);
-          continue;
-        }
-        const int p8 = 8 * (lane + s * LPR);  // pair index of the vector's first element
-        const uint4 wlo = ld_cached16(wrow + col[slo]);
-        const uint4 whi = ld_cached16(wrow + col[shi]);
-        float2 c[4], sn[4];
-        load_table8<TT>(a.cos, trow + p8, c);
-        load_table8<TT>(a.sin, trow + p8, sn);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float2 lo = mul2(mul2(Elem<T>::unpack(word(xv[slo], k)), rstd2), Elem<T>::unpack(word(wlo, k)));
-          float2 hi = mul2(mul2(Elem<T>::unpack(word(xv[shi], k)), rstd2), Elem<T>::unpack(word(whi, k)));
-          if constexpr (kRound) {
-            lo = round_trip<T>(lo);
-            hi = round_trip<T>(hi);
-          }
-          float2 ylo = sub2(mul2(lo, c[k]), mul2(hi, sn[k]));
-          float2 yhi = add2(mul2(hi, c[k]), mul2(lo, sn[k]));
-          if constexpr (MODE == MODE_QK) {
-            yf[slo][k] = ylo;
-            yf[shi][k] = yhi;
-          } else {
-            const uint32_t plo = Elem<T>::pack(ylo), phi = Elem<T>::pack(yhi);
-            set_word(yp[slo], k, plo);
-            set_word(yp[shi], k, phi);
-            if constexpr (kQuant) amax = absmax4(amax, Elem<T>::unpack(plo), Elem<T>::unpack(phi));
-          }
-        }
-        if constexpr (MODE == MODE_QK) {
-          amax = absmax4(absmax4(amax, yf[slo][0], yf[slo][1]), yf[slo][2], yf[slo][3]);
-          amax = absmax4(absmax4(amax, yf[shi][0], yf[shi][1]), yf[shi][2], yf[shi][3]);
-        }
-      }
-    }
-
-    // a5: y
-    if constexpr (MODE != MODE_QK) {
-      if (a.y != nullptr && rv) {
-        T* yrow = static_cast<T*>(a.y) + static_cast<int64_t>(r) * N;
-#pragma unroll
-        for (int s = 0; s < kV; ++s)
-          if (ok[s]) st_stream16(yrow + col[s], yp[s]);
-      }
-    }
-
-    // a6-a8: scale and codes
-    if constexpr (kQuant) {
-      amax = fmaxf(group_max<LPR>(amax), 1e-4f);
-      const float sc = __fdiv_rn(amax, a.fp8_max);
-      const float rc = __frcp_rn(sc);
-      const bool clamp = a.fp8_max != 448.0f;
-      if (rv) {
-        uint8_t* qrow = a.q + static_cast<int64_t>(r) * N;
-#pragma unroll
-        for (int s = 0; s < kV; ++s) {
-          if (!ok[s]) continue;
-          float2 v[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 yy = (MODE == MODE_QK) ? yf[s][k] : Elem<T>::unpack(word(yp[s], k));
-            v[k] = div2_by(yy, sc, rc);
-            if (clamp) v[k] = make_float2(clamp_abs(v[k].x, a.fp8_max), clamp_abs(v[k].y, a.fp8_max));
-          }
-          st_stream8(qrow + col[s], pack_e4m3x8(v[0], v[1], v[2], v[3]));
-        }
-        if (lane == 0) a.scale[r] = sc;
+      for (int b = 0; b < kBatch2; ++b) {
+        const int v = v0 + 32 * b;
+        if (v >= nv) continue;
+        uint4 out;
+        out.x = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(xv[b].x), rstd2), Elem<T>::unpack(wv[b].x)));
+        out.y = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(xv[b].y), rstd2), Elem<T>::unpack(wv[b].y)));
+        out.z = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(xv[b].z), rstd2), Elem<T>::unpack(wv[b].z)));
+        out.w = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(xv[b].w), rstd2), Elem<T>::unpack(wv[b].w)));
+        st_stream16(yrow + 8 * v, out);
       }
     }
   }
+}
+
+template <typename T>
+bool launch_wide_fwd(const RowArgs& a, cudaStream_t s) {
+  auto kern = rows_wide_fwd_kernel<T>;
+  static int blocks_per_sm = -1;
+  if (blocks_per_sm < 0) {
+    int b = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kThreads, 0) != cudaSuccess || b < 1) b = 1;
+    blocks_per_sm = b;
+  }
+  const int64_t need = (a.rows + kThreads / 32 - 1) / (kThreads / 32);
+  const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
+  kern<<<static_cast<int>(need < cap ? need : cap), kThreads, 0, s>>>(a);
+  return true;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -235,14 +159,17 @@ struct Shape {
 
 template <typename T, typename TT, int MODE, int LPR, int HS, int TS>
 bool launch_one(const RowArgs& a, cudaStream_t s) {
-  auto kern = rows_vec_kernel<T, TT, MODE, LPR, HS, TS>;
+  // One row per lane group per iteration: two (all loads first) measured slower on the narrow-row
+  // workloads (fewer CTAs, more registers); U stays a template parameter for experiments.
+  constexpr int U = 1;
+  auto kern = rows_vec_kernel<T, TT, MODE, LPR, HS, TS, U>;
   static int blocks_per_sm = -1;
   if (blocks_per_sm < 0) {
     int b = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kThreads, 0) != cudaSuccess || b < 1) b = 1;
     blocks_per_sm = b;
   }
-  constexpr int kRowsPerCta = kThreads / LPR;
+  constexpr int kRowsPerCta = (kThreads / LPR) * U;
   const int64_t need = (a.rows + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
   const int grid = static_cast<int>(need < cap ? need : cap);
@@ -278,6 +205,7 @@ bool dispatch_shape(const RowArgs& a, cudaStream_t s) {
 
 template <typename T, int MODE>
 bool dispatch_table(const RowArgs& a, int table_dtype, cudaStream_t s) {
+  if (MODE == MODE_FWD && a.N >= 1024) return launch_wide_fwd<T>(a, s);
   if (MODE == MODE_FWD || a.R == 0) return dispatch_shape<T, T, MODE>(a, s);
   if (table_dtype == DT_FP32) return dispatch_shape<T, float, MODE>(a, s);
   return dispatch_shape<T, T, MODE>(a, s);  // caller checked table_dtype == dtype

@@ -1,0 +1,323 @@
+// fq_rows_tma.cu -- TMA-fed persistent kernels for RMSNorm forward and RMSNorm + NeoX partial RoPE
+// over contiguous rows ("rmsnorm_tl.py" (Ch.17), _rmsnorm_fwd; "rmsnorm_rope_quant.py" (Ch.13
+// fusion), rms_norm_rope_fused / torch_reference_fused).
+//
+// Every CTA owns a contiguous, row-balanced range of rows. One producer lane streams it through a
+// ring of shared-memory stages with cp.async.bulk: a stage is SR consecutive x rows (one bulk copy)
+// and, with rotation, their SR cos and SR sin table rows (the tables of these calls have one row per
+// x row); an mbarrier counts the bytes and every wait is bounded (fq_sync.cuh). Bytes in flight do
+// not depend on registers, which is what the register-hungry, latency-bound global-load kernels
+// lacked. Eight consumer warps read x from the stage:
+//   - narrow rows: the lane-group layout and arithmetic of the generic row kernel (fq_rows.cuh),
+//     one row per lane group per stage, tables read from the stage;
+//   - wide rows (RMSNorm forward, N >= 1024): one warp per row, two passes over the staged row (sum
+//     of squares, then normalise and store), so registers stay low.
+// y is written with 16-byte evict-first stores. x and the tables are read from HBM exactly once.
+#include "fq_device.cuh"
+#include "fq_internal.h"
+#include "fq_rows.cuh"
+#include "fq_sync.cuh"
+
+namespace fq {
+namespace {
+
+using namespace rows;
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+struct StreamArgs {
+  RowArgs a;
+  unsigned int* status;
+  int32_t stages;       // ring depth
+  int32_t stage_bytes;  // x block + 2 table blocks, multiple of 128
+  int32_t tab_off;      // byte offset of the cos block in a stage (0 when there is no rotation)
+  int32_t tab_block;    // bytes of one table block
+  int32_t depth;        // the producer keeps at most this many stages in flight
+};
+
+// Producer: one lane streams the CTA's stages. Returns after issuing everything (or giving up).
+__device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem, uint64_t* full, uint64_t* empty,
+                                        int32_t r0, int32_t r1, int SR, int esize, int tsize) {
+  const RowArgs& a = p.a;
+  const int S = p.stages;
+  const int nst = (r1 - r0 + SR - 1) / SR;
+  const uint32_t xrow = static_cast<uint32_t>(a.N) * esize;
+  const uint32_t trow = static_cast<uint32_t>(a.R / 2) * tsize;
+  int slot = 0, dslot = 0;
+  uint32_t phase = 0, dphase = 0;
+  int k = 0;
+  bool ok = true;
+  for (; k < nst; ++k) {
+    if (k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) {
+      ok = false;
+      break;
+    }
+    if (k >= p.depth) {
+      if (!mbar_wait(kWaitLimitNs, &full[dslot], dphase)) {
+        ok = false;
+        break;
+      }
+      if (++dslot == S) {
+        dslot = 0;
+        dphase ^= 1u;
+      }
+    }
+    const int32_t rs = r0 + k * SR;
+    const uint32_t nr = static_cast<uint32_t>(min(SR, r1 - rs));
+    unsigned char* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
+    const uint32_t tb = (a.R > 0) ? nr * trow : 0u;
+    mbar_arrive_expect_tx(&full[slot], nr * xrow + 2u * tb);
+    bulk_g2s(st, static_cast<const unsigned char*>(a.x) + static_cast<int64_t>(rs) * xrow, nr * xrow, &full[slot]);
+    if (tb > 0) {
+      bulk_g2s(st + p.tab_off, static_cast<const unsigned char*>(a.cos) + static_cast<int64_t>(rs) * trow, tb,
+               &full[slot]);
+      bulk_g2s(st + p.tab_off + p.tab_block,
+               static_cast<const unsigned char*>(a.sin) + static_cast<int64_t>(rs) * trow, tb, &full[slot]);
+    }
+    if (++slot == S) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+  if (!ok) {
+    flag_failure(p.status);
+    for (int j = max(0, k - S); j < k; ++j)
+      if (!mbar_wait(kWaitLimitNs, &full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
+  }
+}
+
+// Shared set-up of both kernels: ring layout, barriers, programmatic-launch handshake. Returns the
+// CTA's row range.
+struct Ring {
+  unsigned char* smem;
+  uint64_t* full;
+  uint64_t* empty;
+  int32_t r0, r1;
+};
+
+__device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* smem_raw) {
+  Ring g;
+  const uint32_t raw = smem_addr(smem_raw);
+  g.smem = smem_raw + ((128u - (raw & 127u)) & 127u);
+  g.full = reinterpret_cast<uint64_t*>(g.smem + static_cast<size_t>(p.stages) * p.stage_bytes);
+  g.empty = g.full + p.stages;
+  g.r0 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x) * p.a.rows) / gridDim.x);
+  g.r1 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x + 1) * p.a.rows) / gridDim.x);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(&g.full[s], 1);
+      mbar_init(&g.empty[s], kConsumerWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  return g;
+}
+
+// ---------------------------------------------------------------------------------- narrow rows
+template <typename T, typename TT, int MODE, int LPR, int HS, int TS>
+__global__ void __launch_bounds__(kThreads) rows_tma_kernel(const StreamArgs p) {
+  extern __shared__ unsigned char smem_raw[];
+  constexpr int kV = HS + 2 * TS;
+  constexpr int SR = kConsumerWarps * (32 / LPR);  // one row per lane group per stage
+  const Ring g = ring_setup(p, smem_raw);
+  const RowArgs& a = p.a;
+  const int warp = threadIdx.x >> 5, lane32 = threadIdx.x & 31;
+  if (warp == kConsumerWarps) {
+    if (lane32 == 0) produce(p, g.smem, g.full, g.empty, g.r0, g.r1, SR, sizeof(T), sizeof(TT));
+    return;
+  }
+  const int lane = lane32 & (LPR - 1);
+  const int l = warp * (32 / LPR) + lane32 / LPR;  // row within each stage
+  const int N = a.N;
+  const int hv = (N - a.R) >> 3, th = a.R >> 4, half = a.R >> 1;
+  const float fN = static_cast<float>(N);
+  const int nst = (g.r1 - g.r0 + SR - 1) / SR;
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int k = 0; k < nst; ++k) {
+    if (!mbar_wait(kWaitLimitNs, &g.full[slot], phase)) {
+      flag_failure(p.status);
+      return;
+    }
+    const unsigned char* st = g.smem + static_cast<size_t>(slot) * p.stage_bytes;
+    const int32_t rs = g.r0 + k * SR;
+    const bool live = l < g.r1 - rs;
+    const int lr = live ? l : 0;  // dead lane groups read row 0 of the stage (always present)
+    const T* xs = reinterpret_cast<const T*>(st) + static_cast<int64_t>(lr) * N;
+    uint4 xv[kV];
+#pragma unroll
+    for (int s = 0; s < kV; ++s)
+      xv[s] = slot_ok<LPR, HS, TS>(s, lane, hv, th)
+                  ? *reinterpret_cast<const uint4*>(xs + slot_col<LPR, HS, TS>(s, lane, hv, th))
+                  : make_uint4(0u, 0u, 0u, 0u);
+    row_body<T, TT, MODE, LPR, HS, TS, true>(a, rs + l, live, 0, xv, lane, hv, th, fN, st + p.tab_off,
+                                              st + p.tab_off + p.tab_block, static_cast<int64_t>(lr) * half);
+    __syncwarp();
+    if (lane32 == 0) mbar_arrive(&g.empty[slot]);  // x and this stage's table rows have been read
+    if (++slot == p.stages) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------- wide rows
+template <typename T>
+__global__ void __launch_bounds__(kThreads) rows_tma_wide_fwd_kernel(const StreamArgs p) {
+  extern __shared__ unsigned char smem_raw[];
+  constexpr int SR = kConsumerWarps;  // one row per warp per stage
+  const Ring g = ring_setup(p, smem_raw);
+  const RowArgs& a = p.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kConsumerWarps) {
+    if (lane == 0) produce(p, g.smem, g.full, g.empty, g.r0, g.r1, SR, sizeof(T), 2);
+    return;
+  }
+  const int N = a.N, nv = N >> 3;
+  const float fN = static_cast<float>(N);
+  const T* w = static_cast<const T*>(a.wq);
+  const int nst = (g.r1 - g.r0 + SR - 1) / SR;
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int k = 0; k < nst; ++k) {
+    if (!mbar_wait(kWaitLimitNs, &g.full[slot], phase)) {
+      flag_failure(p.status);
+      return;
+    }
+    const int32_t r = g.r0 + k * SR + warp;
+    if (r < g.r1) {  // warp-uniform
+      const T* xs = reinterpret_cast<const T*>(g.smem + static_cast<size_t>(slot) * p.stage_bytes) +
+                    static_cast<int64_t>(warp) * N;
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      for (int v = lane; v < nv; v += 32) {
+        const uint4 u = *reinterpret_cast<const uint4*>(xs + 8 * v);
+        const float2 f0 = Elem<T>::unpack(u.x), f1 = Elem<T>::unpack(u.y);
+        const float2 f2 = Elem<T>::unpack(u.z), f3 = Elem<T>::unpack(u.w);
+        acc0 = fma2(f0, f0, acc0);
+        acc1 = fma2(f1, f1, acc1);
+        acc0 = fma2(f2, f2, acc0);
+        acc1 = fma2(f3, f3, acc1);
+      }
+      const float2 acc = add2(acc0, acc1);
+      const float2 rstd2 = splat2(rstd_from_ss(group_sum<32>(acc.x + acc.y), fN, a.eps));
+      T* yrow = static_cast<T*>(a.y) + static_cast<int64_t>(r) * N;
+      for (int v = lane; v < nv; v += 32) {
+        const uint4 u = *reinterpret_cast<const uint4*>(xs + 8 * v);
+        const uint4 wv = ld_cached16(w + 8 * v);
+        uint4 out;
+        out.x = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.x), rstd2), Elem<T>::unpack(wv.x)));
+        out.y = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.y), rstd2), Elem<T>::unpack(wv.y)));
+        out.z = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.z), rstd2), Elem<T>::unpack(wv.z)));
+        out.w = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.w), rstd2), Elem<T>::unpack(wv.w)));
+        st_stream16(yrow + 8 * v, out);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&g.empty[slot]);
+    if (++slot == p.stages) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------- host side
+template <typename K>
+bool launch_stream(K kern, StreamArgs p, int stage_rows, int x_row_bytes, int tab_row_bytes, cudaStream_t s) {
+  const RowArgs& a = p.a;
+  p.status = device_status_ptr();
+  p.tab_block = ((stage_rows * tab_row_bytes) + 127) & ~127;
+  p.tab_off = (stage_rows * x_row_bytes + 127) & ~127;
+  p.stage_bytes = p.tab_off + 2 * p.tab_block;
+  // Two CTAs per SM when stages are small; as many stages as fit, at most 8.
+  const int budget = p.stage_bytes <= 32 * 1024 ? 110 * 1024 : 220 * 1024;
+  p.stages = (budget - 256) / p.stage_bytes;
+  if (p.stages > 8) p.stages = 8;
+  if (p.stages < 2) return false;
+  // Keep about 48 KB in flight per CTA (at least two stages), never more than the ring.
+  p.depth = (48 * 1024 + p.stage_bytes - 1) / p.stage_bytes;
+  if (p.depth < 2) p.depth = 2;
+  if (p.depth > p.stages) p.depth = p.stages;
+  const size_t smem = 128 + static_cast<size_t>(p.stages) * p.stage_bytes + 2 * p.stages * sizeof(uint64_t);
+  if (smem > 227 * 1024) return false;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return false;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
+    return false;
+  const int64_t want = (a.rows + stage_rows - 1) / stage_rows;
+  const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess;
+}
+
+template <typename T, typename TT, int MODE, int LPR, int HS, int TS>
+bool launch_narrow(const RowArgs& a, cudaStream_t s) {
+  StreamArgs p{};
+  p.a = a;
+  constexpr int SR = kConsumerWarps * (32 / LPR);
+  return launch_stream(rows_tma_kernel<T, TT, MODE, LPR, HS, TS>, p, SR, a.N * static_cast<int>(sizeof(T)),
+                       (a.R / 2) * static_cast<int>(sizeof(TT)), s);
+}
+
+template <typename T, typename TT, int MODE>
+bool dispatch_narrow(const RowArgs& a, cudaStream_t s) {
+  const int hv = (a.N - a.R) / 8, th = a.R / 16;
+#define FQ_TMA_TRY(L, H, S)                                       \
+  if (hv <= (L) * (H) && th <= (L) * (S) && ((S) > 0 || th == 0)) \
+    return launch_narrow<T, TT, MODE, L, H, S>(a, s);
+  if constexpr (MODE == MODE_FWD) {
+    FQ_TMA_TRY(8, 2, 0) FQ_TMA_TRY(16, 2, 0) FQ_TMA_TRY(32, 2, 0)
+  } else {
+    FQ_TMA_TRY(8, 0, 1) FQ_TMA_TRY(8, 2, 1) FQ_TMA_TRY(16, 2, 1) FQ_TMA_TRY(32, 2, 1) FQ_TMA_TRY(32, 4, 1)
+  }
+#undef FQ_TMA_TRY
+  return false;
+}
+
+}  // namespace
+
+bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s) {
+  if (a.rows < 4096 || a.rows > 0x7fffffffLL) return false;  // small problems: launch-bound, generic kernel
+  if (a.token_stride != a.N || a.H != 1) return false;       // contiguous rows only
+  if (mode != MODE_FWD && mode != MODE_ROPE) return false;
+  if (mode == MODE_ROPE && a.R > 0 && table_dtype != DT_FP32 && table_dtype != dtype) return false;
+  if (mode == MODE_FWD && a.N >= 1024) {
+    StreamArgs p{};
+    p.a = a;
+    p.a.R = 0;
+    const int xrow = a.N * 2;
+    if (dtype == DT_BF16)
+      return launch_stream(rows_tma_wide_fwd_kernel<__nv_bfloat16>, p, kConsumerWarps, xrow, 0, s);
+    return launch_stream(rows_tma_wide_fwd_kernel<__half>, p, kConsumerWarps, xrow, 0, s);
+  }
+  if (mode == MODE_FWD) {
+    if (dtype == DT_BF16) return dispatch_narrow<__nv_bfloat16, __nv_bfloat16, MODE_FWD>(a, s);
+    return dispatch_narrow<__half, __half, MODE_FWD>(a, s);
+  }
+  if (a.R == 0) {
+    if (dtype == DT_BF16) return dispatch_narrow<__nv_bfloat16, __nv_bfloat16, MODE_ROPE>(a, s);
+    return dispatch_narrow<__half, __half, MODE_ROPE>(a, s);
+  }
+  if (dtype == DT_BF16) {
+    if (table_dtype == DT_FP32) return dispatch_narrow<__nv_bfloat16, float, MODE_ROPE>(a, s);
+    return dispatch_narrow<__nv_bfloat16, __nv_bfloat16, MODE_ROPE>(a, s);
+  }
+  if (table_dtype == DT_FP32) return dispatch_narrow<__half, float, MODE_ROPE>(a, s);
+  return dispatch_narrow<__half, __half, MODE_ROPE>(a, s);
+}
+
+}  // namespace fq

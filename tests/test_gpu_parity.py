@@ -290,3 +290,28 @@ def test_bounded_wait_gives_up_and_context_stays_usable(orc, cuda_ok):
     assert_scale_close(s, s_ref)
     assert_codes_close(q, q_ref)
     assert fq.device_status(clear=True) == 0
+
+
+# ----------------------------------------------------------------------------------- TMA row-stream kernels
+@pytest.mark.parametrize("case", [(4099, 256, "bf16"), (4500, 1024, "bf16"), (4097, 4096, "fp16"), (5000, 64, "fp16"),
+                                  (4608, 2048, "bf16")], ids=lambda c: "M%d-N%d-%s" % c)
+def test_rmsnorm_fwd_stream_kernel(orc, cuda_ok, case):
+    M, N, dt = case
+    d = wl.rmsnorm_inputs(M, N, dt, seed=900 + M)
+    g = cuda(d)
+    y = fq.rmsnorm_fwd(g["x"], g["w"])
+    assert_storage_close(y, orc.rmsnorm_fwd(d["x"], d["w"]))
+    assert fq.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("case", [(5000, 192, 64, "fp16", "fp16", 32), (4097, 128, 128, "bf16", "fp32", 1),
+                                  (4200, 512, 64, "bf16", "bf16", 8), (4100, 256, 32, "fp16", "fp32", 4),
+                                  (4099, 1024, 128, "bf16", "bf16", 1), (4096, 96, 0, "bf16", "bf16", 1)],
+                         ids=lambda c: "M%d-N%d-R%d-%s-%s-h%d" % c)
+def test_rmsnorm_rope_stream_kernel(orc, cuda_ok, case):
+    M, N, R, dt, tdt, hpt = case
+    d = wl.rows_inputs(M, N, R, dt, tdt, seed=950 + M, heads_per_token=hpt)
+    g = cuda(d)
+    y = fq.rmsnorm_rope(g["x"], g["w"], g["cos"], g["sin"])
+    assert_storage_close(y, orc.rmsnorm_rope(d["x"], d["w"], d["cos"], d["sin"]))
+    assert fq.device_status(clear=True) == 0
