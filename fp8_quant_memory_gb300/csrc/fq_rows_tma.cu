@@ -7,11 +7,13 @@
 // and, with rotation, their SR cos and SR sin table rows (the tables of these calls have one row per
 // x row); an mbarrier counts the bytes and every wait is bounded (fq_sync.cuh). Bytes in flight do
 // not depend on registers, which is what the register-hungry, latency-bound global-load kernels
-// lacked. Eight consumer warps read x from the stage:
-//   - narrow rows: the lane-group layout and arithmetic of the generic row kernel (fq_rows.cuh),
-//     one row per lane group per stage, tables read from the stage;
-//   - wide rows (RMSNorm forward, N >= 1024): one warp per row, two passes over the staged row (sum
-//     of squares, then normalise and store), so registers stay low.
+// lacked. The consumer warps read x from the stage:
+//   - narrow rows: eight consumer warps with the lane-group layout and arithmetic of the generic row
+//     kernel (fq_rows.cuh), one row per lane group per stage, tables read from the stage;
+//   - wide rows (RMSNorm forward, N >= 1024): four consumer warps, one row per warp per stage, two
+//     passes over the staged row (sum of squares, then normalise and store), each unrolled four
+//     16-byte vectors deep; the weight row is copied into shared memory once per CTA. Two CTAs
+//     share an SM, so a stage is four rows and the ring fills and drains in small steps.
 // y is written with 16-byte evict-first stores. x and the tables are read from HBM exactly once.
 #include "fq_device.cuh"
 #include "fq_internal.h"
@@ -23,8 +25,11 @@ namespace {
 
 using namespace rows;
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 8;  // narrow-row kernel
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kWideWarps = 4;  // wide-row kernel
+constexpr int kWideThreads = (kWideWarps + 1) * 32;
+constexpr int kWideUnroll = 4;
 
 struct StreamArgs {
   RowArgs a;
@@ -34,13 +39,19 @@ struct StreamArgs {
   int32_t tab_off;      // byte offset of the cos block in a stage (0 when there is no rotation)
   int32_t tab_block;    // bytes of one table block
   int32_t depth;        // the producer keeps at most this many stages in flight
+  int32_t w_bytes;      // bytes of the weight row staged once per CTA (0: none)
 };
 
 // Producer: one lane streams the CTA's stages. Returns after issuing everything (or giving up).
 __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem, uint64_t* full, uint64_t* empty,
-                                        int32_t r0, int32_t r1, int SR, int esize, int tsize) {
+                                        uint64_t* wbar, unsigned char* wsm, int32_t r0, int32_t r1, int SR,
+                                        int esize, int tsize) {
   const RowArgs& a = p.a;
   const int S = p.stages;
+  if (p.w_bytes > 0) {
+    mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(p.w_bytes));
+    bulk_g2s(wsm, a.wq, static_cast<uint32_t>(p.w_bytes), wbar);
+  }
   const int nst = (r1 - r0 + SR - 1) / SR;
   const uint32_t xrow = static_cast<uint32_t>(a.N) * esize;
   const uint32_t trow = static_cast<uint32_t>(a.R / 2) * tsize;
@@ -89,26 +100,38 @@ __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem
 
 // Shared set-up of both kernels: ring layout, barriers, programmatic-launch handshake. Returns the
 // CTA's row range.
+// Shared memory: [pad to 128][stages x stage_bytes][full x stages][empty x stages][wbar][pad to 128]
+// [weight row, w_bytes].
 struct Ring {
   unsigned char* smem;
   uint64_t* full;
   uint64_t* empty;
+  uint64_t* wbar;
+  unsigned char* w;
   int32_t r0, r1;
 };
 
-__device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* smem_raw) {
+__host__ __device__ constexpr size_t ring_bytes(int stages, int stage_bytes, int w_bytes) {
+  return 128 + static_cast<size_t>(stages) * stage_bytes + (2 * stages + 1) * sizeof(uint64_t) + 128 + w_bytes;
+}
+
+__device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* smem_raw, int consumers) {
   Ring g;
   const uint32_t raw = smem_addr(smem_raw);
   g.smem = smem_raw + ((128u - (raw & 127u)) & 127u);
   g.full = reinterpret_cast<uint64_t*>(g.smem + static_cast<size_t>(p.stages) * p.stage_bytes);
   g.empty = g.full + p.stages;
+  g.wbar = g.empty + p.stages;
+  const uintptr_t wend = reinterpret_cast<uintptr_t>(g.wbar + 1);
+  g.w = reinterpret_cast<unsigned char*>((wend + 127) & ~static_cast<uintptr_t>(127));
   g.r0 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x) * p.a.rows) / gridDim.x);
   g.r1 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x + 1) * p.a.rows) / gridDim.x);
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&g.full[s], 1);
-      mbar_init(&g.empty[s], kConsumerWarps);
+      mbar_init(&g.empty[s], consumers);
     }
+    mbar_init(g.wbar, 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -123,11 +146,11 @@ __global__ void __launch_bounds__(kThreads) rows_tma_kernel(const StreamArgs p) 
   extern __shared__ unsigned char smem_raw[];
   constexpr int kV = HS + 2 * TS;
   constexpr int SR = kConsumerWarps * (32 / LPR);  // one row per lane group per stage
-  const Ring g = ring_setup(p, smem_raw);
+  const Ring g = ring_setup(p, smem_raw, kConsumerWarps);
   const RowArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane32 = threadIdx.x & 31;
   if (warp == kConsumerWarps) {
-    if (lane32 == 0) produce(p, g.smem, g.full, g.empty, g.r0, g.r1, SR, sizeof(T), sizeof(TT));
+    if (lane32 == 0) produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.r0, g.r1, SR, sizeof(T), sizeof(TT));
     return;
   }
   const int lane = lane32 & (LPR - 1);
@@ -167,19 +190,45 @@ __global__ void __launch_bounds__(kThreads) rows_tma_kernel(const StreamArgs p) 
 
 // ---------------------------------------------------------------------------------- wide rows
 template <typename T>
-__global__ void __launch_bounds__(kThreads) rows_tma_wide_fwd_kernel(const StreamArgs p) {
+__device__ __forceinline__ float2 sq_acc(uint4 u, float2 acc) {
+  const float2 f0 = Elem<T>::unpack(u.x), f1 = Elem<T>::unpack(u.y);
+  const float2 f2 = Elem<T>::unpack(u.z), f3 = Elem<T>::unpack(u.w);
+  acc = fma2(f0, f0, acc);
+  acc = fma2(f1, f1, acc);
+  acc = fma2(f2, f2, acc);
+  return fma2(f3, f3, acc);
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 norm8(uint4 u, uint4 wv, float2 rstd2) {
+  uint4 out;
+  out.x = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.x), rstd2), Elem<T>::unpack(wv.x)));
+  out.y = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.y), rstd2), Elem<T>::unpack(wv.y)));
+  out.z = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.z), rstd2), Elem<T>::unpack(wv.z)));
+  out.w = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.w), rstd2), Elem<T>::unpack(wv.w)));
+  return out;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kWideThreads) rows_tma_wide_fwd_kernel(const StreamArgs p) {
   extern __shared__ unsigned char smem_raw[];
-  constexpr int SR = kConsumerWarps;  // one row per warp per stage
-  const Ring g = ring_setup(p, smem_raw);
+  constexpr int SR = kWideWarps;  // one row per warp per stage
+  constexpr int U = kWideUnroll;
+  static_assert(U == 4, "the partial sums below are combined for four accumulators");
+  const Ring g = ring_setup(p, smem_raw, kWideWarps);
   const RowArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == kConsumerWarps) {
-    if (lane == 0) produce(p, g.smem, g.full, g.empty, g.r0, g.r1, SR, sizeof(T), 2);
+  if (warp == kWideWarps) {
+    if (lane == 0) produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.r0, g.r1, SR, sizeof(T), 2);
     return;
   }
   const int N = a.N, nv = N >> 3;
   const float fN = static_cast<float>(N);
-  const T* w = static_cast<const T*>(a.wq);
+  const uint4* ws = reinterpret_cast<const uint4*>(g.w);
+  if (!mbar_wait(kWaitLimitNs, g.wbar, 0u)) {
+    flag_failure(p.status);
+    return;
+  }
   const int nst = (g.r1 - g.r0 + SR - 1) / SR;
   int slot = 0;
   uint32_t phase = 0;
@@ -190,31 +239,36 @@ __global__ void __launch_bounds__(kThreads) rows_tma_wide_fwd_kernel(const Strea
     }
     const int32_t r = g.r0 + k * SR + warp;
     if (r < g.r1) {  // warp-uniform
-      const T* xs = reinterpret_cast<const T*>(g.smem + static_cast<size_t>(slot) * p.stage_bytes) +
-                    static_cast<int64_t>(warp) * N;
-      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-      for (int v = lane; v < nv; v += 32) {
-        const uint4 u = *reinterpret_cast<const uint4*>(xs + 8 * v);
-        const float2 f0 = Elem<T>::unpack(u.x), f1 = Elem<T>::unpack(u.y);
-        const float2 f2 = Elem<T>::unpack(u.z), f3 = Elem<T>::unpack(u.w);
-        acc0 = fma2(f0, f0, acc0);
-        acc1 = fma2(f1, f1, acc1);
-        acc0 = fma2(f2, f2, acc0);
-        acc1 = fma2(f3, f3, acc1);
+      const uint4* xs = reinterpret_cast<const uint4*>(g.smem + static_cast<size_t>(slot) * p.stage_bytes +
+                                                       static_cast<size_t>(warp) * N * sizeof(T));
+      float2 acc[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) acc[j] = make_float2(0.f, 0.f);
+      int v = lane;
+      for (; v + 32 * (U - 1) < nv; v += 32 * U) {
+        uint4 u[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) u[j] = xs[v + 32 * j];
+#pragma unroll
+        for (int j = 0; j < U; ++j) acc[j] = sq_acc<T>(u[j], acc[j]);
       }
-      const float2 acc = add2(acc0, acc1);
-      const float2 rstd2 = splat2(rstd_from_ss(group_sum<32>(acc.x + acc.y), fN, a.eps));
-      T* yrow = static_cast<T*>(a.y) + static_cast<int64_t>(r) * N;
-      for (int v = lane; v < nv; v += 32) {
-        const uint4 u = *reinterpret_cast<const uint4*>(xs + 8 * v);
-        const uint4 wv = ld_cached16(w + 8 * v);
-        uint4 out;
-        out.x = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.x), rstd2), Elem<T>::unpack(wv.x)));
-        out.y = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.y), rstd2), Elem<T>::unpack(wv.y)));
-        out.z = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.z), rstd2), Elem<T>::unpack(wv.z)));
-        out.w = Elem<T>::pack(mul2(mul2(Elem<T>::unpack(u.w), rstd2), Elem<T>::unpack(wv.w)));
-        st_stream16(yrow + 8 * v, out);
+      for (; v < nv; v += 32) acc[0] = sq_acc<T>(xs[v], acc[0]);
+      const float2 s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
+      const float2 sum = add2(s01, s23);
+      const float2 rstd2 = splat2(rstd_from_ss(group_sum<32>(sum.x + sum.y), fN, a.eps));
+      uint4* yrow = reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N);
+      v = lane;
+      for (; v + 32 * (U - 1) < nv; v += 32 * U) {
+        uint4 u[U], wv[U];
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          u[j] = xs[v + 32 * j];
+          wv[j] = ws[v + 32 * j];
+        }
+#pragma unroll
+        for (int j = 0; j < U; ++j) st_stream16(yrow + v + 32 * j, norm8<T>(u[j], wv[j], rstd2));
       }
+      for (; v < nv; v += 32) st_stream16(yrow + v, norm8<T>(xs[v], ws[v], rstd2));
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&g.empty[slot]);
@@ -227,7 +281,8 @@ __global__ void __launch_bounds__(kThreads) rows_tma_wide_fwd_kernel(const Strea
 
 // ---------------------------------------------------------------------------------- host side
 template <typename K>
-bool launch_stream(K kern, StreamArgs p, int stage_rows, int x_row_bytes, int tab_row_bytes, cudaStream_t s) {
+bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_bytes, int tab_row_bytes,
+                   cudaStream_t s) {
   const RowArgs& a = p.a;
   p.status = device_status_ptr();
   p.tab_block = ((stage_rows * tab_row_bytes) + 127) & ~127;
@@ -235,25 +290,25 @@ bool launch_stream(K kern, StreamArgs p, int stage_rows, int x_row_bytes, int ta
   p.stage_bytes = p.tab_off + 2 * p.tab_block;
   // Two CTAs per SM when stages are small; as many stages as fit, at most 8.
   const int budget = p.stage_bytes <= 32 * 1024 ? 110 * 1024 : 220 * 1024;
-  p.stages = (budget - 256) / p.stage_bytes;
+  p.stages = (budget - static_cast<int>(ring_bytes(0, 0, p.w_bytes)) - 8) / (p.stage_bytes + 16);
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) return false;
   // Keep about 48 KB in flight per CTA (at least two stages), never more than the ring.
   p.depth = (48 * 1024 + p.stage_bytes - 1) / p.stage_bytes;
   if (p.depth < 2) p.depth = 2;
   if (p.depth > p.stages) p.depth = p.stages;
-  const size_t smem = 128 + static_cast<size_t>(p.stages) * p.stage_bytes + 2 * p.stages * sizeof(uint64_t);
+  const size_t smem = ring_bytes(p.stages, p.stage_bytes, p.w_bytes);
   if (smem > 227 * 1024) return false;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return false;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
     return false;
   const int64_t want = (a.rows + stage_rows - 1) / stage_rows;
   const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -269,8 +324,8 @@ bool launch_narrow(const RowArgs& a, cudaStream_t s) {
   StreamArgs p{};
   p.a = a;
   constexpr int SR = kConsumerWarps * (32 / LPR);
-  return launch_stream(rows_tma_kernel<T, TT, MODE, LPR, HS, TS>, p, SR, a.N * static_cast<int>(sizeof(T)),
-                       (a.R / 2) * static_cast<int>(sizeof(TT)), s);
+  return launch_stream(rows_tma_kernel<T, TT, MODE, LPR, HS, TS>, kThreads, p, SR,
+                       a.N * static_cast<int>(sizeof(T)), (a.R / 2) * static_cast<int>(sizeof(TT)), s);
 }
 
 template <typename T, typename TT, int MODE>
@@ -300,9 +355,10 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
     p.a = a;
     p.a.R = 0;
     const int xrow = a.N * 2;
+    p.w_bytes = xrow;  // N % 8 == 0 and a 16-byte aligned w: a legal bulk copy
     if (dtype == DT_BF16)
-      return launch_stream(rows_tma_wide_fwd_kernel<__nv_bfloat16>, p, kConsumerWarps, xrow, 0, s);
-    return launch_stream(rows_tma_wide_fwd_kernel<__half>, p, kConsumerWarps, xrow, 0, s);
+      return launch_stream(rows_tma_wide_fwd_kernel<__nv_bfloat16>, kWideThreads, p, kWideWarps, xrow, 0, s);
+    return launch_stream(rows_tma_wide_fwd_kernel<__half>, kWideThreads, p, kWideWarps, xrow, 0, s);
   }
   if (mode == MODE_FWD) {
     if (dtype == DT_BF16) return dispatch_narrow<__nv_bfloat16, __nv_bfloat16, MODE_FWD>(a, s);
