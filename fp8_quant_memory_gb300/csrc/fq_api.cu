@@ -72,6 +72,11 @@ int check_rope(const char* fn, int64_t N, int64_t R, const void* cos, const void
 constexpr int64_t kMaxRows = 0x7fffffffLL;
 constexpr int64_t kMaxWidth = 1LL << 24;
 
+bool env_is(const char* name, const char* value) {
+  const char* v = std::getenv(name);
+  return v != nullptr && std::string(v) == value;
+}
+
 // Launch a row problem on the vectorised kernel when layout permits, else on the scalar kernel.
 int launch_rows(const char* fn, const fq::RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s) {
   cudaGetLastError();  // drop a stale non-sticky error from an unrelated earlier call
@@ -82,13 +87,14 @@ int launch_rows(const char* fn, const fq::RowArgs& a, int mode, int dtype, int t
   if (a.y != nullptr) vec = vec && aligned(a.y, 16);
   if (a.q != nullptr) vec = vec && aligned(a.q, 8);
   if (a.scale != nullptr) vec = vec && aligned(a.scale, 4);
-  // FQ_PROLOGUE_KERNEL=generic selects the generic vectorised kernel for the prologue instead of the
-  // TMA-fed one (a diagnostic switch: both compute the same result).
-  const char* pick = std::getenv("FQ_PROLOGUE_KERNEL");
-  const bool tma_ok = !(pick != nullptr && std::string(pick) == "generic");
-  if (vec && mode == fq::MODE_QK && tma_ok && fq::launch_prologue_tma(a, dtype, table_dtype, s))
+  // FQ_PROLOGUE_KERNEL=generic (prologue) and FQ_ROWS_KERNEL=generic (RMSNorm forward, RMSNorm +
+  // RoPE) select the generic vectorised kernel instead of the TMA-fed one (diagnostic switches: both
+  // compute the same result).
+  if (vec && mode == fq::MODE_QK && !env_is("FQ_PROLOGUE_KERNEL", "generic") &&
+      fq::launch_prologue_tma(a, dtype, table_dtype, s))
     return check_launch(fn);
-  if (vec && (mode == fq::MODE_FWD || mode == fq::MODE_ROPE) && fq::launch_rows_tma(a, mode, dtype, table_dtype, s))
+  if (vec && (mode == fq::MODE_FWD || mode == fq::MODE_ROPE) && !env_is("FQ_ROWS_KERNEL", "generic") &&
+      fq::launch_rows_tma(a, mode, dtype, table_dtype, s))
     return check_launch(fn);
   if (!(vec && fq::launch_rows_vector(a, mode, dtype, table_dtype, s)))
     fq::launch_rows_scalar(a, mode, dtype, table_dtype, s);

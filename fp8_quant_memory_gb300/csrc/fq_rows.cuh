@@ -81,11 +81,15 @@ __device__ __forceinline__ bool slot_ok(int s, int lane, int hv, int th) {
 // Everything after the loads for one row held by a lane group: rstd, normalise, rotate, write y
 // (fwd / rope modes write each vector as soon as it is computed), amax, scale, codes.
 // Table entries of this row: cos_base/sin_base + trow + pair index (global memory, or a staged block
-// in shared memory when SMEM_TAB).
-template <typename T, typename TT, int MODE, int LPR, int HS, int TS, bool SMEM_TAB>
+// in shared memory when SMEM_TAB). WPRE: the caller holds this lane's weight vectors in `wpre` (one
+// per slot, loaded once for every row it processes; single-weight modes only), else they are read
+// from global memory per row.
+template <typename T, typename TT, int MODE, int LPR, int HS, int TS, bool SMEM_TAB, bool WPRE = false>
 __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, int32_t h,
                                          const uint4 (&xv)[HS + 2 * TS], int lane, int hv, int th, float fN,
-                                         const void* cos_base, const void* sin_base, int64_t trow) {
+                                         const void* cos_base, const void* sin_base, int64_t trow,
+                                         const uint4* wpre = nullptr) {
+  static_assert(!(WPRE && MODE == MODE_QK), "the prologue selects wq or wk per row");
   constexpr bool kQuant = (MODE == MODE_ROPE_QUANT) || (MODE == MODE_QK);
   constexpr bool kRound = (MODE == MODE_ROPE) || (MODE == MODE_ROPE_QUANT);
   constexpr int kV = HS + 2 * TS;  // vector slots per lane: head..., tail-lo..., tail-hi...
@@ -123,7 +127,7 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
       for (int k = 0; k < 4; ++k) yf[s][k] = make_float2(0.f, 0.f);
       continue;
     }
-    const uint4 wv = ld_cached16(wrow + slot_col<LPR, HS, TS>(s, lane, hv, th));
+    const uint4 wv = WPRE ? wpre[s] : ld_cached16(wrow + slot_col<LPR, HS, TS>(s, lane, hv, th));
     uint4 packed;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -159,8 +163,8 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
         continue;
       }
       const int p8 = 8 * (lane + s * LPR);  // pair index of the vector's first element
-      const uint4 wlo = ld_cached16(wrow + slot_col<LPR, HS, TS>(slo, lane, hv, th));
-      const uint4 whi = ld_cached16(wrow + slot_col<LPR, HS, TS>(shi, lane, hv, th));
+      const uint4 wlo = WPRE ? wpre[slo] : ld_cached16(wrow + slot_col<LPR, HS, TS>(slo, lane, hv, th));
+      const uint4 whi = WPRE ? wpre[shi] : ld_cached16(wrow + slot_col<LPR, HS, TS>(shi, lane, hv, th));
       float2 c[4], sn[4];
       load_table8<TT, SMEM_TAB>(cos_base, trow + p8, c);
       load_table8<TT, SMEM_TAB>(sin_base, trow + p8, sn);

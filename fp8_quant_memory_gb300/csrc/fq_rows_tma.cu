@@ -141,8 +141,9 @@ __device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* s
 }
 
 // ---------------------------------------------------------------------------------- narrow rows
+// Up to four vectors per lane the kernel fits two CTAs per SM without spilling; wider rows take one.
 template <typename T, typename TT, int MODE, int LPR, int HS, int TS>
-__global__ void __launch_bounds__(kThreads) rows_tma_kernel(const StreamArgs p) {
+__global__ void __launch_bounds__(kThreads, (HS + 2 * TS) <= 4 ? 2 : 1) rows_tma_kernel(const StreamArgs p) {
   extern __shared__ unsigned char smem_raw[];
   constexpr int kV = HS + 2 * TS;
   constexpr int SR = kConsumerWarps * (32 / LPR);  // one row per lane group per stage
@@ -158,6 +159,13 @@ __global__ void __launch_bounds__(kThreads) rows_tma_kernel(const StreamArgs p) 
   const int N = a.N;
   const int hv = (N - a.R) >> 3, th = a.R >> 4, half = a.R >> 1;
   const float fN = static_cast<float>(N);
+  // This lane's weight vectors are the same for every row: load them once.
+  uint4 wv[kV];
+  const T* w = static_cast<const T*>(a.wq);
+#pragma unroll
+  for (int s = 0; s < kV; ++s)
+    wv[s] = slot_ok<LPR, HS, TS>(s, lane, hv, th) ? ld_cached16(w + slot_col<LPR, HS, TS>(s, lane, hv, th))
+                                                  : make_uint4(0u, 0u, 0u, 0u);
   const int nst = (g.r1 - g.r0 + SR - 1) / SR;
   int slot = 0;
   uint32_t phase = 0;
@@ -177,8 +185,8 @@ __global__ void __launch_bounds__(kThreads) rows_tma_kernel(const StreamArgs p) 
       xv[s] = slot_ok<LPR, HS, TS>(s, lane, hv, th)
                   ? *reinterpret_cast<const uint4*>(xs + slot_col<LPR, HS, TS>(s, lane, hv, th))
                   : make_uint4(0u, 0u, 0u, 0u);
-    row_body<T, TT, MODE, LPR, HS, TS, true>(a, rs + l, live, 0, xv, lane, hv, th, fN, st + p.tab_off,
-                                              st + p.tab_off + p.tab_block, static_cast<int64_t>(lr) * half);
+    row_body<T, TT, MODE, LPR, HS, TS, true, true>(a, rs + l, live, 0, xv, lane, hv, th, fN, st + p.tab_off,
+                                                    st + p.tab_off + p.tab_block, static_cast<int64_t>(lr) * half, wv);
     __syncwarp();
     if (lane32 == 0) mbar_arrive(&g.empty[slot]);  // x and this stage's table rows have been read
     if (++slot == p.stages) {

@@ -293,9 +293,19 @@ def test_bounded_wait_gives_up_and_context_stays_usable(orc, cuda_ok):
 
 
 # ----------------------------------------------------------------------------------- TMA row-stream kernels
+def _rows_kernel(monkeypatch, kernel):
+    if kernel == "generic":
+        monkeypatch.setenv("FQ_ROWS_KERNEL", "generic")
+    else:
+        monkeypatch.delenv("FQ_ROWS_KERNEL", raising=False)
+
+
+@pytest.mark.parametrize("kernel", ["tma", "generic"])
 @pytest.mark.parametrize("case", [(4099, 256, "bf16"), (4500, 1024, "bf16"), (4097, 4096, "fp16"), (5000, 64, "fp16"),
-                                  (4608, 2048, "bf16")], ids=lambda c: "M%d-N%d-%s" % c)
-def test_rmsnorm_fwd_stream_kernel(orc, cuda_ok, case):
+                                  (4608, 2048, "bf16"), (4103, 8192, "bf16"), (4096, 1032, "fp16")],
+                         ids=lambda c: "M%d-N%d-%s" % c)
+def test_rmsnorm_fwd_stream_kernel(orc, cuda_ok, monkeypatch, case, kernel):
+    _rows_kernel(monkeypatch, kernel)
     M, N, dt = case
     d = wl.rmsnorm_inputs(M, N, dt, seed=900 + M)
     g = cuda(d)
@@ -306,9 +316,12 @@ def test_rmsnorm_fwd_stream_kernel(orc, cuda_ok, case):
 
 @pytest.mark.parametrize("case", [(5000, 192, 64, "fp16", "fp16", 32), (4097, 128, 128, "bf16", "fp32", 1),
                                   (4200, 512, 64, "bf16", "bf16", 8), (4100, 256, 32, "fp16", "fp32", 4),
-                                  (4099, 1024, 128, "bf16", "bf16", 1), (4096, 96, 0, "bf16", "bf16", 1)],
+                                  (4099, 1024, 128, "bf16", "bf16", 1), (4096, 96, 0, "bf16", "bf16", 1),
+                                  (4101, 2048, 64, "bf16", "fp32", 2)],
                          ids=lambda c: "M%d-N%d-R%d-%s-%s-h%d" % c)
-def test_rmsnorm_rope_stream_kernel(orc, cuda_ok, case):
+@pytest.mark.parametrize("kernel", ["tma", "generic"])
+def test_rmsnorm_rope_stream_kernel(orc, cuda_ok, monkeypatch, case, kernel):
+    _rows_kernel(monkeypatch, kernel)
     M, N, R, dt, tdt, hpt = case
     d = wl.rows_inputs(M, N, R, dt, tdt, seed=950 + M, heads_per_token=hpt)
     g = cuda(d)
