@@ -1,14 +1,17 @@
 // fq_prologue.cu -- the QK-Norm + RoPE + FP8 attention prologue ("case_norm_rope_quant.py" (Ch.28),
 // module docstring) for head_dim 128 with the whole head rotated, as a TMA-fed persistent kernel.
 //
-// Data movement. Every CTA owns one contiguous range of (token, head) rows, balanced to the row.
-// One producer lane streams that range through a ring of shared-memory stages of 64 rows: two 2-D
-// tensor TMA loads (cp.async.bulk.tensor, 128-byte swizzle) bring the first and second halves of the
-// 64 rows (the NeoX "lo" and "hi" halves, 8 KB each in bf16) and two 1-D bulk copies bring the cos
-// and sin rows of the tokens those rows belong to; an mbarrier counts the bytes. Bytes in flight do
-// not depend on registers or occupancy. x is read from HBM once; each table row once per stage that
-// needs it (L2 serves repeats); the two norm weights once per CTA (shared memory, fp32, in a
-// lane-permuted layout). Codes and scales go straight to global memory with evict-first stores.
+// Data movement. The rows are cut into chunks of SR consecutive (token, head) rows, one per CTA of
+// the grid. The CTAs that are resident take over the chunks of CTAs that have not started yet
+// through cluster launch control (a hardware work queue: no counter in global memory), so every
+// SM keeps streaming until the last chunk is taken and the CTAs finish together. One producer
+// lane streams its chunks through a ring of shared-memory stages, one chunk per stage: two 2-D
+// tensor TMA loads (cp.async.bulk.tensor, 128-byte swizzle) bring the first and second halves of
+// the SR rows (the NeoX "lo" and "hi" halves) and two 1-D bulk copies bring the cos and sin rows
+// of the tokens those rows belong to; an mbarrier counts the bytes. Bytes in flight do not depend
+// on registers or occupancy. x is read from HBM once; each table row once per stage that needs it
+// (L2 serves repeats); the two norm weights once per CTA (shared memory, fp32, in a lane-permuted
+// layout). Codes and scales go straight to global memory with evict-first stores.
 //
 // Work layout. Eight consumer warps, four lanes per row (eight rows per warp, one row per lane group
 // per stage). Lane j of a row holds the NeoX pairs 16j..16j+15 of both halves, so every pair
@@ -207,6 +210,15 @@ __device__ __forceinline__ void prologue_row(const PrologueArgs& a, uint32_t st,
 }
 
 // ------------------------------------------------------------------------------ the kernel
+constexpr int kReq = 2;  // cluster-launch-control requests a producer keeps in flight
+
+// Shared memory: [pad to 1024][stages x stage_bytes][weights 2 x 128 fp32][kReq x 16-byte
+// responses][full x S][empty x S][request barriers x kReq][stage start rows x S].
+__host__ __device__ constexpr size_t prologue_smem_bytes(int stages, int stage_bytes) {
+  return 1024 + static_cast<size_t>(stages) * stage_bytes + 2 * kD * sizeof(float) + kReq * 16 +
+         (2 * stages + kReq) * sizeof(uint64_t) + stages * sizeof(int32_t);
+}
+
 template <typename T, typename TT, int SR>
 __global__ void __launch_bounds__(kThreads, 2)
     prologue_tma_kernel(const __grid_constant__ CUtensorMap xmap, const PrologueArgs a) {
@@ -216,14 +228,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const int S = a.stages;
   float* wsm = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * a.stage_bytes);  // 2 x 128 floats
-  uint64_t* full = reinterpret_cast<uint64_t*>(wsm + 2 * kD);
+  uint4* resp = reinterpret_cast<uint4*>(wsm + 2 * kD);
+  uint64_t* full = reinterpret_cast<uint64_t*>(resp + kReq);
   uint64_t* empty = full + S;
+  uint64_t* cbar = empty + S;
+  int32_t* stage_row = reinterpret_cast<int32_t*>(cbar + kReq);  // first row of each slot's chunk, -1 = end
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int32_t r0 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x) * a.rows) / gridDim.x);
-  const int32_t r1 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x + 1) * a.rows) / gridDim.x);
-  const int nst = (r1 - r0 + SR - 1) / SR;
   constexpr int kTabRow = (kD / 2) * static_cast<int>(sizeof(TT));  // bytes of one table row
 
   if (threadIdx.x == 0) {
@@ -231,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kConsumerWarps / 2);  // each stage is consumed by one half of the warps
     }
+    for (int c = 0; c < kReq; ++c) mbar_init(&cbar[c], 1);
     fence_barrier_init();
   }
   __syncthreads();
@@ -249,13 +262,18 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t phase = 0;  // parity of the slot's current use; its release completes phase ^ 1
     int dslot = 0;       // slot and parity of stage k - depth
     uint32_t dphase = 0;
-    for (; k < nst; ++k) {
+    // Request n (n = 0, 1, ...) uses response slot n % kReq and completes that slot's barrier phase
+    // n / kReq; responses are consumed in request order.
+    int issued = 0, answered = 0;
+    for (; issued < kReq; ++issued) clc_try_cancel(&resp[issued], &cbar[issued]);
+    uint32_t chunk = blockIdx.x;
+    for (;;) {
       if (k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) {
         ok = false;
         break;
       }
       // Keep at most `depth` stages in flight: every CTA's next stage then queues behind few
-      // others, which evens out when the CTAs' data arrives (the last CTA sets the kernel's end).
+      // others, which evens out when the CTAs' data arrives.
       if (k >= a.depth) {
         if (!mbar_wait(kWaitLimitNs, &full[dslot], dphase)) {
           ok = false;
@@ -266,12 +284,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           dphase ^= 1u;
         }
       }
-      const int32_t rs = r0 + k * SR;
-      const int32_t re = min(rs + SR, r1);
+      const int32_t rs = static_cast<int32_t>(chunk) * SR;
+      const int32_t re = min(rs + SR, a.rows);
       const int32_t tf = static_cast<int32_t>((static_cast<uint64_t>(rs) * a.magic) >> a.shift);
       const int32_t tl = static_cast<int32_t>((static_cast<uint64_t>(re - 1) * a.magic) >> a.shift);
       const uint32_t tbytes = static_cast<uint32_t>(tl - tf + 1) * kTabRow;
       unsigned char* st = smem + static_cast<size_t>(slot) * a.stage_bytes;
+      stage_row[slot] = rs;  // published to the consumers by the barrier's phase completion
       // Rows past the end of the tensor are zero-filled and still counted in full.
       mbar_arrive_expect_tx(&full[slot], 2u * half_tile<SR>() + 2u * tbytes);
       tma_load_2d(st, &xmap, 0, rs, &full[slot]);
@@ -280,6 +299,41 @@ __global__ void __launch_bounds__(kThreads, 2)
                tbytes, &full[slot]);
       bulk_g2s(st + 2 * half_tile<SR>() + a.tab_block,
                static_cast<const unsigned char*>(a.sin) + static_cast<int64_t>(tf) * kTabRow, tbytes, &full[slot]);
+      ++k;
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
+      // The next chunk: the oldest outstanding request's answer.
+      const int c = answered % kReq;
+      if (!mbar_wait(kWaitLimitNs, &cbar[c], static_cast<uint32_t>(answered / kReq) & 1u)) {
+        ok = false;
+        break;
+      }
+      ++answered;
+      uint32_t next;
+      if (!clc_query(&resp[c], &next)) break;  // no CTA left to take over: this CTA is done
+      chunk = next;
+      clc_try_cancel(&resp[c], &cbar[c]);
+      ++issued;
+    }
+    // Requests still in flight end as failures; they write this CTA's shared memory, so wait.
+    while (ok && answered < issued) {
+      if (!mbar_wait(kWaitLimitNs, &cbar[answered % kReq], static_cast<uint32_t>(answered / kReq) & 1u)) {
+        ok = false;
+        break;
+      }
+      ++answered;
+    }
+    // End marker for each consumer half (the halves take alternate stages).
+    for (int e = 0; ok && e < 2; ++e) {
+      if (k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) {
+        ok = false;
+        break;
+      }
+      stage_row[slot] = -1;
+      mbar_arrive(&full[slot]);
+      ++k;
       if (++slot == S) {
         slot = 0;
         phase ^= 1u;
@@ -290,6 +344,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       // Let the copies already issued land before this CTA's shared memory goes away.
       for (int j = max(0, k - S); j < k; ++j)
         if (!mbar_wait(kWaitLimitNs, &full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
+      for (; answered < issued; ++answered)
+        if (!mbar_wait(kWaitLimitNs, &cbar[answered % kReq], static_cast<uint32_t>(answered / kReq) & 1u)) break;
     }
     return;
   }
@@ -322,17 +378,19 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   int slot = half;  // stage k lives in slot k % S; S >= 2
   uint32_t phase = 0;
-  for (int k = half; k < nst; k += 2) {
+  for (;;) {
     if (!mbar_wait(kWaitLimitNs, &full[slot], phase)) {
       flag_failure(a.status);
       return;
     }
+    const int32_t rs = stage_row[slot];
+    if (rs < 0) break;  // end marker
     const uint32_t st = smem_addr(smem + static_cast<size_t>(slot) * a.stage_bytes);
-    const int32_t rs = r0 + k * SR;
+    const int32_t re = min(rs + SR, a.rows);
     const int32_t tf = static_cast<int32_t>((static_cast<uint64_t>(rs) * a.magic) >> a.shift);
 #pragma unroll
     for (int u = 0; u < (SR / kGroupsPerHalf); ++u)
-      prologue_row<T, TT, SR>(a, st, l0 + u * kGroupsPerHalf, j, rev, wbase, rs, r1, tf, clamp);
+      prologue_row<T, TT, SR>(a, st, l0 + u * kGroupsPerHalf, j, rev, wbase, rs, re, tf, clamp);
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the stage's shared memory
     slot += 2;
@@ -403,7 +461,7 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
   p.tab_block = ((tab_rows * (kD / 2) * tsz) + 127) & ~127;
   p.stage_bytes = ((2 * half_tile<SR>() + 2 * p.tab_block) + 1023) & ~1023;
   // Ring depth: as many stages (up to 12) as fit two CTAs per SM in GB300's 228 KB of shared memory.
-  const int fixed = 1024 + 2 * kD * static_cast<int>(sizeof(float)) + 2 * 12 * static_cast<int>(sizeof(uint64_t));
+  const int fixed = static_cast<int>(prologue_smem_bytes(12, 0));
   p.stages = (110 * 1024 - fixed) / p.stage_bytes;
   if (p.stages > 12) p.stages = 12;
   if (p.stages < 2) p.stages = 2;
@@ -412,8 +470,7 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
   // k - depth, whose slot must not have been refilled yet.
   p.depth = 128 / SR;
   if (p.depth > p.stages) p.depth = p.stages;
-  const size_t smem = 1024 + static_cast<size_t>(p.stages) * p.stage_bytes + 2 * kD * sizeof(float) +
-                      2 * p.stages * sizeof(uint64_t);
+  const size_t smem = prologue_smem_bytes(p.stages, p.stage_bytes);
   if (smem > 227 * 1024) return false;
 
   void (*kern)(const CUtensorMap, const PrologueArgs);
@@ -430,12 +487,9 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
       return false;
     configured[key] = static_cast<int>(smem);
   }
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess || per_sm < 1)
-    per_sm = 1;
-  const int64_t want = (a.rows + SR - 1) / SR;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
-  const int grid = static_cast<int>(want < cap ? want : cap);
+  // One CTA per chunk of SR rows. Only the CTAs that fit on the GPU at once start; they take over
+  // the rest of the grid chunk by chunk (cluster launch control), so the grid is not a wave count.
+  const int grid = static_cast<int>((a.rows + SR - 1) / SR);
   // Programmatic stream serialisation: this grid may be scheduled while the previous kernel in the
   // stream drains; griddepcontrol.wait inside the kernel orders every global access after it.
   cudaLaunchConfig_t cfg{};
@@ -455,7 +509,7 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
 
 bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
   if (a.N != kD || a.R != kD) return false;
-  if (a.rows <= 0 || a.rows > 0x7fffffffLL) return false;
+  if (a.rows <= 0 || a.rows > 0x7fffffffLL - 128) return false;  // row + stage size stays in int32
   if (a.token_stride != static_cast<int64_t>(a.H) * kD) return false;  // packed [T, H, 128] only
   if (a.H + 64 >= (1 << 21)) return false;
   if (!(table_dtype == DT_FP32 || table_dtype == dtype)) return false;

@@ -75,6 +75,39 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
+// ------------------------------------------------------------------------------------------------
+// Cluster launch control (sm_100-class): a running CTA asks the hardware scheduler to cancel the
+// launch of a CTA of the same grid that has not started yet, and takes over its work. The 16-byte
+// response lands in shared memory through the async proxy; completion is tracked with an mbarrier
+// (16 transaction bytes), like a bulk copy. Once a CTA has observed a failed request it must not
+// issue another; requests issued before that observation complete (as failures) and must still be
+// waited for before the CTA exits, because they write its shared memory.
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ void clc_try_cancel(void* response, uint64_t* bar) {
+  mbar_arrive_expect_tx(bar, 16u);
+  asm volatile(
+      "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+          smem_addr(response)),
+      "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Decodes a completed response: true and the cancelled CTA's blockIdx.x if the request succeeded.
+__device__ __forceinline__ bool clc_query(const void* response, uint32_t* ctaid_x) {
+  uint32_t ok, x = 0;
+  asm volatile(
+      "{\n\t.reg .b128 r;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 r, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, r;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "@p clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, r;\n\t}"
+      : "=r"(ok), "+r"(x)
+      : "r"(smem_addr(response))
+      : "memory");
+  *ctaid_x = x;
+  return ok != 0;
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

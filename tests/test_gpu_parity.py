@@ -260,6 +260,29 @@ def test_prologue_tma_kernel_parity(orc, cuda_ok, monkeypatch, case, kernel):
     assert fq.device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("case", [(4096, 32, 8), (1000, 3, 1), (333, 64, 8), (5, 1, 0)],
+                         ids=lambda c: "T%d-%d+%d" % c)
+def test_prologue_tma_writes_every_row(orc, cuda_ok, monkeypatch, case):
+    """Every chunk of rows is processed exactly once, whichever CTA takes it over: outputs pre-filled
+    with NaN codes and NaN scales hold no leftover after the call, twice in a row on the same buffers
+    with different inputs (so a skipped chunk cannot pass on the previous call's values)."""
+    T, Hq, Hk = case
+    monkeypatch.delenv("FQ_PROLOGUE_KERNEL", raising=False)
+    H = Hq + Hk
+    q = torch.full((T, H, 128), 0x7F, dtype=torch.uint8, device="cuda")
+    s = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
+    for seed in (901, 902):
+        d = wl.qk_inputs(T, Hq, Hk, 128, "bf16", "fp32", seed=seed + T, std=2.0)
+        q_ref, s_ref = orc.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], Hq, Hk)
+        g = cuda(d)
+        fq.qk_norm_rope_quant(g["qk"], g["wq"], g["wk"], g["cos"], g["sin"], Hq, Hk, q_out=q, scale=s)
+        torch.cuda.synchronize()
+        assert not bool(torch.isnan(s).any())
+        assert_scale_close(s, s_ref)
+        assert_codes_close(q, q_ref)
+    assert fq.device_status(clear=True) == 0
+
+
 def test_prologue_tma_matches_generic_kernel(cuda_ok, monkeypatch):
     """Both kernels on identical inputs: scales within 1e-6 relative, codes at most one step apart."""
     d = cuda(wl.qk_inputs(777, 32, 8, 128, "bf16", "fp32", seed=790, std=2.0))
