@@ -2,12 +2,15 @@
 // over contiguous rows ("rmsnorm_tl.py" (Ch.17), _rmsnorm_fwd; "rmsnorm_rope_quant.py" (Ch.13
 // fusion), rms_norm_rope_fused / torch_reference_fused).
 //
-// Every CTA owns a contiguous, row-balanced range of rows. One producer lane streams it through a
-// ring of shared-memory stages with cp.async.bulk: a stage is SR consecutive x rows (one bulk copy)
-// and, with rotation, their SR cos and SR sin table rows (the tables of these calls have one row per
-// x row); an mbarrier counts the bytes and every wait is bounded (fq_sync.cuh). Bytes in flight do
-// not depend on registers, which is what the register-hungry, latency-bound global-load kernels
-// lacked. The consumer warps read x from the stage:
+// The rows are cut into stages of SR consecutive rows, one per CTA of the grid. The CTAs that are
+// resident take over the stages of CTAs that have not started yet through cluster launch control (a
+// hardware work queue: no counter in global memory), so every SM keeps streaming until the last
+// stage is taken. One producer lane streams its stages through a ring in shared memory with
+// cp.async.bulk: a stage is SR consecutive x rows (one bulk copy) and, with rotation, their SR cos
+// and SR sin table rows (the tables of these calls have one row per x row); an mbarrier counts the
+// bytes and every wait is bounded (fq_sync.cuh). Bytes in flight do not depend on registers, which is
+// what the register-hungry, latency-bound global-load kernels lacked. The consumer warps read x from
+// the stage:
 //   - narrow rows: eight consumer warps with the lane-group layout and arithmetic of the generic row
 //     kernel (fq_rows.cuh), one row per lane group per stage, tables read from the stage;
 //   - wide rows (RMSNorm forward, N >= 1024): four consumer warps, one row per warp per stage, two
@@ -42,24 +45,30 @@ struct StreamArgs {
   int32_t w_bytes;      // bytes of the weight row staged once per CTA (0: none)
 };
 
-// Producer: one lane streams the CTA's stages. Returns after issuing everything (or giving up).
+constexpr int kReq = 2;  // cluster-launch-control requests a producer keeps in flight
+
+// Producer: one lane streams the stages this CTA takes (its own first, then those of CTAs it takes
+// over), posts an end marker, and returns. `issued` work requests were started before the dependency
+// wait (ring_setup).
 __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem, uint64_t* full, uint64_t* empty,
-                                        uint64_t* wbar, unsigned char* wsm, int32_t r0, int32_t r1, int SR,
-                                        int esize, int tsize) {
+                                        uint64_t* wbar, unsigned char* wsm, uint4* resp, uint64_t* cbar,
+                                        int32_t* stage_row, int SR, int esize, int tsize) {
   const RowArgs& a = p.a;
   const int S = p.stages;
   if (p.w_bytes > 0) {
     mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(p.w_bytes));
     bulk_g2s(wsm, a.wq, static_cast<uint32_t>(p.w_bytes), wbar);
   }
-  const int nst = (r1 - r0 + SR - 1) / SR;
   const uint32_t xrow = static_cast<uint32_t>(a.N) * esize;
   const uint32_t trow = static_cast<uint32_t>(a.R / 2) * tsize;
   int slot = 0, dslot = 0;
   uint32_t phase = 0, dphase = 0;
   int k = 0;
   bool ok = true;
-  for (; k < nst; ++k) {
+  // Request n uses response slot n % kReq and completes that slot's barrier phase n / kReq.
+  int issued = kReq, answered = 0;
+  uint32_t chunk = blockIdx.x;
+  for (;;) {
     if (k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) {
       ok = false;
       break;
@@ -74,10 +83,11 @@ __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem
         dphase ^= 1u;
       }
     }
-    const int32_t rs = r0 + k * SR;
-    const uint32_t nr = static_cast<uint32_t>(min(SR, r1 - rs));
+    const int32_t rs = static_cast<int32_t>(chunk) * SR;
+    const uint32_t nr = static_cast<uint32_t>(min(SR, static_cast<int32_t>(a.rows) - rs));
     unsigned char* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
     const uint32_t tb = (a.R > 0) ? nr * trow : 0u;
+    stage_row[slot] = rs;  // published to the consumers by the barrier's phase completion
     mbar_arrive_expect_tx(&full[slot], nr * xrow + 2u * tb);
     bulk_g2s(st, static_cast<const unsigned char*>(a.x) + static_cast<int64_t>(rs) * xrow, nr * xrow, &full[slot]);
     if (tb > 0) {
@@ -86,56 +96,93 @@ __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem
       bulk_g2s(st + p.tab_off + p.tab_block,
                static_cast<const unsigned char*>(a.sin) + static_cast<int64_t>(rs) * trow, tb, &full[slot]);
     }
+    ++k;
     if (++slot == S) {
       slot = 0;
       phase ^= 1u;
     }
+    // The next stage: the oldest outstanding request's answer.
+    const int c = answered % kReq;
+    if (!mbar_wait(kWaitLimitNs, &cbar[c], static_cast<uint32_t>(answered / kReq) & 1u)) {
+      ok = false;
+      break;
+    }
+    ++answered;
+    uint32_t next;
+    if (!clc_query(&resp[c], &next)) break;  // no CTA left to take over: this CTA is done
+    chunk = next;
+    clc_try_cancel(&resp[c], &cbar[c]);
+    ++issued;
   }
-  if (!ok) {
-    flag_failure(p.status);
-    for (int j = max(0, k - S); j < k; ++j)
-      if (!mbar_wait(kWaitLimitNs, &full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
+  // Requests still in flight end as failures; they write this CTA's shared memory, so wait.
+  while (ok && answered < issued) {
+    if (!mbar_wait(kWaitLimitNs, &cbar[answered % kReq], static_cast<uint32_t>(answered / kReq) & 1u)) {
+      ok = false;
+      break;
+    }
+    ++answered;
   }
+  // End marker (every consumer warp reads every stage).
+  if (ok && k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) ok = false;
+  if (ok) {
+    stage_row[slot] = -1;
+    mbar_arrive(&full[slot]);
+    return;
+  }
+  flag_failure(p.status);
+  for (int j = max(0, k - S); j < k; ++j)
+    if (!mbar_wait(kWaitLimitNs, &full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
+  for (; answered < issued; ++answered)
+    if (!mbar_wait(kWaitLimitNs, &cbar[answered % kReq], static_cast<uint32_t>(answered / kReq) & 1u)) break;
 }
 
-// Shared set-up of both kernels: ring layout, barriers, programmatic-launch handshake. Returns the
-// CTA's row range.
-// Shared memory: [pad to 128][stages x stage_bytes][full x stages][empty x stages][wbar][pad to 128]
-// [weight row, w_bytes].
+// Shared set-up of both kernels: ring layout, barriers, programmatic-launch handshake, the first
+// work requests.
+// Shared memory: [pad to 128][stages x stage_bytes][kReq x 16-byte responses][full x stages]
+// [empty x stages][request barriers x kReq][wbar][stage start rows x stages][pad to 128][weight row].
 struct Ring {
   unsigned char* smem;
   uint64_t* full;
   uint64_t* empty;
   uint64_t* wbar;
   unsigned char* w;
-  int32_t r0, r1;
+  uint4* resp;
+  uint64_t* cbar;
+  int32_t* stage_row;
 };
 
 __host__ __device__ constexpr size_t ring_bytes(int stages, int stage_bytes, int w_bytes) {
-  return 128 + static_cast<size_t>(stages) * stage_bytes + (2 * stages + 1) * sizeof(uint64_t) + 128 + w_bytes;
+  return 128 + static_cast<size_t>(stages) * stage_bytes + kReq * 16 + (2 * stages + kReq + 1) * sizeof(uint64_t) +
+         stages * sizeof(int32_t) + 128 + w_bytes;
 }
 
 __device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* smem_raw, int consumers) {
   Ring g;
   const uint32_t raw = smem_addr(smem_raw);
   g.smem = smem_raw + ((128u - (raw & 127u)) & 127u);
-  g.full = reinterpret_cast<uint64_t*>(g.smem + static_cast<size_t>(p.stages) * p.stage_bytes);
+  g.resp = reinterpret_cast<uint4*>(g.smem + static_cast<size_t>(p.stages) * p.stage_bytes);
+  g.full = reinterpret_cast<uint64_t*>(g.resp + kReq);
   g.empty = g.full + p.stages;
-  g.wbar = g.empty + p.stages;
-  const uintptr_t wend = reinterpret_cast<uintptr_t>(g.wbar + 1);
+  g.cbar = g.empty + p.stages;
+  g.wbar = g.cbar + kReq;
+  g.stage_row = reinterpret_cast<int32_t*>(g.wbar + 1);
+  const uintptr_t wend = reinterpret_cast<uintptr_t>(g.stage_row + p.stages);
   g.w = reinterpret_cast<unsigned char*>((wend + 127) & ~static_cast<uintptr_t>(127));
-  g.r0 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x) * p.a.rows) / gridDim.x);
-  g.r1 = static_cast<int32_t>((static_cast<int64_t>(blockIdx.x + 1) * p.a.rows) / gridDim.x);
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) {
       mbar_init(&g.full[s], 1);
       mbar_init(&g.empty[s], consumers);
     }
+    for (int c = 0; c < kReq; ++c) mbar_init(&g.cbar[c], 1);
     mbar_init(g.wbar, 1);
     fence_barrier_init();
   }
   __syncthreads();
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // The work requests touch no data of the previous kernel: the producer lane starts them before the
+  // dependency wait. Every global access comes after it.
+  if (threadIdx.x == consumers * 32)
+    for (int c = 0; c < kReq; ++c) clc_try_cancel(&g.resp[c], &g.cbar[c]);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   return g;
 }
@@ -151,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, (HS + 2 * TS) <= 4 ? 2 : 1) rows_tma
   const RowArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane32 = threadIdx.x & 31;
   if (warp == kConsumerWarps) {
-    if (lane32 == 0) produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.r0, g.r1, SR, sizeof(T), sizeof(TT));
+    if (lane32 == 0)
+      produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, SR, sizeof(T), sizeof(TT));
     return;
   }
   const int lane = lane32 & (LPR - 1);
@@ -166,17 +214,17 @@ __global__ void __launch_bounds__(kThreads, (HS + 2 * TS) <= 4 ? 2 : 1) rows_tma
   for (int s = 0; s < kV; ++s)
     wv[s] = slot_ok<LPR, HS, TS>(s, lane, hv, th) ? ld_cached16(w + slot_col<LPR, HS, TS>(s, lane, hv, th))
                                                   : make_uint4(0u, 0u, 0u, 0u);
-  const int nst = (g.r1 - g.r0 + SR - 1) / SR;
   int slot = 0;
   uint32_t phase = 0;
-  for (int k = 0; k < nst; ++k) {
+  for (;;) {
     if (!mbar_wait(kWaitLimitNs, &g.full[slot], phase)) {
       flag_failure(p.status);
       return;
     }
+    const int32_t rs = g.stage_row[slot];
+    if (rs < 0) break;  // end marker
     const unsigned char* st = g.smem + static_cast<size_t>(slot) * p.stage_bytes;
-    const int32_t rs = g.r0 + k * SR;
-    const bool live = l < g.r1 - rs;
+    const bool live = l < static_cast<int32_t>(a.rows) - rs;
     const int lr = live ? l : 0;  // dead lane groups read row 0 of the stage (always present)
     const T* xs = reinterpret_cast<const T*>(st) + static_cast<int64_t>(lr) * N;
     uint4 xv[kV];
@@ -227,7 +275,7 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_fwd_kernel(const S
   const RowArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == kWideWarps) {
-    if (lane == 0) produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.r0, g.r1, SR, sizeof(T), 2);
+    if (lane == 0) produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, SR, sizeof(T), 2);
     return;
   }
   const int N = a.N, nv = N >> 3;
@@ -237,16 +285,17 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_fwd_kernel(const S
     flag_failure(p.status);
     return;
   }
-  const int nst = (g.r1 - g.r0 + SR - 1) / SR;
   int slot = 0;
   uint32_t phase = 0;
-  for (int k = 0; k < nst; ++k) {
+  for (;;) {
     if (!mbar_wait(kWaitLimitNs, &g.full[slot], phase)) {
       flag_failure(p.status);
       return;
     }
-    const int32_t r = g.r0 + k * SR + warp;
-    if (r < g.r1) {  // warp-uniform
+    const int32_t rs = g.stage_row[slot];
+    if (rs < 0) break;  // end marker
+    const int32_t r = rs + warp;
+    if (r < static_cast<int32_t>(a.rows)) {  // warp-uniform
       const uint4* xs = reinterpret_cast<const uint4*>(g.smem + static_cast<size_t>(slot) * p.stage_bytes +
                                                        static_cast<size_t>(warp) * N * sizeof(T));
       float2 acc[U];
@@ -298,7 +347,7 @@ bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_
   p.stage_bytes = p.tab_off + 2 * p.tab_block;
   // Two CTAs per SM when stages are small; as many stages as fit, at most 8.
   const int budget = p.stage_bytes <= 32 * 1024 ? 110 * 1024 : 220 * 1024;
-  p.stages = (budget - static_cast<int>(ring_bytes(0, 0, p.w_bytes)) - 8) / (p.stage_bytes + 16);
+  p.stages = (budget - static_cast<int>(ring_bytes(0, 0, p.w_bytes)) - 8) / (p.stage_bytes + 20);
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) return false;
   // Keep about 48 KB in flight per CTA (at least two stages), never more than the ring.
@@ -309,13 +358,10 @@ bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_
   if (smem > 227 * 1024) return false;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return false;
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem) != cudaSuccess || per_sm < 1)
-    return false;
-  const int64_t want = (a.rows + stage_rows - 1) / stage_rows;
-  const int64_t cap = static_cast<int64_t>(sm_count()) * per_sm;
+  // One CTA per stage of rows. Only the CTAs that fit on the GPU at once start; they take over the
+  // rest of the grid stage by stage (cluster launch control), so the grid is not a wave count.
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(static_cast<unsigned>(want < cap ? want : cap));
+  cfg.gridDim = dim3(static_cast<unsigned>((a.rows + stage_rows - 1) / stage_rows));
   cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -354,7 +400,8 @@ bool dispatch_narrow(const RowArgs& a, cudaStream_t s) {
 }  // namespace
 
 bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s) {
-  if (a.rows < 4096 || a.rows > 0x7fffffffLL) return false;  // small problems: launch-bound, generic kernel
+  // Small problems are launch-bound: the generic kernel. Row indices and row + stage stay in int32.
+  if (a.rows < 4096 || a.rows > 0x7fffffffLL - 256) return false;
   if (a.token_stride != a.N || a.H != 1) return false;       // contiguous rows only
   if (mode != MODE_FWD && mode != MODE_ROPE) return false;
   if (mode == MODE_ROPE && a.R > 0 && table_dtype != DT_FP32 && table_dtype != dtype) return false;

@@ -46,14 +46,26 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
-// Wait for the phase with the given parity to complete; false once `limit_ns` of %globaltimer time
-// has passed without it (or after 2^32 polls). Callers report the failure and stop; nothing traps.
+// Wait for the phase with the given parity to complete; false once `limit_ns` of waiting has
+// accumulated without it (or after 2^32 polls). Callers report the failure and stop; nothing traps.
+// The waiting time is summed from %globaltimer readings taken every 64 polls, each step clamped to
+// [0, 1 ms]: the timer can be stepped (it follows the host's clock), and a step backwards or
+// forwards must neither end a healthy wait early nor stretch a failing one.
+constexpr uint64_t kMaxTimerStepNs = 1000000ull;
+
 __device__ __forceinline__ bool mbar_wait(uint64_t limit_ns, uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
+  uint64_t prev = global_ns(), waited = 0;
   for (uint32_t i = 1; i != 0; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
+    if ((i & 63u) == 0) {
+      const uint64_t now = global_ns();
+      const int64_t step = static_cast<int64_t>(now - prev);
+      prev = now;
+      waited += step < 0 ? 0ull : (static_cast<uint64_t>(step) > kMaxTimerStepNs ? kMaxTimerStepNs
+                                                                                : static_cast<uint64_t>(step));
+      if (waited > limit_ns) return false;
+    }
   }
   return false;
 }
