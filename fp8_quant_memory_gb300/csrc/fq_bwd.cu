@@ -8,12 +8,21 @@
 //   stage 2: every column adds its chunk partials in chunk order.
 // No atomics anywhere, so dw is bitwise reproducible run to run and independent of the grid.
 //
-// Stage 1 reads x and g once (16-byte streaming loads) and writes dx once. A row is owned by a
+// Stage 1 reads x and g once and writes dx once. Rows of 1032..4096 elements take a TMA-fed kernel:
+// a producer lane bulk-copies each x and g row of the chunk into a ring in shared memory, so the
+// next rows are already on chip while a row is reduced (the global-load kernel, which loads two rows
+// at the top of each iteration, exposes the memory latency once per iteration); eight consumer
+// warps own 16-byte column vectors, hold their weights and their dw partials in registers, and meet
+// once per row at a named barrier for the row's two sums. Narrower rows use 16-byte streaming loads. A row is owned by a
 // team of TPR threads (a lane group for narrow rows, several warps for wide rows); one reduction
 // per row yields both sum(x^2) and sum(gw*x), and c = rstd * sum(gw*x) / N (the same quantity as
 // mean(gw*xn) up to fp32 rounding order).
 #include "fq_device.cuh"
 #include "fq_internal.h"
+#include "fq_sync.cuh"
+
+#include <cstdlib>
+#include <cstring>
 
 namespace fq {
 namespace {
@@ -284,6 +293,226 @@ __global__ void __launch_bounds__(kThreads) bwd_stage1_scalar_kernel(const BwdAr
   }
 }
 
+
+// ------------------------------------------------------------------------------ TMA-fed stage 1
+constexpr int kStreamWarps = 8;                          // consumer warps
+constexpr int kStreamThreads = (kStreamWarps + 1) * 32;  // + one producer warp
+
+struct BwdStream {
+  BwdArgs a;
+  int64_t rows_per_chunk;
+  unsigned int* status;
+  int32_t stages;       // ring depth
+  int32_t stage_bytes;  // x row + g row, multiple of 128
+  int32_t depth;        // the producer keeps at most this many rows in flight
+};
+
+__host__ __device__ constexpr size_t stream_smem_bytes(int stages, int stage_bytes) {
+  return 128 + static_cast<size_t>(stages) * stage_bytes + 2 * stages * sizeof(uint64_t) +
+         2 * kStreamWarps * 2 * sizeof(float);
+}
+
+// Named barrier of the consumer warps that also ANDs a predicate over them: every consumer learns
+// whether all of them got their data, so a failed wait never leaves the others at the barrier.
+__device__ __forceinline__ bool consumers_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, 1, %2, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "n"(kStreamWarps * 32)
+      : "memory");
+  return r != 0;
+}
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kStreamThreads, 2) bwd_stage1_stream_kernel(const BwdStream p) {
+  extern __shared__ unsigned char smem_raw[];
+  const BwdArgs& a = p.a;
+  const uint32_t raw = smem_addr(smem_raw);
+  unsigned char* smem = smem_raw + ((128u - (raw & 127u)) & 127u);
+  const int S = p.stages;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * p.stage_bytes);
+  uint64_t* empty = full + S;
+  float* red = reinterpret_cast<float*>(empty + S);  // [2][kStreamWarps][2], double buffered
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int N = a.N, nv = N >> 3;
+  const uint32_t row_bytes = static_cast<uint32_t>(N) * sizeof(T);
+  const int64_t c0 = static_cast<int64_t>(blockIdx.x) * p.rows_per_chunk;
+  const int64_t c1 = min(c0 + p.rows_per_chunk, a.M);
+  const int n = static_cast<int>(c1 - c0);
+
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kStreamWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  if (warp == kStreamWarps) {
+    // ---------------------------------------------------------------- producer (one lane)
+    if (lane != 0) return;
+    int slot = 0, dslot = 0, k = 0;
+    uint32_t phase = 0, dphase = 0;
+    bool ok = true;
+    for (; k < n; ++k) {
+      if (k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) {
+        ok = false;
+        break;
+      }
+      if (k >= p.depth) {
+        if (!mbar_wait(kWaitLimitNs, &full[dslot], dphase)) {
+          ok = false;
+          break;
+        }
+        if (++dslot == S) {
+          dslot = 0;
+          dphase ^= 1u;
+        }
+      }
+      unsigned char* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
+      const int64_t off = (c0 + k) * static_cast<int64_t>(row_bytes);
+      mbar_arrive_expect_tx(&full[slot], 2u * row_bytes);
+      bulk_g2s(st, static_cast<const unsigned char*>(a.x) + off, row_bytes, &full[slot]);
+      bulk_g2s(st + row_bytes, static_cast<const unsigned char*>(a.g) + off, row_bytes, &full[slot]);
+      if (++slot == S) {
+        slot = 0;
+        phase ^= 1u;
+      }
+    }
+    if (!ok) {
+      flag_failure(p.status);
+      for (int j = max(0, k - S); j < k; ++j)
+        if (!mbar_wait(kWaitLimitNs, &full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
+    }
+    return;
+  }
+
+  // ------------------------------------------------------------------ consumers
+  // Thread t owns the 16-byte column vectors t, t + 256, ...: its weights and its dw partial sums
+  // stay in registers for the whole chunk.
+  const T* wp = static_cast<const T*>(a.w);
+  float2 wf[VPT][4], acc[VPT][4];
+  bool okv[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int v = tid + k * kStreamWarps * 32;
+    okv[k] = v < nv;
+    const uint4 u = okv[k] ? ld_cached16(wp + 8 * v) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      wf[k][e] = Elem<T>::unpack(word(u, e));
+      acc[k][e] = make_float2(0.f, 0.f);
+    }
+  }
+  const float fN = static_cast<float>(N);
+  int slot = 0;
+  uint32_t phase = 0;
+  for (int k = 0; k < n; ++k) {
+    const bool got = mbar_wait(kWaitLimitNs, &full[slot], phase);
+    if (!got) flag_failure(p.status);
+    const unsigned char* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
+    uint4 xv[VPT], gv[VPT];
+#pragma unroll
+    for (int q = 0; q < VPT; ++q) {
+      const int v = tid + q * kStreamWarps * 32;
+      const bool live = got && okv[q];
+      xv[q] = live ? reinterpret_cast<const uint4*>(st)[v] : make_uint4(0u, 0u, 0u, 0u);
+      gv[q] = live ? reinterpret_cast<const uint4*>(st + row_bytes)[v] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    __syncwarp();
+    if (got && lane == 0) mbar_arrive(&empty[slot]);  // the row is in registers: release the stage
+    float2 s2 = make_float2(0.f, 0.f), g2 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < VPT; ++q)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 xf = Elem<T>::unpack(word(xv[q], e));
+        const float2 gw = mul2(Elem<T>::unpack(word(gv[q], e)), wf[q][e]);
+        s2 = fma2(xf, xf, s2);
+        g2 = fma2(gw, xf, g2);
+      }
+    const float ss_w = group_sum<32>(s2.x + s2.y);
+    const float sg_w = group_sum<32>(g2.x + g2.y);
+    float* rb = red + (k & 1) * (2 * kStreamWarps);
+    if (lane == 0) {
+      rb[2 * warp] = ss_w;
+      rb[2 * warp + 1] = sg_w;
+    }
+    if (!consumers_all(got)) return;  // a stage never arrived: every consumer stops here
+    float ss = 0.f, sg = 0.f;
+#pragma unroll
+    for (int w = 0; w < kStreamWarps; ++w) {  // fixed order
+      ss += rb[2 * w];
+      sg += rb[2 * w + 1];
+    }
+    const float rstd = rstd_from_ss(ss, fN, a.eps);
+    const float c = __fdiv_rn(__fmul_rn(sg, rstd), fN);
+    const float2 rstd2 = splat2(rstd), c2 = splat2(c);
+    T* dxrow = static_cast<T*>(a.dx) + (c0 + k) * N;
+#pragma unroll
+    for (int q = 0; q < VPT; ++q) {
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 xn = mul2(unpack_again<T>(word(xv[q], e)), rstd2);
+        const float2 gf = unpack_again<T>(word(gv[q], e));
+        const float2 d = sub2(mul2(gf, wf[q][e]), mul2(xn, c2));
+        pk[e] = Elem<T>::pack(mul2(rstd2, d));
+        acc[q][e] = fma2(gf, xn, acc[q][e]);
+      }
+      if (okv[q]) st_stream16(dxrow + 8 * (tid + q * kStreamWarps * 32), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+    }
+    if (++slot == S) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+  float* prow = a.partial + static_cast<int64_t>(blockIdx.x) * N;
+#pragma unroll
+  for (int q = 0; q < VPT; ++q) {
+    if (!okv[q]) continue;
+    float* pp = prow + 8 * (tid + q * kStreamWarps * 32);
+    reinterpret_cast<float4*>(pp)[0] = make_float4(acc[q][0].x, acc[q][0].y, acc[q][1].x, acc[q][1].y);
+    reinterpret_cast<float4*>(pp)[1] = make_float4(acc[q][2].x, acc[q][2].y, acc[q][3].x, acc[q][3].y);
+  }
+}
+
+template <typename T, int VPT>
+bool launch_stage1_stream(const BwdArgs& a, const BwdPlan& plan, cudaStream_t s) {
+  BwdStream p{};
+  p.a = a;
+  p.rows_per_chunk = plan.rows_per_chunk;
+  p.status = device_status_ptr();
+  p.stage_bytes = ((2 * a.N * static_cast<int>(sizeof(T))) + 127) & ~127;
+  // As many stages as fit two CTAs per SM (at most 8); about 64 KB in flight per CTA.
+  p.stages = static_cast<int>((110 * 1024 - stream_smem_bytes(0, 0)) / (p.stage_bytes + 16));
+  if (p.stages > 8) p.stages = 8;
+  if (p.stages < 2) return false;
+  p.depth = (64 * 1024 + p.stage_bytes - 1) / p.stage_bytes;
+  if (p.depth < 2) p.depth = 2;
+  if (p.depth > p.stages) p.depth = p.stages;
+  const size_t smem = stream_smem_bytes(p.stages, p.stage_bytes);
+  auto kern = bwd_stage1_stream_kernel<T, VPT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    return false;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(plan.chunks));
+  cfg.blockDim = dim3(kStreamThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess;
+}
+
 template <typename T, int TPR, int VPT, int RB>
 void launch_stage1(const BwdArgs& a, const BwdPlan& p, cudaStream_t s) {
   constexpr int G = kThreads / TPR;
@@ -304,7 +533,11 @@ void launch_bwd_t(const BwdArgs& a, cudaStream_t s) {
   if (a.M > 0) {
     const int nv = a.N / 8;
     const bool vec = vector_ok(a, sizeof(T));
-    if (vec && nv <= 16) launch_stage1<T, 16, 1, 2>(a, p, s);
+    const char* sel = getenv("FQ_BWD_KERNEL");  // "generic": the global-load kernel (diagnostic switch)
+    const bool stream = vec && nv > 128 && nv <= 512 && !(sel != nullptr && strcmp(sel, "generic") == 0);
+    if (stream && nv <= 256 && launch_stage1_stream<T, 1>(a, p, s)) {
+    } else if (stream && launch_stage1_stream<T, 2>(a, p, s)) {
+    } else if (vec && nv <= 16) launch_stage1<T, 16, 1, 2>(a, p, s);
     else if (vec && nv <= 32) launch_stage1<T, 32, 1, 2>(a, p, s);
     else if (vec && nv <= 64) launch_stage1<T, 64, 1, 2>(a, p, s);
     else if (vec && nv <= 128) launch_stage1<T, 128, 1, 2>(a, p, s);

@@ -195,6 +195,39 @@ def test_rmsnorm_bwd_parity(orc, cuda_ok, case):
     assert torch.equal(dw.cpu(), dw32.cpu().to(dw.dtype))
 
 
+@pytest.mark.parametrize("kernel", ["stream", "generic"])
+@pytest.mark.parametrize("case", [(1000, 1536, "bf16"), (513, 4096, "fp16"), (300, 2056, "bf16")],
+                         ids=lambda c: "M%d-N%d-%s" % c)
+def test_rmsnorm_bwd_stream_kernel(orc, cuda_ok, monkeypatch, case, kernel):
+    """The TMA-fed stage 1 (rows of 1032..4096 elements) and the global-load stage 1 against the
+    oracle; idle column threads (N not a multiple of 2048) and fp16 included."""
+    M, N, dt = case
+    if kernel == "generic":
+        monkeypatch.setenv("FQ_BWD_KERNEL", "generic")
+    else:
+        monkeypatch.delenv("FQ_BWD_KERNEL", raising=False)
+    d = wl.rmsnorm_inputs(M, N, dt, seed=580 + M)
+    dx_ref, dw_ref, dw32_ref = orc.rmsnorm_bwd(d["x"], d["w"], d["g"])
+    g = cuda(d)
+    dx, dw, dw32 = fq.rmsnorm_bwd(g["x"], g["w"], g["g"])
+    assert_storage_close(dx, dx_ref, "dx")
+    assert_dw_close(dw32, dw32_ref)
+    assert_within_one_ulp(dw, dw_ref)
+    assert fq.device_status(clear=True) == 0
+
+
+def test_rmsnorm_bwd_stream_matches_generic_bitwise(cuda_ok, monkeypatch):
+    """Both stage-1 kernels give each thread the same columns and add in the same order: dx and the
+    fp32 dw sums agree bit for bit."""
+    d = cuda(wl.rmsnorm_inputs(777, 4096, "bf16", seed=590))
+    monkeypatch.delenv("FQ_BWD_KERNEL", raising=False)
+    a = fq.rmsnorm_bwd(d["x"], d["w"], d["g"])
+    monkeypatch.setenv("FQ_BWD_KERNEL", "generic")
+    b = fq.rmsnorm_bwd(d["x"], d["w"], d["g"])
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
 def test_rmsnorm_bwd_deterministic(cuda_ok):
     d = cuda(wl.rmsnorm_inputs(1000, 4096, "bf16", seed=550))
     a = fq.rmsnorm_bwd(d["x"], d["w"], d["g"])
