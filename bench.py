@@ -41,7 +41,8 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 T_TOK, HQ, HK, D = 4096, 32, 8, 128
 WORKLOAD = "qk_norm_rope_quant T=4096 Hq=32 Hk=8 D=128 rope_dim=128 bf16->e4m3 fp32-tables"
-KERNEL_SOURCES = ["fp8_quant_memory_gb300/csrc/fq_prologue.cu", "fp8_quant_memory_gb300/csrc/fq_device.cuh"]
+KERNEL_SOURCES = ["fp8_quant_memory_gb300/csrc/fq_prologue.cu", "fp8_quant_memory_gb300/csrc/fq_device.cuh",
+                  "fp8_quant_memory_gb300/csrc/fq_sync.cuh"]
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "qk_norm_rope_quant_4k.md")
 
 
