@@ -35,6 +35,9 @@ _SIGS = {
     "or_rmsnorm_rope": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _f32],
     "or_rmsnorm_rope_quant": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _f32, _f32],
     "or_quant_rows": [_vp, _vp, _vp, _i64, _i64, _int, _f32],
+    "or_rmsnorm_rope_quant_groups": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _int, _int,
+                                     _f32, _f32],
+    "or_quant_groups": [_vp, _vp, _vp, _i64, _i64, _i64, _int, _f32],
     "or_qk_norm_rope_quant": [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                               _int, _int, _f32, _f32],
     "or_rmsnorm_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _f32],
@@ -131,6 +134,30 @@ def quant_rows(y: torch.Tensor, fp8_max: float = 448.0):
     scale = torch.empty((M,), dtype=torch.float32)
     _check(lib().or_quant_rows(_p(y.contiguous()), _p(q), _p(scale), M, N, _FMT[y.dtype], fp8_max),
            "quant_rows")
+    return q, scale
+
+
+def rmsnorm_rope_quant_groups(x, w, cos, sin, group_size: int, eps: float = 1e-6, fp8_max: float = 448.0,
+                              want_y: bool = True):
+    """Group-wise scales: returns (y or None, q uint8 [M,N], scale fp32 [M, N/group_size])."""
+    M, N = x.shape
+    R = 2 * cos.shape[-1]
+    y = torch.empty_like(x) if want_y else None
+    q = torch.empty((M, N), dtype=torch.uint8)
+    scale = torch.empty((M, N // group_size), dtype=torch.float32)
+    _check(lib().or_rmsnorm_rope_quant_groups(_p(x), _p(w), _p(cos), _p(sin), _p(y), _p(q), _p(scale), M, N,
+                                              R, group_size, _FMT[x.dtype], _FMT[cos.dtype], eps, fp8_max),
+           "rmsnorm_rope_quant_groups")
+    return y, q, scale
+
+
+def quant_groups(y: torch.Tensor, group_size: int, fp8_max: float = 448.0):
+    """The group-wise quantiser alone on rows of a stored y: (q uint8 [M,N], scale fp32 [M, N/gs])."""
+    M, N = y.shape
+    q = torch.empty((M, N), dtype=torch.uint8)
+    scale = torch.empty((M, N // group_size), dtype=torch.float32)
+    _check(lib().or_quant_groups(_p(y.contiguous()), _p(q), _p(scale), M, N, group_size, _FMT[y.dtype],
+                                 fp8_max), "quant_groups")
     return q, scale
 
 

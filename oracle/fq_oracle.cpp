@@ -205,6 +205,26 @@ float quant_row(const float* y, int64_t N, float fp8_max, uint8_t* q) {
   return scale;
 }
 
+// Step 3 of "rms_norm_rope_quant_fused" on one fp32 row: the row viewed as n_groups = N / gs groups
+// of gs consecutive columns; per group, amax of |y| clamped at 1e-4, scale = amax / fp8_max, and
+// every element of the group divided by its group's scale, clamped to +-fp8_max, rounded to e4m3fn.
+void quant_groups(const float* y, int64_t N, int64_t gs, float fp8_max, uint8_t* q, float* scale) {
+  const int64_t n_groups = N / gs;
+  for (int64_t g = 0; g < n_groups; ++g) {
+    const float* yg = y + g * gs;
+    float amax = 0.0f;
+    for (int64_t k = 0; k < gs; ++k) amax = std::fmax(amax, std::fabs(yg[k]));
+    const float sc = std::fmax(amax, 1e-4f) / fp8_max;
+    for (int64_t k = 0; k < gs; ++k) {
+      float v = yg[k] / sc;
+      if (v > fp8_max) v = fp8_max;
+      if (v < -fp8_max) v = -fp8_max;
+      q[g * gs + k] = e4m3_encode(v);
+    }
+    scale[g] = sc;
+  }
+}
+
 }  // namespace
 
 extern "C" {
@@ -312,6 +332,42 @@ int or_quant_rows(const void* y, uint8_t* q, float* scale, int64_t M, int64_t N,
   for (int64_t i = 0; i < M; ++i) {
     for (int64_t j = 0; j < N; ++j) yr[j] = load_elem(dtype, y, i * N + j);
     scale[i] = quant_row(yr.data(), N, fp8_max, q + i * N);
+  }
+  return OR_OK;
+}
+
+// ---- a1-a8 with group-wise scales ("rmsnorm_rope_quant.py", rms_norm_rope_quant_fused: one fp32
+// scale per group_size consecutive columns, Scale[M, N / group_size]). N % group_size == 0.
+int or_rmsnorm_rope_quant_groups(const void* x, const void* w, const void* cs, const void* sn, void* y,
+                                 uint8_t* q, float* scale, int64_t M, int64_t N, int64_t R, int64_t gs,
+                                 int dtype, int tdtype, float eps, float fp8_max) {
+  if (!x || !w || (R > 0 && (!cs || !sn)) || !q || !scale || M < 0 || N <= 0 || R < 0 || R % 2 || R > N ||
+      gs < 1 || N % gs != 0 || !is_storage(dtype) || !is_table(tdtype) || !(fp8_max > 0.0f) ||
+      fp8_max > 448.0f)
+    return OR_BAD_ARG;
+  const int64_t n_groups = N / gs;
+  std::vector<float> wr(N), xr(N), yr(N), cr(R / 2 + 1), sr(R / 2 + 1);
+  for (int64_t j = 0; j < N; ++j) wr[j] = load_elem(dtype, w, j);
+  for (int64_t i = 0; i < M; ++i) {
+    normed_rope_row(dtype, tdtype, x, wr.data(), cs, sn, i, N, R, eps, xr.data(), yr.data(), cr.data(),
+                    sr.data());
+    if (y)
+      for (int64_t j = 0; j < N; ++j) store_elem(dtype, y, i * N + j, yr[j]);
+    quant_groups(yr.data(), N, gs, fp8_max, q + i * N, scale + i * n_groups);
+  }
+  return OR_OK;
+}
+
+// ---- the group-wise quantiser alone on a stored y
+int or_quant_groups(const void* y, uint8_t* q, float* scale, int64_t M, int64_t N, int64_t gs, int dtype,
+                    float fp8_max) {
+  if (!y || !q || !scale || M < 0 || N <= 0 || gs < 1 || N % gs != 0 || !is_table(dtype) ||
+      !(fp8_max > 0.0f) || fp8_max > 448.0f)
+    return OR_BAD_ARG;
+  std::vector<float> yr(N);
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) yr[j] = load_elem(dtype, y, i * N + j);
+    quant_groups(yr.data(), N, gs, fp8_max, q + i * N, scale + i * (N / gs));
   }
   return OR_OK;
 }

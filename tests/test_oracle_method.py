@@ -268,6 +268,77 @@ def test_quant_custom_fp8_max(orc):
     assert orc.decode(q[:, 3:]).item() == 240.0
 
 
+# --------------------------------------------------------------------------- group-wise scales
+def test_worked_quant_groups(orc):
+    c = G["quant_groups"]
+    y = torch.tensor(c["y_bf16"], dtype=FP32).to(BF16)
+    q, scale = orc.quant_groups(y, c["group_size"])
+    assert q.tolist() == c["q"]
+    assert scale.tolist() == [[float(np.float32(v)) for v in row] for row in c["scale"]]
+    q_row, _ = orc.quant_rows(y[:1].contiguous())
+    assert q_row[0].tolist() == c["q_per_row_row0"]
+
+
+def test_quant_groups_one_group_is_the_per_row_quantiser(orc):
+    """group_size = N reduces to one scale per row: bit for bit the per-row oracle."""
+    d = _quant_inputs(21)
+    y, q, scale = orc.rmsnorm_rope_quant(d["x"], d["w"], d["cos"], d["sin"])
+    N = d["x"].shape[1]
+    yg, qg, sg = orc.rmsnorm_rope_quant_groups(d["x"], d["w"], d["cos"], d["sin"], N)
+    assert torch.equal(yg.view(torch.int16), y.view(torch.int16))
+    assert torch.equal(qg, q) and torch.equal(sg[:, 0], scale)
+
+
+@pytest.mark.parametrize("gs", [8, 64, 128])
+def test_quant_groups_equal_rows_of_groups(orc, gs):
+    """Each group is quantised exactly like a row of its own: the [M, N] group-wise result equals
+    the per-row quantiser on the [M * N/gs, gs] view of the same y."""
+    d = _quant_inputs(22)
+    y, q, scale = orc.rmsnorm_rope_quant_groups(d["x"], d["w"], d["cos"], d["sin"], gs)
+    M, N = y.shape
+    q2, s2 = orc.quant_rows(y.reshape(M * N // gs, gs).contiguous())
+    assert torch.equal(q, q2.reshape(M, N)) and torch.equal(scale, s2.reshape(M, N // gs))
+    y_full = orc.rmsnorm_rope(d["x"], d["w"], d["cos"], d["sin"])
+    assert torch.equal(y.view(torch.int16), y_full.view(torch.int16))
+
+
+def test_quant_groups_each_group_reaches_fp8_max_and_is_local(orc):
+    """Every group's amax element lands on +-448 (code 0x7E/0xFE), and changing the values of one
+    group leaves every other group's codes and scales unchanged."""
+    gs = 128
+    y = (torch.randn(16, 512, generator=torch.Generator().manual_seed(23)) * 3).to(BF16)
+    q, scale = orc.quant_groups(y, gs)
+    mag = (q & 0x7F).reshape(16, 4, gs)
+    assert (mag.amax(-1) == 0x7E).all()
+    y2 = y.clone()
+    y2[:, 128:256] *= 7
+    q2, s2 = orc.quant_groups(y2, gs)
+    keep = torch.ones(4, dtype=torch.bool)
+    keep[1] = False
+    assert torch.equal(q.reshape(16, 4, gs)[:, keep], q2.reshape(16, 4, gs)[:, keep])
+    assert torch.equal(scale[:, keep], s2[:, keep])
+    assert not torch.equal(scale[:, 1], s2[:, 1])
+
+
+def test_quant_groups_dequant_error_bound(orc):
+    """|decode(q) * scale_g - y| <= half an e4m3 step of |y / scale_g| in every group."""
+    gs = 64
+    d = _quant_inputs(24)
+    y, q, scale = orc.rmsnorm_rope_quant_groups(d["x"], d["w"], d["cos"], d["sin"], gs)
+    M, N = y.shape
+    ratio = y.double().reshape(M, N // gs, gs) / scale.double()[:, :, None]
+    v = orc.decode(q).double().reshape(M, N // gs, gs)
+    err = (v - ratio).abs()
+    bound = torch.where(ratio.abs() >= 2.0 ** -6, ratio.abs() * 2.0 ** -4, torch.full_like(ratio, 2.0 ** -10))
+    assert (err <= bound * (1 + 1e-6)).all()
+
+
+def test_quant_groups_rejects_ragged_groups(orc):
+    d = _quant_inputs(25)
+    with pytest.raises(ValueError):
+        orc.rmsnorm_rope_quant_groups(d["x"], d["w"], d["cos"], d["sin"], 96)  # 512 % 96 != 0
+
+
 # --------------------------------------------------------------------------- prologue
 def _qk(T=6, Hq=4, Hk=2, D=128, seed=15, **kw):
     return wl.qk_inputs(T, Hq, Hk, D, seed=seed, **kw)
