@@ -258,8 +258,11 @@ class RopeCase(Case):
         self.fq.rmsnorm_rope(s["x"], s["w"], s["cos"], s["sin"], out=s["y"])
 
 
-class RopeQuantTinyCase(Case):
-    def __init__(self, dev, M=256, N=512, R=64, n_sets=8):
+class RopeQuantCase(Case):
+    """rmsnorm_rope_quant (one scale per row) or rmsnorm_rope_quant_groups (one per group_size columns)."""
+
+    def __init__(self, dev, M=256, N=512, R=64, group_size=None, write_y=True, n_sets=8, note="",
+                 seed=20261202):
         import fp8_quant_memory_gb300 as fq
         from fp8_quant_memory_gb300 import ledger
         from fp8_quant_memory_gb300 import workloads as wl
@@ -267,21 +270,30 @@ class RopeQuantTinyCase(Case):
         import torch
 
         self.fq = fq
-        self.name = f"rmsnorm_rope_quant M={M} N={N} R={R} bf16 (launch-bound)"
-        h = wl.rows_inputs(M, N, R, "bf16", "bf16", seed=20261202)
+        self.gs = group_size
+        self.write_y = write_y
+        kind = "rmsnorm_rope_quant" if group_size is None else f"rmsnorm_rope_quant_groups gs={group_size}"
+        self.name = f"{kind} M={M} N={N} R={R} bf16{'' if write_y else ' (no y)'}{note}"
+        h = wl.rows_inputs(M, N, R, "bf16", "bf16", seed=seed)
         self.sets = _make_sets(h, n_sets, dev)
+        n_scales = M if group_size is None else M * (N // group_size)
         for s in self.sets:
-            s["y"] = torch.empty_like(s["x"])
+            s["y"] = torch.empty_like(s["x"]) if write_y else None
             s["q"] = torch.empty((M, N), dtype=torch.uint8, device=dev)
-            s["scale"] = torch.empty((M,), dtype=torch.float32, device=dev)
-        self._bytes = ledger.rope_quant_bytes(M, N, R, "bf16", "bf16", write_y=True)
+            s["scale"] = torch.empty((n_scales,), dtype=torch.float32, device=dev)
+        self._bytes = ledger.rope_quant_bytes(M, N, R, "bf16", "bf16", write_y=write_y, group_size=group_size)
 
     def bytes_per_step(self):
         return self._bytes
 
     def launch(self, i):
         s = self.sets[i % len(self.sets)]
-        self.fq.rmsnorm_rope_quant(s["x"], s["w"], s["cos"], s["sin"], y=s["y"], q=s["q"], scale=s["scale"])
+        if self.gs is None:
+            self.fq.rmsnorm_rope_quant(s["x"], s["w"], s["cos"], s["sin"], want_y=self.write_y, y=s["y"],
+                                       q=s["q"], scale=s["scale"])
+        else:
+            self.fq.rmsnorm_rope_quant_groups(s["x"], s["w"], s["cos"], s["sin"], self.gs, want_y=self.write_y,
+                                              y=s["y"], q=s["q"], scale=s["scale"])
 
 
 class TorchEagerPrologueCase(Case):
@@ -509,7 +521,12 @@ SECONDARY = {
     "rmsnorm_fwd_8k_4k": lambda dev: RmsnormFwdCase(dev),
     "rmsnorm_bwd_8k_4k": lambda dev: RmsnormBwdCase(dev),
     "rope_fp16_64k": lambda dev: RopeCase(dev),
-    "rope_quant_tiny": lambda dev: RopeQuantTinyCase(dev),
+    "rope_quant_tiny": lambda dev: RopeQuantCase(dev, note=" (launch-bound)"),
+    "rope_quant_groups_tiny": lambda dev: RopeQuantCase(dev, group_size=128, note=" (launch-bound)"),
+    "rope_quant_ledger_4k": lambda dev: RopeQuantCase(dev, M=4096, N=4096, R=128, write_y=False, n_sets=8,
+                                                      note=" (Ch.13 ledger fused workload)"),
+    "rope_quant_groups_ledger_4k": lambda dev: RopeQuantCase(dev, M=4096, N=4096, R=128, group_size=128,
+                                                             write_y=False, n_sets=8),
     "qk_prologue_32k": lambda dev: PrologueCase(dev, T=32768, Hq=64, Hk=8, std=1.0, theta=1e6, positions="uniform",
                                                 outlier_frac=0.01, n_sets=2, seed=20261202 + 4),
 }

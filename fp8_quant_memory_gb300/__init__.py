@@ -22,7 +22,8 @@ import torch
 
 from . import _capi
 
-__all__ = ["rmsnorm_fwd", "rmsnorm_rope", "rmsnorm_rope_quant", "qk_norm_rope_quant", "rmsnorm_bwd",
+__all__ = ["rmsnorm_fwd", "rmsnorm_rope", "rmsnorm_rope_quant", "rmsnorm_rope_quant_groups", "qk_norm_rope_quant",
+           "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_bytes", "rmsnorm", "RMSNormFunction", "device_status", "check_bounded_wait",
            "FqError"]
 
@@ -112,6 +113,28 @@ def rmsnorm_rope_quant(x, w, cos, sin, eps: float = 1e-6, fp8_max: float = 448.0
     scale = torch.empty((M,), dtype=torch.float32, device=dev) if scale is None else scale
     _capi.call("fq_rmsnorm_rope_quant", _ptr(x), _ptr(w), _ptr(cos), _ptr(sin), _ptr(y), _ptr(q), _ptr(scale),
                M, N, R, _dtype(name, x), _table_dtype(name, cos, sin), eps, fp8_max, _stream(dev))
+    return y, q, scale
+
+
+def rmsnorm_rope_quant_groups(x, w, cos, sin, group_size: int, eps: float = 1e-6, fp8_max: float = 448.0,
+                              want_y: bool = True, y: torch.Tensor | None = None, q: torch.Tensor | None = None,
+                              scale: torch.Tensor | None = None):
+    """RMSNorm + NeoX partial RoPE + FP8 with one scale per group_size columns.
+    Returns (y or None, q uint8 [M,N], scale fp32 [M, N // group_size])."""
+    name = "rmsnorm_rope_quant_groups"
+    dev = _need_cuda(name, x, w, cos, sin, y, q, scale)
+    _contig(name, x=x, w=w, cos=cos, sin=sin, y=y, q=q, scale=scale)
+    M, N = x.shape
+    R = 2 * cos.shape[-1]
+    if group_size < 1 or N % group_size != 0:
+        raise ValueError(f"{name}: group_size must divide N (N={N}, group_size={group_size})")
+    if y is None and want_y:
+        y = torch.empty_like(x)
+    q = torch.empty((M, N), dtype=torch.uint8, device=dev) if q is None else q
+    scale = torch.empty((M, N // group_size), dtype=torch.float32, device=dev) if scale is None else scale
+    _capi.call("fq_rmsnorm_rope_quant_groups", _ptr(x), _ptr(w), _ptr(cos), _ptr(sin), _ptr(y), _ptr(q),
+               _ptr(scale), M, N, R, group_size, _dtype(name, x), _table_dtype(name, cos, sin), eps, fp8_max,
+               _stream(dev))
     return y, q, scale
 
 

@@ -87,6 +87,7 @@ int launch_rows(const char* fn, const fq::RowArgs& a, int mode, int dtype, int t
   if (a.y != nullptr) vec = vec && aligned(a.y, 16);
   if (a.q != nullptr) vec = vec && aligned(a.q, 8);
   if (a.scale != nullptr) vec = vec && aligned(a.scale, 4);
+  if (a.group > 0) vec = vec && (a.group % 8 == 0) && (a.N / a.group) <= fq::kMaxVecGroups;
   // FQ_PROLOGUE_KERNEL=generic (prologue) and FQ_ROWS_KERNEL=generic (RMSNorm forward, RMSNorm +
   // RoPE) select the generic vectorised kernel instead of the TMA-fed one (diagnostic switches: both
   // compute the same result).
@@ -197,14 +198,22 @@ int fq_rmsnorm_rope(const void* x, const void* w, const void* cos, const void* s
   return launch_rows(fn, a, fq::MODE_ROPE, dtype, table_dtype, stream);
 }
 
-int fq_rmsnorm_rope_quant(const void* x, const void* w, const void* cos, const void* sin, void* y,
-                          uint8_t* q, float* scale, int64_t M, int64_t N, int64_t rope_dim, int dtype,
-                          int table_dtype, float eps, float fp8_max, cudaStream_t stream) {
-  const char* fn = "fq_rmsnorm_rope_quant";
+}  // extern "C"
+
+namespace {
+
+// Shared body of fq_rmsnorm_rope_quant (group = 0: one scale per row) and
+// fq_rmsnorm_rope_quant_groups (group = columns per scale).
+int rope_quant(const char* fn, const void* x, const void* w, const void* cos, const void* sin, void* y, uint8_t* q,
+               float* scale, int64_t M, int64_t N, int64_t rope_dim, int64_t group, int dtype, int table_dtype,
+               float eps, float fp8_max, cudaStream_t stream) {
   if (int rc = check_common(fn, dtype, eps)) return rc;
   if (int rc = check_fp8_max(fn, fp8_max)) return rc;
   if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
     return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
+  if (group < 0 || (group > 0 && N % group != 0))
+    return fail(FQ_ERR_INVALID_ARG, "%s: group_size must divide N (N = %lld, group_size = %lld)", fn,
+                static_cast<long long>(N), static_cast<long long>(group));
   if (int rc = check_rope(fn, N, rope_dim, cos, sin, table_dtype, M == 0)) return rc;
   if (M == 0) return ok();
   if (x == nullptr || w == nullptr || q == nullptr || scale == nullptr)
@@ -224,7 +233,30 @@ int fq_rmsnorm_rope_quant(const void* x, const void* w, const void* cos, const v
   a.R = static_cast<int32_t>(rope_dim);
   a.eps = eps;
   a.fp8_max = fp8_max;
+  a.group = (group == N) ? 0 : static_cast<int32_t>(group);  // one group per row is the per-row path
   return launch_rows(fn, a, fq::MODE_ROPE_QUANT, dtype, table_dtype, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+int fq_rmsnorm_rope_quant(const void* x, const void* w, const void* cos, const void* sin, void* y,
+                          uint8_t* q, float* scale, int64_t M, int64_t N, int64_t rope_dim, int dtype,
+                          int table_dtype, float eps, float fp8_max, cudaStream_t stream) {
+  return rope_quant("fq_rmsnorm_rope_quant", x, w, cos, sin, y, q, scale, M, N, rope_dim, 0, dtype, table_dtype,
+                    eps, fp8_max, stream);
+}
+
+int fq_rmsnorm_rope_quant_groups(const void* x, const void* w, const void* cos, const void* sin, void* y,
+                                 uint8_t* q, float* scale, int64_t M, int64_t N, int64_t rope_dim,
+                                 int64_t group_size, int dtype, int table_dtype, float eps, float fp8_max,
+                                 cudaStream_t stream) {
+  if (group_size < 1)
+    return fail(FQ_ERR_INVALID_ARG, "fq_rmsnorm_rope_quant_groups: group_size must be >= 1, got %lld",
+                static_cast<long long>(group_size));
+  return rope_quant("fq_rmsnorm_rope_quant_groups", x, w, cos, sin, y, q, scale, M, N, rope_dim, group_size, dtype,
+                    table_dtype, eps, fp8_max, stream);
 }
 
 int fq_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, const void* wk,

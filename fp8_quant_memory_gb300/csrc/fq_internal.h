@@ -35,7 +35,11 @@ struct RowArgs {
   int32_t N, R;
   float eps;
   float fp8_max;
+  int32_t group;  // MODE_ROPE_QUANT: columns per fp32 scale, scale[r * (N / group) + g]; 0: one per row
 };
+
+// Group-wise scales on the vectorised path: group % 8 == 0 and at most this many groups per row.
+constexpr int kMaxVecGroups = 512;
 
 // Vectorised path: needs N % 8 == 0, R % 16 == 0, 16-byte aligned x/w/y/cos/sin and token stride,
 // 8-byte aligned q, table dtype equal to the storage dtype or fp32, and a supported width.

@@ -31,6 +31,7 @@ template <typename T, typename TT, int MODE, int LPR, int HS, int TS, int U>
 __global__ void __launch_bounds__(kThreads) rows_vec_kernel(const RowArgs a) {
   constexpr int kRowsPerCta = kThreads / LPR;
   constexpr int kV = HS + 2 * TS;
+  extern __shared__ uint32_t group_max[];  // [kRowsPerCta][N / a.group] with group-wise scales
 
   const int lane = threadIdx.x & (LPR - 1);
   const int grp = threadIdx.x / LPR;
@@ -63,10 +64,11 @@ __global__ void __launch_bounds__(kThreads) rows_vec_kernel(const RowArgs a) {
                        ? ld_stream16(xrow + slot_col<LPR, HS, TS>(s, lane, hv, th))
                        : make_uint4(0u, 0u, 0u, 0u);
     }
+    uint32_t* gmax = (MODE == MODE_ROPE_QUANT && a.group > 0) ? group_max + grp * (N / a.group) : nullptr;
 #pragma unroll
     for (int u = 0; u < U; ++u)
       row_body<T, TT, MODE, LPR, HS, TS, false>(a, r[u], rv[u], h[u], xv[u], lane, hv, th, fN, a.cos, a.sin,
-                                                static_cast<int64_t>(t[u]) * half);
+                                                static_cast<int64_t>(t[u]) * half, nullptr, gmax);
   }
 }
 
@@ -173,7 +175,18 @@ bool launch_one(const RowArgs& a, cudaStream_t s) {
   const int64_t need = (a.rows + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t cap = static_cast<int64_t>(sm_count()) * blocks_per_sm;
   const int grid = static_cast<int>(need < cap ? need : cap);
-  kern<<<grid, kThreads, 0, s>>>(a);
+  size_t smem = 0;
+  if (MODE == MODE_ROPE_QUANT && a.group > 0) {
+    smem = static_cast<size_t>(kThreads / LPR) * (a.N / a.group) * sizeof(uint32_t);
+    static size_t configured = 48 * 1024;
+    if (smem > configured) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+          cudaSuccess)
+        return false;
+      configured = smem;
+    }
+  }
+  kern<<<grid, kThreads, smem, s>>>(a);
   return true;
 }
 

@@ -80,6 +80,11 @@ __device__ __forceinline__ bool slot_ok(int s, int lane, int hv, int th) {
 
 // Everything after the loads for one row held by a lane group: rstd, normalise, rotate, write y
 // (fwd / rope modes write each vector as soon as it is computed), amax, scale, codes.
+// Group-wise scales (MODE_ROPE_QUANT with a.group > 0, "rms_norm_rope_quant_fused" step 3): `gmax`
+// is this row's array of N / a.group words in shared memory; each lane folds its slots' |y| maxima
+// into their groups with atomicMax on the float bits (non-negative floats order like their bits),
+// and quantises each slot with its own group's scale. A 16-byte vector never straddles a group
+// (a.group % 8 == 0).
 // Table entries of this row: cos_base/sin_base + trow + pair index (global memory, or a staged block
 // in shared memory when SMEM_TAB). WPRE: the caller holds this lane's weight vectors in `wpre` (one
 // per slot, loaded once for every row it processes; single-weight modes only), else they are read
@@ -88,7 +93,7 @@ template <typename T, typename TT, int MODE, int LPR, int HS, int TS, bool SMEM_
 __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, int32_t h,
                                          const uint4 (&xv)[HS + 2 * TS], int lane, int hv, int th, float fN,
                                          const void* cos_base, const void* sin_base, int64_t trow,
-                                         const uint4* wpre = nullptr) {
+                                         const uint4* wpre = nullptr, uint32_t* gmax = nullptr) {
   static_assert(!(WPRE && MODE == MODE_QK), "the prologue selects wq or wk per row");
   constexpr bool kQuant = (MODE == MODE_ROPE_QUANT) || (MODE == MODE_QK);
   constexpr bool kRound = (MODE == MODE_ROPE) || (MODE == MODE_ROPE_QUANT);
@@ -116,11 +121,13 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
 
   uint4 yp[kV];      // rounded y kept for the quantiser (MODE_ROPE_QUANT)
   float2 yf[kV][4];  // fp32 y kept for the quantiser (MODE_QK)
+  float ams[kV];     // per-slot |y| maxima (group-wise scales)
   float amax = 0.f;
 
   // a3: head columns, normalised (rounded to the storage dtype unless MODE_QK)
 #pragma unroll
   for (int s = 0; s < HS; ++s) {
+    ams[s] = 0.f;
     if (!slot_ok<LPR, HS, TS>(s, lane, hv, th)) {
       yp[s] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -139,7 +146,7 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
         set_word(packed, k, pk);
         if constexpr (kQuant) {
           const float2 rn = Elem<T>::unpack(pk);
-          amax = fmaxf(amax, fmaxf(fabsf(rn.x), fabsf(rn.y)));
+          ams[s] = fmaxf(ams[s], fmaxf(fabsf(rn.x), fabsf(rn.y)));
         }
       }
     }
@@ -147,7 +154,10 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
       amax = absmax4(absmax4(amax, yf[s][0], yf[s][1]), yf[s][2], yf[s][3]);
     } else {
       if (yrow != nullptr) st_stream16(yrow + slot_col<LPR, HS, TS>(s, lane, hv, th), packed);
-      if constexpr (kQuant) yp[s] = packed;
+      if constexpr (kQuant) {
+        yp[s] = packed;
+        amax = fmaxf(amax, ams[s]);
+      }
     }
   }
 
@@ -156,6 +166,7 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
 #pragma unroll
     for (int s = 0; s < TS; ++s) {
       const int slo = HS + s, shi = HS + TS + s;
+      ams[slo] = ams[shi] = 0.f;
       if (!slot_ok<LPR, HS, TS>(slo, lane, hv, th)) {
         yp[slo] = yp[shi] = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
@@ -186,7 +197,11 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
           const uint32_t plo = Elem<T>::pack(ylo), phi = Elem<T>::pack(yhi);
           set_word(plo4, k, plo);
           set_word(phi4, k, phi);
-          if constexpr (kQuant) amax = absmax4(amax, Elem<T>::unpack(plo), Elem<T>::unpack(phi));
+          if constexpr (kQuant) {
+            const float2 rl = Elem<T>::unpack(plo), rh = Elem<T>::unpack(phi);
+            ams[slo] = fmaxf(ams[slo], fmaxf(fabsf(rl.x), fabsf(rl.y)));
+            ams[shi] = fmaxf(ams[shi], fmaxf(fabsf(rh.x), fabsf(rh.y)));
+          }
         }
       }
       if constexpr (MODE == MODE_QK) {
@@ -200,8 +215,45 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
         if constexpr (kQuant) {
           yp[slo] = plo4;
           yp[shi] = phi4;
+          amax = fmaxf(amax, fmaxf(ams[slo], ams[shi]));
         }
       }
+    }
+  }
+
+  // a6-a8 with group-wise scales
+  if constexpr (MODE == MODE_ROPE_QUANT) {
+    if (gmax != nullptr) {
+      const int gs = a.group, G = N / gs;
+      __syncwarp();  // the previous row's readers of this array are done
+      for (int g = lane; g < G; g += LPR) gmax[g] = 0u;
+      __syncwarp();
+#pragma unroll
+      for (int s = 0; s < kV; ++s)
+        if (slot_ok<LPR, HS, TS>(s, lane, hv, th))
+          atomicMax(&gmax[slot_col<LPR, HS, TS>(s, lane, hv, th) / gs], __float_as_uint(ams[s]));
+      __syncwarp();
+      if (rv) {
+        const bool clamp = a.fp8_max != 448.0f;
+        uint8_t* qrow = a.q + static_cast<int64_t>(r) * N;
+#pragma unroll
+        for (int s = 0; s < kV; ++s) {
+          if (!slot_ok<LPR, HS, TS>(s, lane, hv, th)) continue;
+          const int col = slot_col<LPR, HS, TS>(s, lane, hv, th);
+          const float sc = __fdiv_rn(fmaxf(__uint_as_float(gmax[col / gs]), 1e-4f), a.fp8_max);
+          const float rc = __frcp_rn(sc);
+          float2 v[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[k] = div2_by(Elem<T>::unpack(word(yp[s], k)), sc, rc);
+            if (clamp) v[k] = make_float2(clamp_abs(v[k].x, a.fp8_max), clamp_abs(v[k].y, a.fp8_max));
+          }
+          st_stream8(qrow + col, pack_e4m3x8(v[0], v[1], v[2], v[3]));
+        }
+        for (int g = lane; g < G; g += LPR)
+          a.scale[static_cast<int64_t>(r) * G + g] = __fdiv_rn(fmaxf(__uint_as_float(gmax[g]), 1e-4f), a.fp8_max);
+      }
+      return;
     }
   }
 

@@ -100,21 +100,27 @@ __global__ void __launch_bounds__(kThreads)
     ss = group_sum<32>(ss);
     c.rstd = rstd_from_ss(ss, static_cast<float>(a.N), a.eps);
 
-    float amax = 0.f;
-    for (int j = lane; j < a.N; j += 32) {
-      const float y = (mode == MODE_FWD) ? __fmul_rn(__fmul_rn(ld_any(dt, c.x, j), c.rstd), ld_any(dt, c.w, j))
-                                         : y_at(c, a.cos, a.sin, j);
-      if (a.y != nullptr && mode != MODE_QK) st_any(dt, a.y, r * a.N + j, y);
-      amax = fmaxf(amax, fabsf(y));
-    }
+    if (mode != MODE_QK && a.y != nullptr)
+      for (int j = lane; j < a.N; j += 32) {
+        const float y = (mode == MODE_FWD) ? __fmul_rn(__fmul_rn(ld_any(dt, c.x, j), c.rstd), ld_any(dt, c.w, j))
+                                           : y_at(c, a.cos, a.sin, j);
+        st_any(dt, a.y, r * a.N + j, y);
+      }
     if (!quant) continue;
-    amax = fmaxf(group_max<32>(amax), 1e-4f);
-    const float sc = __fdiv_rn(amax, a.fp8_max);
-    for (int j = lane; j < a.N; j += 32) {
-      const float y = y_at(c, a.cos, a.sin, j);
-      a.q[r * a.N + j] = e4m3(clamp_abs(__fdiv_rn(y, sc), a.fp8_max));
+    // One scale per group of gs consecutive columns (gs = N: one per row).
+    const int gs = (mode == MODE_ROPE_QUANT && a.group > 0) ? a.group : a.N;
+    const int G = a.N / gs;
+    for (int g = 0; g < G; ++g) {
+      float amax = 0.f;
+      for (int j = g * gs + lane; j < (g + 1) * gs; j += 32) amax = fmaxf(amax, fabsf(y_at(c, a.cos, a.sin, j)));
+      amax = fmaxf(group_max<32>(amax), 1e-4f);
+      const float sc = __fdiv_rn(amax, a.fp8_max);
+      for (int j = g * gs + lane; j < (g + 1) * gs; j += 32) {
+        const float y = y_at(c, a.cos, a.sin, j);
+        a.q[r * a.N + j] = e4m3(clamp_abs(__fdiv_rn(y, sc), a.fp8_max));
+      }
+      if (lane == 0) a.scale[r * G + g] = sc;
     }
-    if (lane == 0) a.scale[r] = sc;
   }
 }
 

@@ -25,10 +25,13 @@ def qk_prologue_bytes(T: int, Hq: int, Hk: int, D: int, R: int | None = None, dt
 
 
 def rope_quant_bytes(M: int, N: int, R: int, dtype: str = "bf16", table_dtype: str = "bf16",
-                     write_y: bool = True) -> int:
+                     write_y: bool = True, group_size: int | None = None) -> int:
+    """x, w, cos/sin read; y (optional), codes and the fp32 scales written (one per row, or one per
+    group_size columns)."""
     e = ELEM_BYTES[dtype]
+    n_scales = M if group_size is None else M * (N // group_size)
     return (M * N * e + N * e + 2 * M * (R // 2) * ELEM_BYTES[table_dtype] + (M * N * e if write_y else 0)
-            + M * N + M * 4)
+            + M * N + n_scales * 4)
 
 
 def rope_bytes(M: int, N: int, R: int, dtype: str = "fp16", table_dtype: str = "fp16") -> int:

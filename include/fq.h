@@ -109,6 +109,23 @@ int fq_rmsnorm_rope_quant(const void* x, const void* w, const void* cos, const v
                           int table_dtype, float eps, float fp8_max, cudaStream_t stream);
 
 /*
+ * RMSNorm + NeoX partial RoPE + FP8 with group-wise scales ("rmsnorm_rope_quant.py",
+ * rms_norm_rope_quant_fused, step 3: one fp32 scale per group_size consecutive columns):
+ *   y as in fq_rmsnorm_rope (rounded to dtype);
+ *   for every row i and group g < G = N / group_size, columns J_g = [g*group_size, (g+1)*group_size):
+ *     scale[i*G + g] = max(max_{j in J_g} |y_ij|, 1e-4) / fp8_max               (fp32)
+ *     q_ij = e4m3fn_round_to_nearest_even(clamp(y_ij / scale[i*G + g], -fp8_max, fp8_max))
+ * y: [M, N] dtype or null; q: [M, N] uint8 e4m3fn codes; scale: [M, G] fp32, row-major.
+ * group_size >= 1 must divide N (else FQ_ERR_INVALID_ARG); group_size = N gives exactly
+ * fq_rmsnorm_rope_quant. Other arguments and errors as fq_rmsnorm_rope_quant. Group sizes that are
+ * multiples of 8 with at most 512 groups per row take the vectorised kernel, others the scalar one.
+ */
+int fq_rmsnorm_rope_quant_groups(const void* x, const void* w, const void* cos, const void* sin, void* y,
+                                 uint8_t* q, float* scale, int64_t M, int64_t N, int64_t rope_dim,
+                                 int64_t group_size, int dtype, int table_dtype, float eps, float fp8_max,
+                                 cudaStream_t stream);
+
+/*
  * QK-Norm + RoPE + FP8 attention prologue ("case_norm_rope_quant.py", module docstring; design C):
  *   for every token t < T and head h < H = Hq + Hk, the row x = qk[t*token_stride + h*D + (0..D-1)]
  *   is normalised with wq (h < Hq) or wk (h >= Hq), its last R columns are rotated with table row t

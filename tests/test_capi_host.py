@@ -98,6 +98,18 @@ def test_shape_rules_rejected(lib):
                1e-6, 448.0, NULL)[0] == 1
 
 
+def test_group_size_rules_rejected(lib):
+    """Group-wise scales: group_size must be >= 1 and divide N; checked on the host."""
+    p = ctypes.c_void_p(16)
+    f = "fq_rmsnorm_rope_quant_groups"
+    rc, msg = _rc(lib, f, p, p, p, p, NULL, p, p, 4, 512, 64, 96, 0, 0, 1e-6, 448.0, NULL)
+    assert rc == 1 and "group_size" in msg
+    assert _rc(lib, f, p, p, p, p, NULL, p, p, 4, 512, 64, 0, 0, 0, 1e-6, 448.0, NULL)[0] == 1
+    assert _rc(lib, f, p, p, p, p, NULL, p, p, 4, 512, 64, -8, 0, 0, 1e-6, 448.0, NULL)[0] == 1
+    assert _rc(lib, f, p, p, p, p, NULL, NULL, p, 4, 512, 64, 128, 0, 0, 1e-6, 448.0, NULL)[0] == 1  # null q
+    assert _rc(lib, f, p, p, p, p, NULL, p, p, 0, 512, 64, 128, 0, 0, 1e-6, 448.0, NULL)[0] == 0     # empty
+
+
 def test_empty_batches_are_noops_without_cuda(lib):
     p = ctypes.c_void_p(16)
     assert _rc(lib, "fq_rmsnorm_fwd", p, p, p, 0, 8, 0, 1e-6, NULL)[0] == 0

@@ -148,6 +148,59 @@ def test_rmsnorm_rope_quant_scalar_path_matches(orc, cuda_ok):
     assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
 
 
+# ----------------------------------------------------------------------------------- group-wise scales
+GROUP_CASES = [
+    # M, N, R, group_size, dtype, table
+    (256, 512, 64, 128, "bf16", "bf16"),   # the tiny workload, 4 groups (the last spans head and tail)
+    (300, 512, 64, 64, "fp16", "fp32"),
+    (100, 192, 64, 32, "bf16", "bf16"),    # groups inside the tail-lo / tail-hi halves
+    (77, 4096, 128, 128, "bf16", "bf16"),  # 32 groups on a wide row
+    (50, 1024, 0, 8, "bf16", "bf16"),      # the smallest vector group, no rotation
+    (9, 2048, 64, 8, "fp16", "fp16"),      # 256 groups per row
+    (33, 96, 32, 12, "bf16", "bf16"),      # group not a multiple of 8: scalar kernel
+    (40, 100, 50, 25, "bf16", "fp32"),     # odd width: scalar kernel
+    (5, 64, 16, 1, "bf16", "bf16"),        # one column per group: scalar kernel
+]
+
+
+@pytest.mark.parametrize("case", GROUP_CASES, ids=lambda c: "M%d-N%d-R%d-g%d-%s-%s" % c)
+def test_rmsnorm_rope_quant_groups_parity(orc, cuda_ok, case):
+    M, N, R, gs, dt, tdt = case
+    d = wl.rows_inputs(M, N, R, dt, tdt, seed=260 + M)
+    y_ref, q_ref, s_ref = orc.rmsnorm_rope_quant_groups(d["x"], d["w"], d["cos"], d["sin"], gs)
+    g = cuda(d)
+    y, q, s = fq.rmsnorm_rope_quant_groups(g["x"], g["w"], g["cos"], g["sin"], gs)
+    torch.cuda.synchronize()
+    assert s.shape == (M, N // gs)
+    assert_storage_close(y, y_ref)
+    # codes and scales are the group-wise quantiser applied to the kernel's own y: exact
+    q_own, s_own = orc.quant_groups(y.cpu(), gs)
+    assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
+    assert_codes_close(q, q_ref)
+    _, q2, s2 = fq.rmsnorm_rope_quant_groups(g["x"], g["w"], g["cos"], g["sin"], gs, want_y=False)
+    assert torch.equal(q2, q) and torch.equal(s2, s)
+    assert fq.device_status(clear=True) == 0
+
+
+def test_rmsnorm_rope_quant_groups_one_group_is_per_row(cuda_ok):
+    """group_size = N is the per-row entry point, bit for bit."""
+    g = cuda(wl.rows_inputs(128, 512, 64, "bf16", "bf16", seed=290))
+    y1, q1, s1 = fq.rmsnorm_rope_quant(g["x"], g["w"], g["cos"], g["sin"])
+    y2, q2, s2 = fq.rmsnorm_rope_quant_groups(g["x"], g["w"], g["cos"], g["sin"], 512)
+    assert torch.equal(y1, y2) and torch.equal(q1, q2) and torch.equal(s1, s2[:, 0])
+
+
+def test_rmsnorm_rope_quant_groups_scalar_path_matches(orc, cuda_ok):
+    """A vector-eligible shape at a misaligned address takes the scalar kernel: same rules."""
+    d = wl.rows_inputs(61, 512, 64, "bf16", "bf16", seed=291)
+    y_ref, q_ref, _ = orc.rmsnorm_rope_quant_groups(d["x"], d["w"], d["cos"], d["sin"], 128)
+    g = cuda(d)
+    y, q, s = fq.rmsnorm_rope_quant_groups(misalign(g["x"]), g["w"], g["cos"], g["sin"], 128)
+    assert_storage_close(y, y_ref)
+    q_own, s_own = orc.quant_groups(y.cpu(), 128)
+    assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
+
+
 # ----------------------------------------------------------------------------------- rmsnorm_rope
 @pytest.mark.parametrize("case", [(4096, 192, 64, "fp16", "fp16", 32), (100, 192, 64, "bf16", "fp32", 1),
                                   (64, 256, 32, "bf16", "bf16", 1), (10, 70, 14, "fp16", "fp16", 1)],
