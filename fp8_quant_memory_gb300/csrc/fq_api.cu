@@ -94,7 +94,8 @@ int launch_rows(const char* fn, const fq::RowArgs& a, int mode, int dtype, int t
   if (vec && mode == fq::MODE_QK && !env_is("FQ_PROLOGUE_KERNEL", "generic") &&
       fq::launch_prologue_tma(a, dtype, table_dtype, s))
     return check_launch(fn);
-  if (vec && (mode == fq::MODE_FWD || mode == fq::MODE_ROPE) && !env_is("FQ_ROWS_KERNEL", "generic") &&
+  if (vec && (mode == fq::MODE_FWD || mode == fq::MODE_ROPE || mode == fq::MODE_ROPE_QUANT) &&
+      !env_is("FQ_ROWS_KERNEL", "generic") &&
       fq::launch_rows_tma(a, mode, dtype, table_dtype, s))
     return check_launch(fn);
   if (!(vec && fq::launch_rows_vector(a, mode, dtype, table_dtype, s)))

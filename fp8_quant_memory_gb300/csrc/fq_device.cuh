@@ -143,10 +143,14 @@ __device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
 // q0 = RN(y*r) is within one ulp of y/s, the residual y - q0*s is exact in one FMA, and
 // RN(q0 + residual*r) is the correctly rounded quotient (Markstein's correction, IBM J. Res.
 // Dev. 34(1), 1990; Muller et al., Handbook of Floating-Point Arithmetic, ch. 4).
+// The correction step turns y = -0 into +0 (+0 + -0 rounds to +0), while the definition's y / s
+// keeps the sign of zero (and e4m3fn codes it as 0x80); every other quotient already has the sign
+// of y, so copying that sign back is exact.
 __device__ __forceinline__ float2 div2_by(float2 y, float s, float r) {
   const float2 q0 = mul2(y, splat2(r));
   const float2 e = fma2(q0, splat2(-s), y);  // y - q0*s, exact: (-q0)*s == q0*(-s)
-  return fma2(e, splat2(r), q0);
+  const float2 q = fma2(e, splat2(r), q0);
+  return make_float2(copysignf(q.x, y.x), copysignf(q.y, y.y));
 }
 
 // ------------------------------------------------------------------------------------------------

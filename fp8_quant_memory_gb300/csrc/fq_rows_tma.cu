@@ -336,25 +336,200 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_fwd_kernel(const S
   }
 }
 
+// ------------------------------------------------------------------ wide rows, rotation (+ FP8)
+// RMSNorm + NeoX partial RoPE, and with QUANT the per-row or group-wise FP8 codes, for rows of
+// N >= 1024: four consumer warps, one row per warp per stage. Pass 1: sum of squares over the
+// staged row. Pass 2: head vectors normalised, rotary pairs normalised and rotated (both members of
+// a pair and the row's cos/sin entries are in shared memory: no shuffle), each result rounded to
+// the storage dtype as the definition does, written to y and -- when quantising -- back into the
+// row's own place in the stage. Pass 3 (QUANT): codes from the staged y with the row's (or the
+// group's) scale. Group maxima: atomicMax on the float bits in a per-warp array of N / group words.
+template <typename T, typename TT, bool QUANT>
+__global__ void __launch_bounds__(kWideThreads) rows_tma_wide_rope_kernel(const StreamArgs p) {
+  extern __shared__ unsigned char smem_raw[];
+  constexpr int SR = kWideWarps;  // one row per warp per stage
+  const Ring g = ring_setup(p, smem_raw, kWideWarps);
+  const RowArgs& a = p.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kWideWarps) {
+    if (lane == 0)
+      produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, SR, sizeof(T), sizeof(TT));
+    return;
+  }
+  const int N = a.N, nv = N >> 3, hv = (N - a.R) >> 3, th = a.R >> 4, half = a.R >> 1;
+  const float fN = static_cast<float>(N);
+  const uint4* ws = reinterpret_cast<const uint4*>(g.w);
+  const bool grouped = QUANT && a.group > 0;
+  const int gs = grouped ? a.group : N;
+  const int G = N / gs;
+  // Per warp: [G] group maxima (float bits), then [G] scales and [G] reciprocals.
+  uint32_t* gmax = grouped ? reinterpret_cast<uint32_t*>(g.w + p.w_bytes) + warp * 3 * G : nullptr;
+  float* gsc = grouped ? reinterpret_cast<float*>(gmax + G) : nullptr;
+  float* grc = grouped ? gsc + G : nullptr;
+  const bool clamp = a.fp8_max != 448.0f;
+  if (!mbar_wait(kWaitLimitNs, g.wbar, 0u)) {
+    flag_failure(p.status);
+    return;
+  }
+  int slot = 0;
+  uint32_t phase = 0;
+  for (;;) {
+    if (!mbar_wait(kWaitLimitNs, &g.full[slot], phase)) {
+      flag_failure(p.status);
+      return;
+    }
+    const int32_t rs = g.stage_row[slot];
+    if (rs < 0) break;  // end marker
+    const int32_t r = rs + warp;
+    if (r < static_cast<int32_t>(a.rows)) {  // warp-uniform
+      unsigned char* st = g.smem + static_cast<size_t>(slot) * p.stage_bytes;
+      uint4* xs = reinterpret_cast<uint4*>(st + static_cast<size_t>(warp) * N * sizeof(T));
+      const TT* cs = reinterpret_cast<const TT*>(st + p.tab_off) + warp * half;
+      const TT* sn = reinterpret_cast<const TT*>(st + p.tab_off + p.tab_block) + warp * half;
+      // pass 1: sum of squares
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      for (int v = lane; v < nv; v += 32) {
+        const uint4 u = xs[v];
+        const float2 f0 = Elem<T>::unpack(u.x), f1 = Elem<T>::unpack(u.y);
+        const float2 f2 = Elem<T>::unpack(u.z), f3 = Elem<T>::unpack(u.w);
+        acc0 = fma2(f0, f0, acc0);
+        acc1 = fma2(f1, f1, acc1);
+        acc0 = fma2(f2, f2, acc0);
+        acc1 = fma2(f3, f3, acc1);
+      }
+      const float2 acc = add2(acc0, acc1);
+      const float2 rstd2 = splat2(rstd_from_ss(group_sum<32>(acc.x + acc.y), fN, a.eps));
+      T* yrow = a.y != nullptr ? static_cast<T*>(a.y) + static_cast<int64_t>(r) * N : nullptr;
+      float amax = 0.f;
+      if (grouped) {
+        __syncwarp();  // the previous row's readers of the group maxima are done
+        for (int q = lane; q < G; q += 32) gmax[q] = 0u;
+        __syncwarp();
+      }
+      // pass 2a: head columns
+      for (int v = lane; v < hv; v += 32) {
+        const uint4 u = xs[v], wv = ws[v];
+        uint4 out;
+        float m = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t pk =
+              Elem<T>::pack(mul2(mul2(Elem<T>::unpack(rows::word(u, k)), rstd2), Elem<T>::unpack(rows::word(wv, k))));
+          rows::set_word(out, k, pk);
+          if (QUANT) {
+            const float2 rn = Elem<T>::unpack(pk);
+            m = fmaxf(m, fmaxf(fabsf(rn.x), fabsf(rn.y)));
+          }
+        }
+        if (yrow != nullptr) st_stream16(yrow + 8 * v, out);
+        if (QUANT) {
+          xs[v] = out;
+          amax = fmaxf(amax, m);
+          if (grouped) atomicMax(&gmax[(8 * v) / gs], __float_as_uint(m));
+        }
+      }
+      // pass 2b: rotary pairs (tail-lo vector hv + i with tail-hi vector hv + th + i)
+      for (int i = lane; i < th; i += 32) {
+        const int vlo = hv + i, vhi = hv + th + i;
+        const uint4 ulo = xs[vlo], uhi = xs[vhi], wlo = ws[vlo], whi = ws[vhi];
+        float2 c[4], s4[4];
+        rows::load_table8<TT, true>(cs, 8 * i, c);
+        rows::load_table8<TT, true>(sn, 8 * i, s4);
+        uint4 plo4, phi4;
+        float mlo = 0.f, mhi = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 lo =
+              round_trip<T>(mul2(mul2(Elem<T>::unpack(rows::word(ulo, k)), rstd2), Elem<T>::unpack(rows::word(wlo, k))));
+          const float2 hi =
+              round_trip<T>(mul2(mul2(Elem<T>::unpack(rows::word(uhi, k)), rstd2), Elem<T>::unpack(rows::word(whi, k))));
+          const uint32_t plo = Elem<T>::pack(sub2(mul2(lo, c[k]), mul2(hi, s4[k])));
+          const uint32_t phi = Elem<T>::pack(add2(mul2(hi, c[k]), mul2(lo, s4[k])));
+          rows::set_word(plo4, k, plo);
+          rows::set_word(phi4, k, phi);
+          if (QUANT) {
+            const float2 rl = Elem<T>::unpack(plo), rh = Elem<T>::unpack(phi);
+            mlo = fmaxf(mlo, fmaxf(fabsf(rl.x), fabsf(rl.y)));
+            mhi = fmaxf(mhi, fmaxf(fabsf(rh.x), fabsf(rh.y)));
+          }
+        }
+        if (yrow != nullptr) {
+          st_stream16(yrow + 8 * vlo, plo4);
+          st_stream16(yrow + 8 * vhi, phi4);
+        }
+        if (QUANT) {
+          xs[vlo] = plo4;
+          xs[vhi] = phi4;
+          amax = fmaxf(amax, fmaxf(mlo, mhi));
+          if (grouped) {
+            atomicMax(&gmax[(8 * vlo) / gs], __float_as_uint(mlo));
+            atomicMax(&gmax[(8 * vhi) / gs], __float_as_uint(mhi));
+          }
+        }
+      }
+      if constexpr (QUANT) {
+        // pass 3: codes from the staged y
+        __syncwarp();
+        const float sc = __fdiv_rn(fmaxf(group_max<32>(amax), 1e-4f), a.fp8_max);
+        const float rc = __frcp_rn(sc);
+        if (grouped) {  // one scale and reciprocal per group, then written out
+          for (int q = lane; q < G; q += 32) {
+            const float sg = __fdiv_rn(fmaxf(__uint_as_float(gmax[q]), 1e-4f), a.fp8_max);
+            gsc[q] = sg;
+            grc[q] = __frcp_rn(sg);
+            a.scale[static_cast<int64_t>(r) * G + q] = sg;
+          }
+          __syncwarp();
+        }
+        uint8_t* qrow = a.q + static_cast<int64_t>(r) * N;
+        for (int v = lane; v < nv; v += 32) {
+          const uint4 u = xs[v];
+          float s_v = sc, r_v = rc;
+          if (grouped) {
+            const int q = (8 * v) / gs;
+            s_v = gsc[q];
+            r_v = grc[q];
+          }
+          float2 q4[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            q4[k] = div2_by(Elem<T>::unpack(rows::word(u, k)), s_v, r_v);
+            if (clamp) q4[k] = make_float2(clamp_abs(q4[k].x, a.fp8_max), clamp_abs(q4[k].y, a.fp8_max));
+          }
+          st_stream8(qrow + 8 * v, pack_e4m3x8(q4[0], q4[1], q4[2], q4[3]));
+        }
+        if (!grouped && lane == 0) a.scale[r] = sc;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&g.empty[slot]);
+    if (++slot == p.stages) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------- host side
 template <typename K>
 bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_bytes, int tab_row_bytes,
-                   cudaStream_t s) {
+                   cudaStream_t s, int extra_bytes = 0) {
   const RowArgs& a = p.a;
   p.status = device_status_ptr();
   p.tab_block = ((stage_rows * tab_row_bytes) + 127) & ~127;
   p.tab_off = (stage_rows * x_row_bytes + 127) & ~127;
   p.stage_bytes = p.tab_off + 2 * p.tab_block;
-  // Two CTAs per SM when stages are small; as many stages as fit, at most 8.
-  const int budget = p.stage_bytes <= 32 * 1024 ? 110 * 1024 : 220 * 1024;
-  p.stages = (budget - static_cast<int>(ring_bytes(0, 0, p.w_bytes)) - 8) / (p.stage_bytes + 20);
+  // Two CTAs per SM when stages are small (a four-row stage of 4096-wide rows with its table rows
+  // still fits three times); as many stages as fit, at most 8.
+  const int budget = p.stage_bytes <= 36 * 1024 ? 110 * 1024 : 220 * 1024;
+  p.stages = (budget - static_cast<int>(ring_bytes(0, 0, p.w_bytes)) - extra_bytes - 8) / (p.stage_bytes + 20);
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) return false;
   // Keep about 48 KB in flight per CTA (at least two stages), never more than the ring.
   p.depth = (48 * 1024 + p.stage_bytes - 1) / p.stage_bytes;
   if (p.depth < 2) p.depth = 2;
   if (p.depth > p.stages) p.depth = p.stages;
-  const size_t smem = ring_bytes(p.stages, p.stage_bytes, p.w_bytes);
+  const size_t smem = ring_bytes(p.stages, p.stage_bytes, p.w_bytes) + extra_bytes;
   if (smem > 227 * 1024) return false;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return false;
@@ -403,8 +578,30 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
   // Small problems are launch-bound: the generic kernel. Row indices and row + stage stay in int32.
   if (a.rows < 4096 || a.rows > 0x7fffffffLL - 256) return false;
   if (a.token_stride != a.N || a.H != 1) return false;       // contiguous rows only
-  if (mode != MODE_FWD && mode != MODE_ROPE) return false;
-  if (mode == MODE_ROPE && a.R > 0 && table_dtype != DT_FP32 && table_dtype != dtype) return false;
+  if (mode != MODE_FWD && mode != MODE_ROPE && mode != MODE_ROPE_QUANT) return false;
+  if (mode != MODE_FWD && a.R > 0 && table_dtype != DT_FP32 && table_dtype != dtype) return false;
+  if (mode != MODE_FWD && a.N >= 1024) {
+    StreamArgs p{};
+    p.a = a;
+    const int xrow = a.N * 2;
+    p.w_bytes = xrow;
+    const int tsz = (a.R > 0 && table_dtype == DT_FP32) ? 4 : 2;
+    const int trow = (a.R / 2) * tsz;
+    const int extra = (mode == MODE_ROPE_QUANT && a.group > 0) ? kWideWarps * 3 * (a.N / a.group) * 4 : 0;
+    const bool quant = mode == MODE_ROPE_QUANT;
+#define FQ_WIDE(T, TT)                                                                                      \
+  return quant ? launch_stream(rows_tma_wide_rope_kernel<T, TT, true>, kWideThreads, p, kWideWarps, xrow, trow, s, \
+                               extra)                                                                       \
+               : launch_stream(rows_tma_wide_rope_kernel<T, TT, false>, kWideThreads, p, kWideWarps, xrow, trow, s)
+    if (dtype == DT_BF16) {
+      if (tsz == 4) FQ_WIDE(__nv_bfloat16, float);
+      FQ_WIDE(__nv_bfloat16, __nv_bfloat16);
+    }
+    if (tsz == 4) FQ_WIDE(__half, float);
+    FQ_WIDE(__half, __half);
+#undef FQ_WIDE
+  }
+  if (mode == MODE_ROPE_QUANT) return false;  // narrower quantising rows: the generic kernel
   if (mode == MODE_FWD && a.N >= 1024) {
     StreamArgs p{};
     p.a = a;

@@ -2,6 +2,8 @@
 
 - bf16 outputs: |gpu - ref| <= max(2^-7 |ref|, 1e-3)   (the stated bf16 tolerance)
 - fp16 outputs: |gpu - ref| <= max(2^-9 |ref|, 1e-3)   (two fp16 ulps; fp16 has 3 more bits)
+- rotated columns of rmsnorm_rope(_quant): the same relative bound applied to |y| + |lo*c| + |hi*s|
+  (assert_rope_close: the definition rounds the normalised row before rotating it)
 - fp32 scales:  relative difference <= 1e-5
 - fp8 codes:    identical, or one e4m3 step apart on at most 0.1% of the elements
 - dw (fp32 sums): |gpu - ref| <= 1e-3 * max(|ref|, rms(ref)); bf16/fp16 dw within one ulp
@@ -21,6 +23,38 @@ def assert_storage_close(gpu: torch.Tensor, ref: torch.Tensor, what: str = "y"):
     b = ref.double()
     err = (a - b).abs()
     bound = torch.clamp(b.abs() * rel, min=abs_)
+    bad = err > bound
+    assert not bool(bad.any()), (
+        f"{what}: {int(bad.sum())} of {bad.numel()} elements outside the tolerance; worst err "
+        f"{float(err.max()):.3g} at ref {float(b.flatten()[int(err.flatten().argmax())]):.5g}")
+
+
+def assert_rope_close(gpu: torch.Tensor, ref: torch.Tensor, normed: torch.Tensor, cos: torch.Tensor,
+                      sin: torch.Tensor, what: str = "y"):
+    """Tolerance for rmsnorm_rope / rmsnorm_rope_quant outputs y [M, N] (cos, sin: [M, R/2]).
+
+    Head columns: the storage rule. Rotated columns: "rmsnorm_rope_quant.py" (torch_reference_fused)
+    rounds the normalised row to the storage dtype before rotating it, so a normalised value that
+    lands one storage ulp away -- which a different but equally valid fp32 order of the sum of
+    squares does by moving rstd an ulp -- moves y by up to one ulp of each rotation input. The bound
+    there is rel * (|y| + |lo * c| + |hi * s|) (one rounding of each input and of the output), still
+    far below the error of a wrong pair, sign or table row (of the order of the inputs themselves).
+    `normed` is the oracle's normalised row (rmsnorm_fwd: x * rstd * w rounded to the dtype).
+    """
+    rel, abs_ = storage_tol(ref.dtype)
+    a = gpu.detach().cpu().double()
+    b = ref.double()
+    M, N = b.shape
+    R = 2 * cos.shape[-1]
+    spread = torch.zeros_like(b)
+    if R > 0:
+        n = normed.double()
+        lo, hi = n[:, N - R:N - R // 2], n[:, N - R // 2:]
+        c, s = cos.double(), sin.double()
+        spread[:, N - R:N - R // 2] = (lo * c).abs() + (hi * s).abs()
+        spread[:, N - R // 2:] = (hi * c).abs() + (lo * s).abs()
+    err = (a - b).abs()
+    bound = torch.clamp((b.abs() + spread) * rel, min=abs_)
     bad = err > bound
     assert not bool(bad.any()), (
         f"{what}: {int(bad.sum())} of {bad.numel()} elements outside the tolerance; worst err "

@@ -13,7 +13,8 @@ import torch
 
 import fp8_quant_memory_gb300 as fq
 from fp8_quant_memory_gb300 import workloads as wl
-from parity import (assert_codes_close, assert_dw_close, assert_scale_close, assert_storage_close,
+from parity import (assert_codes_close, assert_dw_close, assert_rope_close, assert_scale_close,
+                    assert_storage_close,
                     assert_within_one_ulp)
 
 pytestmark = pytest.mark.gpu
@@ -80,7 +81,8 @@ def test_rope_fp16_64k_full(orc, cuda_ok):
     g = _cuda(d)
     y = fq.rmsnorm_rope(g["x"], g["w"], g["cos"], g["sin"])
     torch.cuda.synchronize()
-    assert_storage_close(y, orc.rmsnorm_rope(d["x"], d["w"], d["cos"], d["sin"]))
+    assert_rope_close(y, orc.rmsnorm_rope(d["x"], d["w"], d["cos"], d["sin"]), orc.rmsnorm_fwd(d["x"], d["w"]),
+                      d["cos"], d["sin"])
 
 
 def test_rope_quant_tiny_full(orc, cuda_ok):
@@ -88,7 +90,7 @@ def test_rope_quant_tiny_full(orc, cuda_ok):
     g = _cuda(d)
     y, q, s = fq.rmsnorm_rope_quant(g["x"], g["w"], g["cos"], g["sin"])
     y_ref, q_ref, s_ref = orc.rmsnorm_rope_quant(d["x"], d["w"], d["cos"], d["sin"])
-    assert_storage_close(y, y_ref)
+    assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
     q_own, s_own = orc.quant_rows(y.cpu())
     assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
     assert_codes_close(q, q_ref)

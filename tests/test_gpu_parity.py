@@ -8,8 +8,8 @@ import torch
 
 import fp8_quant_memory_gb300 as fq
 from fp8_quant_memory_gb300 import workloads as wl
-from parity import (assert_codes_close, assert_dw_close, assert_scale_close, assert_storage_close,
-                    assert_within_one_ulp)
+from parity import (assert_codes_close, assert_dw_close, assert_rope_close, assert_scale_close,
+                    assert_storage_close, assert_within_one_ulp)
 
 pytestmark = pytest.mark.gpu
 
@@ -128,7 +128,7 @@ def test_rmsnorm_rope_quant_parity(orc, cuda_ok, case, want_y):
     g = cuda(d)
     y, q, s = fq.rmsnorm_rope_quant(g["x"], g["w"], g["cos"], g["sin"], want_y=True)
     torch.cuda.synchronize()
-    assert_storage_close(y, y_ref)
+    assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
     # The codes and scales are the quantiser applied to the kernel's own y: exact.
     q_own, s_own = orc.quant_rows(y.cpu())
     assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
@@ -143,7 +143,7 @@ def test_rmsnorm_rope_quant_scalar_path_matches(orc, cuda_ok):
     y_ref, q_ref, _ = orc.rmsnorm_rope_quant(d["x"], d["w"], d["cos"], d["sin"])
     g = cuda(d)
     y, q, s = fq.rmsnorm_rope_quant(misalign(g["x"]), g["w"], g["cos"], g["sin"])
-    assert_storage_close(y, y_ref)
+    assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
     q_own, s_own = orc.quant_rows(y.cpu())
     assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
 
@@ -172,7 +172,7 @@ def test_rmsnorm_rope_quant_groups_parity(orc, cuda_ok, case):
     y, q, s = fq.rmsnorm_rope_quant_groups(g["x"], g["w"], g["cos"], g["sin"], gs)
     torch.cuda.synchronize()
     assert s.shape == (M, N // gs)
-    assert_storage_close(y, y_ref)
+    assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
     # codes and scales are the group-wise quantiser applied to the kernel's own y: exact
     q_own, s_own = orc.quant_groups(y.cpu(), gs)
     assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
@@ -196,9 +196,94 @@ def test_rmsnorm_rope_quant_groups_scalar_path_matches(orc, cuda_ok):
     y_ref, q_ref, _ = orc.rmsnorm_rope_quant_groups(d["x"], d["w"], d["cos"], d["sin"], 128)
     g = cuda(d)
     y, q, s = fq.rmsnorm_rope_quant_groups(misalign(g["x"]), g["w"], g["cos"], g["sin"], 128)
-    assert_storage_close(y, y_ref)
+    assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
     q_own, s_own = orc.quant_groups(y.cpu(), 128)
     assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
+
+
+# ----------------------------------------------------------------------------------- wide quantising rows
+WIDE_QUANT_CASES = [
+    # M, N, R, group_size (None: one scale per row), dtype, table, write y
+    (4096, 4096, 128, None, "bf16", "bf16", False),  # the Ch.13 ledger's fused workload
+    (4096, 4096, 128, 128, "bf16", "bf16", True),
+    (4099, 1024, 64, 8, "fp16", "fp32", True),        # 128 groups per row, ragged last stage
+    (4100, 2048, 0, None, "bf16", "bf16", True),      # no rotation
+    (4097, 1536, 256, 512, "bf16", "fp32", False),    # groups spanning head and tail
+]
+
+
+@pytest.mark.parametrize("kernel", ["tma", "generic"])
+@pytest.mark.parametrize("case", WIDE_QUANT_CASES, ids=lambda c: "M%d-N%d-R%d-g%s-%s-%s-y%d" % c)
+def test_wide_rows_quant_stream_kernel(orc, cuda_ok, monkeypatch, case, kernel):
+    """RMSNorm + RoPE + FP8 on >= 4096 rows of >= 1024 elements (the TMA-fed wide-row kernel, and the
+    generic kernel on the same inputs): y against the oracle, codes and scales exactly the quantiser
+    of the kernel's own y."""
+    _rows_kernel(monkeypatch, kernel)
+    M, N, R, gs, dt, tdt, want_y = case
+    d = wl.rows_inputs(M, N, R, dt, tdt, seed=970 + M)
+    g = cuda(d)
+    if gs is None:
+        y_ref, q_ref, _ = orc.rmsnorm_rope_quant(d["x"], d["w"], d["cos"], d["sin"])
+        y, q, sc = fq.rmsnorm_rope_quant(g["x"], g["w"], g["cos"], g["sin"], want_y=True)
+        q_own, s_own = orc.quant_rows(y.cpu())
+    else:
+        y_ref, q_ref, _ = orc.rmsnorm_rope_quant_groups(d["x"], d["w"], d["cos"], d["sin"], gs)
+        y, q, sc = fq.rmsnorm_rope_quant_groups(g["x"], g["w"], g["cos"], g["sin"], gs, want_y=True)
+        q_own, s_own = orc.quant_groups(y.cpu(), gs)
+    torch.cuda.synchronize()
+    assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
+    assert torch.equal(q.cpu(), q_own) and torch.equal(sc.cpu(), s_own)
+    assert_codes_close(q, q_ref)
+    if not want_y:
+        if gs is None:
+            _, q2, s2 = fq.rmsnorm_rope_quant(g["x"], g["w"], g["cos"], g["sin"], want_y=False)
+        else:
+            _, q2, s2 = fq.rmsnorm_rope_quant_groups(g["x"], g["w"], g["cos"], g["sin"], gs, want_y=False)
+        assert torch.equal(q2, q) and torch.equal(s2, sc)
+    assert fq.device_status(clear=True) == 0
+
+
+@pytest.mark.parametrize("path", ["vector", "wide_stream", "scalar", "groups", "prologue_tma", "prologue_generic"])
+def test_negative_zero_inputs_give_negative_zero_codes(orc, cuda_ok, monkeypatch, path):
+    """x = -0.0 normalises (and, with angle-free columns, quantises) to -0: the definition's y / scale
+    keeps the sign of zero and e4m3fn codes it 0x80. Planted -0.0 (and +0.0) entries on every path."""
+    monkeypatch.delenv("FQ_PROLOGUE_KERNEL", raising=False)
+    monkeypatch.delenv("FQ_ROWS_KERNEL", raising=False)
+    if path.startswith("prologue"):
+        if path == "prologue_generic":
+            monkeypatch.setenv("FQ_PROLOGUE_KERNEL", "generic")
+        d = wl.qk_inputs(64, 4, 2, 128, "bf16", "fp32", seed=995, std=1.0)
+        d["qk"][3, 1, 5] = -0.0
+        d["qk"][7, 4, 100] = -0.0
+        d["qk"][9, 0, 17] = 0.0
+        q_ref, s_ref = orc.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], 4, 2)
+        g = cuda(d)
+        q, s = fq.qk_norm_rope_quant(g["qk"], g["wq"], g["wk"], g["cos"], g["sin"], 4, 2)
+        torch.cuda.synchronize()
+        assert_codes_close(q, q_ref)
+        assert_scale_close(s, s_ref)
+        return
+    M, N, R = (4096, 1024, 64) if path == "wide_stream" else (64, 512, 64)
+    d = wl.rows_inputs(M, N, R, "bf16", "bf16", seed=996)
+    planted = [(1, 7), (2, 300), (5, 0), (M - 1, N - R - 1)]  # head columns: y = -0 exactly
+    for (i, j) in planted:
+        d["x"][i, j] = -0.0
+    d["x"][3, 11] = 0.0
+    g = cuda(d)
+    x = misalign(g["x"]) if path == "scalar" else g["x"]
+    if path == "groups":
+        y, q, s = fq.rmsnorm_rope_quant_groups(x, g["w"], g["cos"], g["sin"], 128)
+        q_own, s_own = orc.quant_groups(y.cpu(), 128)
+    else:
+        y, q, s = fq.rmsnorm_rope_quant(x, g["w"], g["cos"], g["sin"])
+        q_own, s_own = orc.quant_rows(y.cpu())
+    torch.cuda.synchronize()
+    qc = q.cpu()
+    for (i, j) in planted:
+        assert torch.signbit(y.cpu()[i, j]) and float(y.cpu()[i, j]) == 0.0
+        assert int(qc[i, j]) == 0x80
+    assert int(qc[3, 11]) == 0x00
+    assert torch.equal(qc, q_own) and torch.equal(s.cpu(), s_own)
 
 
 # ----------------------------------------------------------------------------------- rmsnorm_rope
@@ -211,7 +296,7 @@ def test_rmsnorm_rope_parity(orc, cuda_ok, case):
     y_ref = orc.rmsnorm_rope(d["x"], d["w"], d["cos"], d["sin"])
     g = cuda(d)
     y = fq.rmsnorm_rope(g["x"], g["w"], g["cos"], g["sin"])
-    assert_storage_close(y, y_ref)
+    assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
 
 
 # ----------------------------------------------------------------------------------- rmsnorm fwd
@@ -435,5 +520,6 @@ def test_rmsnorm_rope_stream_kernel(orc, cuda_ok, monkeypatch, case, kernel):
     d = wl.rows_inputs(M, N, R, dt, tdt, seed=950 + M, heads_per_token=hpt)
     g = cuda(d)
     y = fq.rmsnorm_rope(g["x"], g["w"], g["cos"], g["sin"])
-    assert_storage_close(y, orc.rmsnorm_rope(d["x"], d["w"], d["cos"], d["sin"]))
+    assert_rope_close(y, orc.rmsnorm_rope(d["x"], d["w"], d["cos"], d["sin"]),
+                      orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
     assert fq.device_status(clear=True) == 0
