@@ -41,6 +41,8 @@ _SIGS = {
     "or_qk_norm_rope_quant": [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                               _int, _int, _f32, _f32],
     "or_rmsnorm_bwd": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _f32],
+    "or_rmsnorm_bwd_rstd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int],
+    "or_rmsnorm_fwd_rstd": [_vp, _vp, _vp, _vp, _i64, _i64, _int, _f32],
     "or_rmsnorm_f64": [_vp, _vp, _vp, _i64, _i64, _f64],
     "or_rope_f64": [_vp, _vp, _vp, _i64, _i64, _i64],
     "or_rmsnorm_bwd_f64": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f64],
@@ -103,6 +105,15 @@ def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6) -> torch.Te
     y = torch.empty_like(x)
     _check(lib().or_rmsnorm_fwd(_p(x), _p(w), _p(y), M, N, _FMT[x.dtype], eps), "rmsnorm_fwd")
     return y
+
+
+def rmsnorm_fwd_rstd(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6):
+    """Forward that also returns each row's fp32 rstd: (y, rstd [M])."""
+    M, N = x.shape
+    y = torch.empty_like(x)
+    rstd = torch.empty((M,), dtype=torch.float32)
+    _check(lib().or_rmsnorm_fwd_rstd(_p(x), _p(w), _p(y), _p(rstd), M, N, _FMT[x.dtype], eps), "rmsnorm_fwd_rstd")
+    return y, rstd
 
 
 def rmsnorm_rope(x, w, cos, sin, eps: float = 1e-6) -> torch.Tensor:
@@ -195,6 +206,17 @@ def rmsnorm_bwd(x, w, g, eps: float = 1e-6):
     dw32 = torch.empty((N,), dtype=torch.float32)
     _check(lib().or_rmsnorm_bwd(_p(x), _p(w), _p(g), _p(dx), _p(dw), _p(dw32), M, N, _FMT[x.dtype], eps),
            "rmsnorm_bwd")
+    return dx, dw, dw32
+
+
+def rmsnorm_bwd_rstd(x, w, g, rstd):
+    """Backward with a saved rstd [M] fp32: (dx, dw, dw_f32)."""
+    M, N = x.shape
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(w)
+    dw32 = torch.empty((N,), dtype=torch.float32)
+    _check(lib().or_rmsnorm_bwd_rstd(_p(x), _p(w), _p(g), _p(rstd.contiguous()), _p(dx), _p(dw), _p(dw32), M, N,
+                                     _FMT[x.dtype]), "rmsnorm_bwd_rstd")
     return dx, dw, dw32
 
 

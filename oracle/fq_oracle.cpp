@@ -412,15 +412,17 @@ int or_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, 
 // ---- b2-b3: RMSNorm backward ("rmsnorm_tl.py", RMSNormTileLang.backward).
 // dx = dtype(rstd*(g*w - xn*mean(g*w*xn))), dw = dtype(sum_rows g*xn). dw_f32 (nullable) receives
 // the fp32 column sums before the final cast.
-int or_rmsnorm_bwd(const void* x, const void* w, const void* g, void* dx, void* dw, float* dw_f32,
-                   int64_t M, int64_t N, int dtype, float eps) {
+// Shared body of the backward: rstd recomputed from x (as the Ch.17 page does) or, when `rstd_in` is
+// given, the forward's saved rstd of each row.
+static int bwd_impl(const void* x, const void* w, const void* g, const float* rstd_in, void* dx, void* dw,
+                    float* dw_f32, int64_t M, int64_t N, int dtype, float eps) {
   if (!x || !w || !g || !dx || !dw || M < 0 || N <= 0 || !is_storage(dtype)) return OR_BAD_ARG;
   std::vector<float> wr(N), xr(N), xn(N), gw(N);
   std::vector<double> dw_acc(N, 0.0);
   for (int64_t j = 0; j < N; ++j) wr[j] = load_elem(dtype, w, j);
   for (int64_t i = 0; i < M; ++i) {
     for (int64_t j = 0; j < N; ++j) xr[j] = load_elem(dtype, x, i * N + j);
-    const float rstd = row_rstd(xr.data(), N, eps);
+    const float rstd = rstd_in ? rstd_in[i] : row_rstd(xr.data(), N, eps);
     double tsum = 0.0;
     for (int64_t j = 0; j < N; ++j) {
       const float gj = load_elem(dtype, g, i * N + j);
@@ -440,6 +442,33 @@ int or_rmsnorm_bwd(const void* x, const void* w, const void* g, void* dx, void* 
     const float s = static_cast<float>(dw_acc[j]);
     if (dw_f32) dw_f32[j] = s;
     store_elem(dtype, dw, j, s);
+  }
+  return OR_OK;
+}
+
+int or_rmsnorm_bwd(const void* x, const void* w, const void* g, void* dx, void* dw, float* dw_f32,
+                   int64_t M, int64_t N, int dtype, float eps) {
+  return bwd_impl(x, w, g, nullptr, dx, dw, dw_f32, M, N, dtype, eps);
+}
+
+// ---- b2-b3 with the forward's rstd saved instead of recomputed (a trade of a 4-byte-per-row write
+// and read for the backward's sum of squares).
+int or_rmsnorm_bwd_rstd(const void* x, const void* w, const void* g, const float* rstd, void* dx, void* dw,
+                        float* dw_f32, int64_t M, int64_t N, int dtype) {
+  if (!rstd && M > 0) return OR_BAD_ARG;
+  return bwd_impl(x, w, g, rstd, dx, dw, dw_f32, M, N, dtype, 0.0f);
+}
+
+// ---- b1 that also returns each row's rstd = 1/sqrt(mean(x^2) + eps) (fp32), for the backward.
+int or_rmsnorm_fwd_rstd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N, int dtype,
+                        float eps) {
+  if (!x || !w || !y || !rstd || M < 0 || N <= 0 || !is_storage(dtype)) return OR_BAD_ARG;
+  std::vector<float> xr(N), wr(N);
+  for (int64_t j = 0; j < N; ++j) wr[j] = load_elem(dtype, w, j);
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) xr[j] = load_elem(dtype, x, i * N + j);
+    rstd[i] = row_rstd(xr.data(), N, eps);
+    for (int64_t j = 0; j < N; ++j) store_elem(dtype, y, i * N + j, (xr[j] * rstd[i]) * wr[j]);
   }
   return OR_OK;
 }

@@ -268,6 +268,51 @@ def test_quant_custom_fp8_max(orc):
     assert orc.decode(q[:, 3:]).item() == 240.0
 
 
+# --------------------------------------------------------------------------- saved rstd
+def test_worked_rstd(orc):
+    """[3, 4], eps = 0: mean(x^2) = 12.5, rstd = 1 / sqrt(12.5) = sqrt(2) / 5, rounded once to fp32."""
+    x = torch.tensor([[3.0, 4.0]]).to(BF16)
+    w = torch.ones(2, dtype=BF16)
+    y, rstd = orc.rmsnorm_fwd_rstd(x, w, eps=0.0)
+    assert rstd.item() == np.float32(np.sqrt(2.0) / 5.0)
+    assert torch.equal(y.view(torch.int16), orc.rmsnorm_fwd(x, w, eps=0.0).view(torch.int16))
+
+
+def test_fwd_rstd_is_the_forward_plus_its_rstd(orc):
+    d = wl.rmsnorm_inputs(37, 1024, "bf16", seed=41)
+    y, rstd = orc.rmsnorm_fwd_rstd(d["x"], d["w"])
+    assert torch.equal(y.view(torch.int16), orc.rmsnorm_fwd(d["x"], d["w"]).view(torch.int16))
+    ref = 1.0 / torch.sqrt(d["x"].double().pow(2).mean(1) + 1e-6)  # fp64 definition
+    assert ((rstd.double() - ref).abs() / ref).max() < 2.0 ** -22  # a few fp32 roundings
+
+
+def test_bwd_with_saved_rstd_equals_recompute(orc):
+    """Reusing the forward's rstd gives the recomputing backward bit for bit (same rstd, same order)."""
+    d = wl.rmsnorm_inputs(53, 512, "bf16", seed=42)
+    _, rstd = orc.rmsnorm_fwd_rstd(d["x"], d["w"])
+    a = orc.rmsnorm_bwd_rstd(d["x"], d["w"], d["g"], rstd)
+    b = orc.rmsnorm_bwd(d["x"], d["w"], d["g"])
+    for u, v in zip(a, b):
+        assert torch.equal(u.view(torch.int16) if u.dtype == BF16 else u, v.view(torch.int16) if v.dtype == BF16 else v)
+
+
+def test_bwd_rstd_is_used_not_recomputed(orc):
+    """The backward uses the rstd it is given: with twice the true rstd, dx and dw follow the
+    definition dx = rstd * (g*w - xn * mean(g*w*xn)), xn = x * rstd, evaluated in fp64 at that rstd
+    (a recomputed rstd would be off by a factor of two)."""
+    d = wl.rmsnorm_inputs(7, 64, "bf16", seed=43)
+    _, rstd = orc.rmsnorm_fwd_rstd(d["x"], d["w"], eps=0.0)
+    r2 = rstd * 2.0  # exact
+    dx, _, dw32 = orc.rmsnorm_bwd_rstd(d["x"], d["w"], d["g"], r2)
+    x, w, g = d["x"].double(), d["w"].double(), d["g"].double()
+    xn = x * r2.double()[:, None]
+    gw = g * w
+    c = (gw * xn).mean(1, keepdim=True)
+    dx64 = r2.double()[:, None] * (gw - xn * c)
+    assert ((dx.double() - dx64).abs() <= torch.clamp(dx64.abs() * 2.0 ** -7, min=1e-3)).all()
+    assert ((dw32.double() - (g * xn).sum(0)).abs() <= 1e-4 * (g * xn).abs().sum(0) + 1e-6).all()
+
+
 # --------------------------------------------------------------------------- group-wise scales
 def test_worked_quant_groups(orc):
     c = G["quant_groups"]
