@@ -234,6 +234,24 @@ class RmsnormBwdCase(Case):
         self.fq.rmsnorm_bwd(s["x"], s["w"], s["g"], workspace=s["ws"], want_dw_f32=False)
 
 
+class RmsnormBwdRstdCase(RmsnormBwdCase):
+    """The backward with the forward's saved rstd: reads 4 more bytes per row, skips the sum of squares."""
+
+    def __init__(self, dev, M=8192, N=4096, n_sets=2):
+        import torch
+
+        super().__init__(dev, M, N, n_sets)
+        self.name = f"rmsnorm_bwd_rstd M={M} N={N} bf16 (saved rstd, dx + deterministic dw)"
+        for s in self.sets:
+            s["rstd"] = self.fq.rmsnorm_fwd_rstd(s["x"], s["w"])[1]
+        torch.cuda.synchronize()
+        self._bytes += M * 4
+
+    def launch(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.fq.rmsnorm_bwd_rstd(s["x"], s["w"], s["g"], s["rstd"], workspace=s["ws"], want_dw_f32=False)
+
+
 class RopeCase(Case):
     def __init__(self, dev, M=65536, N=192, R=64, n_sets=8):
         import torch
@@ -520,6 +538,7 @@ def run_reference(args):
 SECONDARY = {
     "rmsnorm_fwd_8k_4k": lambda dev: RmsnormFwdCase(dev),
     "rmsnorm_bwd_8k_4k": lambda dev: RmsnormBwdCase(dev),
+    "rmsnorm_bwd_rstd_8k_4k": lambda dev: RmsnormBwdRstdCase(dev),
     "rope_fp16_64k": lambda dev: RopeCase(dev),
     "rope_quant_tiny": lambda dev: RopeQuantCase(dev, note=" (launch-bound)"),
     "rope_quant_groups_tiny": lambda dev: RopeQuantCase(dev, group_size=128, note=" (launch-bound)"),

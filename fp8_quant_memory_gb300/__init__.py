@@ -22,7 +22,7 @@ import torch
 
 from . import _capi
 
-__all__ = ["rmsnorm_fwd", "rmsnorm_rope", "rmsnorm_rope_quant", "rmsnorm_rope_quant_groups", "qk_norm_rope_quant",
+__all__ = ["rmsnorm_fwd", "rmsnorm_fwd_rstd", "rmsnorm_bwd_rstd", "rmsnorm_rope", "rmsnorm_rope_quant", "rmsnorm_rope_quant_groups", "qk_norm_rope_quant",
            "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_bytes", "rmsnorm", "RMSNormFunction", "device_status", "check_bounded_wait",
            "FqError"]
@@ -83,6 +83,19 @@ def rmsnorm_fwd(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, out: torch.
     y = torch.empty_like(x) if out is None else out
     _capi.call("fq_rmsnorm_fwd", _ptr(x), _ptr(w), _ptr(y), M, N, _dtype(name, x), eps, _stream(dev))
     return y
+
+
+def rmsnorm_fwd_rstd(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, out: torch.Tensor | None = None,
+                     rstd: torch.Tensor | None = None):
+    """rmsnorm_fwd that also returns each row's fp32 rstd (for rmsnorm_bwd_rstd): (y, rstd [M])."""
+    name = "rmsnorm_fwd_rstd"
+    dev = _need_cuda(name, x, w, out, rstd)
+    _contig(name, x=x, w=w, out=out, rstd=rstd)
+    M, N = x.shape
+    y = torch.empty_like(x) if out is None else out
+    rstd = torch.empty((M,), dtype=torch.float32, device=dev) if rstd is None else rstd
+    _capi.call("fq_rmsnorm_fwd_rstd", _ptr(x), _ptr(w), _ptr(y), _ptr(rstd), M, N, _dtype(name, x), eps, _stream(dev))
+    return y, rstd
 
 
 def rmsnorm_rope(x, w, cos, sin, eps: float = 1e-6, out: torch.Tensor | None = None):
@@ -192,6 +205,23 @@ def rmsnorm_bwd(x, w, grad_y, eps: float = 1e-6, workspace: torch.Tensor | None 
     return dx, dw, dw32
 
 
+def rmsnorm_bwd_rstd(x, w, grad_y, rstd, workspace: torch.Tensor | None = None, want_dw_f32: bool = True):
+    """RMSNorm backward with the forward's saved rstd [M] fp32. Returns (dx, dw, dw_f32 or None)."""
+    name = "rmsnorm_bwd_rstd"
+    dev = _need_cuda(name, x, w, grad_y, rstd, workspace)
+    _contig(name, x=x, w=w, grad_y=grad_y, rstd=rstd, workspace=workspace)
+    M, N = x.shape
+    dx = torch.empty_like(x)
+    dw = torch.empty_like(w)
+    dw32 = torch.empty((N,), dtype=torch.float32, device=dev) if want_dw_f32 else None
+    need = rmsnorm_bwd_workspace_bytes(M, N)
+    if workspace is None:
+        workspace = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    _capi.call("fq_rmsnorm_bwd_rstd", _ptr(x), _ptr(w), _ptr(grad_y), _ptr(rstd), _ptr(dx), _ptr(dw), _ptr(dw32),
+               _ptr(workspace), workspace.numel() * workspace.element_size(), M, N, _dtype(name, x), _stream(dev))
+    return dx, dw, dw32
+
+
 def device_status(clear: bool = True, device=None) -> int:
     """The device status word (bit 0: a pipelined kernel gave up on a bounded wait)."""
     word = ctypes.c_uint(0)
@@ -211,25 +241,34 @@ def check_bounded_wait(limit_ms: int = 50, device=None) -> int:
 
 class RMSNormFunction(torch.autograd.Function):
     """RMSNorm with both directions in libfq ("rmsnorm_tl.py" (Ch.17), RMSNormTileLang): the forward
-    saves x and w only; the backward recomputes rstd."""
+    saves x and w and the backward recomputes rstd, as the page does; with save_rstd the forward also
+    saves its fp32 rstd (4 bytes per row) and the backward reuses it."""
 
     @staticmethod
-    def forward(ctx, x, w, eps):
+    def forward(ctx, x, w, eps, save_rstd=False):
         shape = x.shape
         x2 = x.reshape(-1, shape[-1]).contiguous()
-        y = rmsnorm_fwd(x2, w.contiguous(), eps)
-        ctx.save_for_backward(x2, w)
+        if save_rstd:
+            y, rstd = rmsnorm_fwd_rstd(x2, w.contiguous(), eps)
+            ctx.save_for_backward(x2, w, rstd)
+        else:
+            y = rmsnorm_fwd(x2, w.contiguous(), eps)
+            ctx.save_for_backward(x2, w)
         ctx.eps = eps
         ctx.shape = shape
         return y.view(shape)
 
     @staticmethod
     def backward(ctx, gy):
-        x2, w = ctx.saved_tensors
+        saved = ctx.saved_tensors
+        x2, w = saved[0], saved[1]
         g2 = gy.reshape(-1, x2.shape[-1]).contiguous()
-        dx, dw, _ = rmsnorm_bwd(x2, w.contiguous(), g2, ctx.eps, want_dw_f32=False)
-        return dx.view(ctx.shape), dw, None
+        if len(saved) == 3:
+            dx, dw, _ = rmsnorm_bwd_rstd(x2, w.contiguous(), g2, saved[2], want_dw_f32=False)
+        else:
+            dx, dw, _ = rmsnorm_bwd(x2, w.contiguous(), g2, ctx.eps, want_dw_f32=False)
+        return dx.view(ctx.shape), dw, None, None
 
 
-def rmsnorm(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6) -> torch.Tensor:
-    return RMSNormFunction.apply(x, w, eps)
+def rmsnorm(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, save_rstd: bool = False) -> torch.Tensor:
+    return RMSNormFunction.apply(x, w, eps, save_rstd)

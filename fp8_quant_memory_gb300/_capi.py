@@ -23,6 +23,7 @@ SIGNATURES = {
     "fq_device_status": (_int, [ctypes.POINTER(ctypes.c_uint), _int, _vp]),
     "fq_check_bounded_wait": (_int, [ctypes.c_uint, _vp]),
     "fq_rmsnorm_fwd": (_int, [_vp, _vp, _vp, _i64, _i64, _int, _f32, _vp]),
+    "fq_rmsnorm_fwd_rstd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _int, _f32, _vp]),
     "fq_rmsnorm_rope": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _f32, _vp]),
     "fq_rmsnorm_rope_quant": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _f32,
                                      _f32, _vp]),
@@ -32,6 +33,7 @@ SIGNATURES = {
                                      _int, _int, _f32, _f32, _vp]),
     "fq_rmsnorm_bwd_workspace_bytes": (_sz, [_i64, _i64]),
     "fq_rmsnorm_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _int, _f32, _vp]),
+    "fq_rmsnorm_bwd_rstd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _int, _vp]),
     "fq_rmsnorm_bwd_noalloc": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _f32, _vp]),
 }
 

@@ -151,9 +151,9 @@ int fq_check_bounded_wait(unsigned int limit_ms, cudaStream_t stream) {
   return ok();
 }
 
-int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, int dtype, float eps,
-                   cudaStream_t stream) {
-  const char* fn = "fq_rmsnorm_fwd";
+int fq_rmsnorm_fwd_rstd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N, int dtype,
+                        float eps, cudaStream_t stream) {
+  const char* fn = rstd != nullptr ? "fq_rmsnorm_fwd_rstd" : "fq_rmsnorm_fwd";
   if (int rc = check_common(fn, dtype, eps)) return rc;
   if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
     return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
@@ -163,6 +163,7 @@ int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, 
   a.x = x;
   a.wq = a.wk = w;
   a.y = y;
+  a.rstd = rstd;
   a.rows = M;
   a.token_stride = N;
   a.H = a.Hq = 1;
@@ -171,6 +172,11 @@ int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, 
   a.eps = eps;
   a.fp8_max = 448.0f;
   return launch_rows(fn, a, fq::MODE_FWD, dtype, dtype, stream);
+}
+
+int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, int dtype, float eps,
+                   cudaStream_t stream) {
+  return fq_rmsnorm_fwd_rstd(x, w, y, nullptr, M, N, dtype, eps, stream);
 }
 
 int fq_rmsnorm_rope(const void* x, const void* w, const void* cos, const void* sin, void* y, int64_t M,
@@ -303,10 +309,13 @@ size_t fq_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N) {
   return fq::bwd_workspace_bytes(M, N);
 }
 
-int fq_rmsnorm_bwd(const void* x, const void* w, const void* grad_y, void* dx, void* dw, float* dw_f32,
-                   void* workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype, float eps,
-                   cudaStream_t stream) {
-  const char* fn = "fq_rmsnorm_bwd";
+}  // extern "C"
+
+namespace {
+
+int rmsnorm_bwd(const char* fn, const void* x, const void* w, const void* grad_y, const float* rstd, void* dx,
+                void* dw, float* dw_f32, void* workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype,
+                float eps, cudaStream_t stream) {
   if (int rc = check_common(fn, dtype, eps)) return rc;
   if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
     return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
@@ -326,11 +335,32 @@ int fq_rmsnorm_bwd(const void* x, const void* w, const void* grad_y, void* dx, v
   a.dw = dw;
   a.dw_f32 = dw_f32;
   a.partial = static_cast<float*>(workspace);
+  a.rstd_in = rstd;
   a.M = M;
   a.N = static_cast<int32_t>(N);
   a.eps = eps;
   fq::launch_bwd(a, dtype, stream);
   return check_launch(fn);
 }
+
+}  // namespace
+
+extern "C" {
+
+int fq_rmsnorm_bwd(const void* x, const void* w, const void* grad_y, void* dx, void* dw, float* dw_f32,
+                   void* workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype, float eps,
+                   cudaStream_t stream) {
+  return rmsnorm_bwd("fq_rmsnorm_bwd", x, w, grad_y, nullptr, dx, dw, dw_f32, workspace, workspace_bytes, M, N, dtype,
+                     eps, stream);
+}
+
+int fq_rmsnorm_bwd_rstd(const void* x, const void* w, const void* grad_y, const float* rstd, void* dx, void* dw,
+                        float* dw_f32, void* workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype,
+                        cudaStream_t stream) {
+  if (rstd == nullptr && M > 0) return fail(FQ_ERR_INVALID_ARG, "fq_rmsnorm_bwd_rstd: rstd is null");
+  return rmsnorm_bwd("fq_rmsnorm_bwd_rstd", x, w, grad_y, rstd, dx, dw, dw_f32, workspace, workspace_bytes, M, N,
+                     dtype, 0.0f, stream);
+}
+
 
 }  // extern "C"

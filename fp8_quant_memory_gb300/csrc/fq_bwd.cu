@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_stage1_kernel(const BwdArgs a
     }
 #pragma unroll
     for (int b = 0; b < RB; ++b) {
-      const float rstd = rstd_from_ss(ss[b], fN, a.eps);
+      const float rstd = (a.rstd_in != nullptr) ? (rv[b] ? a.rstd_in[row[b]] : 1.f) : rstd_from_ss(ss[b], fN, a.eps);
       const float c = __fdiv_rn(__fmul_rn(sg[b], rstd), fN);
       const float2 rstd2 = splat2(rstd), c2 = splat2(c);
 #pragma unroll
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) bwd_stage1_scalar_kernel(const BwdAr
       sg += red[w][1];
     }
     __syncthreads();
-    const float rstd = rstd_from_ss(ss, static_cast<float>(N), a.eps);
+    const float rstd = (a.rstd_in != nullptr) ? a.rstd_in[r] : rstd_from_ss(ss, static_cast<float>(N), a.eps);
     const float c = __fdiv_rn(__fmul_rn(sg, rstd), static_cast<float>(N));
     for (int j = tid; j < N; j += kThreads) {
       const float gf = Elem<T>::load1(a.g, r * N + j);
@@ -324,7 +324,8 @@ __device__ __forceinline__ bool consumers_all(bool v) {
   return r != 0;
 }
 
-template <typename T, int VPT>
+// SAVED: rstd comes from the forward (a.rstd_in); the sum of squares is skipped.
+template <typename T, int VPT, bool SAVED>
 __global__ void __launch_bounds__(kStreamThreads, 2) bwd_stage1_stream_kernel(const BwdStream p) {
   extern __shared__ unsigned char smem_raw[];
   const BwdArgs& a = p.a;
@@ -433,10 +434,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) bwd_stage1_stream_kernel(co
       for (int e = 0; e < 4; ++e) {
         const float2 xf = Elem<T>::unpack(word(xv[q], e));
         const float2 gw = mul2(Elem<T>::unpack(word(gv[q], e)), wf[q][e]);
-        s2 = fma2(xf, xf, s2);
+        if (!SAVED) s2 = fma2(xf, xf, s2);
         g2 = fma2(gw, xf, g2);
       }
-    const float ss_w = group_sum<32>(s2.x + s2.y);
+    const float ss_w = SAVED ? 0.f : group_sum<32>(s2.x + s2.y);
     const float sg_w = group_sum<32>(g2.x + g2.y);
     float* rb = red + (k & 1) * (2 * kStreamWarps);
     if (lane == 0) {
@@ -450,7 +451,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) bwd_stage1_stream_kernel(co
       ss += rb[2 * w];
       sg += rb[2 * w + 1];
     }
-    const float rstd = rstd_from_ss(ss, fN, a.eps);
+    const float rstd = SAVED ? a.rstd_in[c0 + k] : rstd_from_ss(ss, fN, a.eps);
     const float c = __fdiv_rn(__fmul_rn(sg, rstd), fN);
     const float2 rstd2 = splat2(rstd), c2 = splat2(c);
     T* dxrow = static_cast<T*>(a.dx) + (c0 + k) * N;
@@ -482,8 +483,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) bwd_stage1_stream_kernel(co
   }
 }
 
-template <typename T, int VPT>
-bool launch_stage1_stream(const BwdArgs& a, const BwdPlan& plan, cudaStream_t s) {
+template <typename T, int VPT, bool SAVED>
+bool launch_stage1_stream_t(const BwdArgs& a, const BwdPlan& plan, cudaStream_t s) {
   BwdStream p{};
   p.a = a;
   p.rows_per_chunk = plan.rows_per_chunk;
@@ -497,7 +498,7 @@ bool launch_stage1_stream(const BwdArgs& a, const BwdPlan& plan, cudaStream_t s)
   if (p.depth < 2) p.depth = 2;
   if (p.depth > p.stages) p.depth = p.stages;
   const size_t smem = stream_smem_bytes(p.stages, p.stage_bytes);
-  auto kern = bwd_stage1_stream_kernel<T, VPT>;
+  auto kern = bwd_stage1_stream_kernel<T, VPT, SAVED>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
     return false;
   cudaLaunchConfig_t cfg{};
@@ -511,6 +512,12 @@ bool launch_stage1_stream(const BwdArgs& a, const BwdPlan& plan, cudaStream_t s)
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess;
+}
+
+template <typename T, int VPT>
+bool launch_stage1_stream(const BwdArgs& a, const BwdPlan& plan, cudaStream_t s) {
+  return a.rstd_in != nullptr ? launch_stage1_stream_t<T, VPT, true>(a, plan, s)
+                              : launch_stage1_stream_t<T, VPT, false>(a, plan, s);
 }
 
 template <typename T, int TPR, int VPT, int RB>

@@ -36,6 +36,7 @@ struct RowArgs {
   float eps;
   float fp8_max;
   int32_t group;  // MODE_ROPE_QUANT: columns per fp32 scale, scale[r * (N / group) + g]; 0: one per row
+  float* rstd;    // MODE_FWD: each row's rstd (fp32) written here when not null
 };
 
 // Group-wise scales on the vectorised path: group % 8 == 0 and at most this many groups per row.
@@ -73,6 +74,7 @@ struct BwdArgs {
   void* dw;
   float* dw_f32;  // nullable
   float* partial;  // [chunks, N] fp32 workspace
+  const float* rstd_in;  // nullable: each row's saved rstd (used instead of recomputing it)
   int64_t M;
   int32_t N;
   float eps;

@@ -110,6 +110,7 @@ __global__ void __launch_bounds__(kThreads) rows_wide_fwd_kernel(const RowArgs a
     }
     const float2 acc = add2(acc0, acc1);
     const float rstd = rstd_from_ss(group_sum<32>(acc.x + acc.y), fN, a.eps);
+    if (a.rstd != nullptr && lane == 0) a.rstd[r] = rstd;
     const float2 rstd2 = splat2(rstd);
     T* yrow = static_cast<T*>(a.y) + static_cast<int64_t>(r) * N;
     for (int v0 = lane; v0 < nv; v0 += 32 * kBatch2) {

@@ -312,7 +312,9 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_fwd_kernel(const S
       for (; v < nv; v += 32) acc[0] = sq_acc<T>(xs[v], acc[0]);
       const float2 s01 = add2(acc[0], acc[1]), s23 = add2(acc[2], acc[3]);
       const float2 sum = add2(s01, s23);
-      const float2 rstd2 = splat2(rstd_from_ss(group_sum<32>(sum.x + sum.y), fN, a.eps));
+      const float rstd = rstd_from_ss(group_sum<32>(sum.x + sum.y), fN, a.eps);
+      if (a.rstd != nullptr && lane == 0) a.rstd[r] = rstd;
+      const float2 rstd2 = splat2(rstd);
       uint4* yrow = reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N);
       v = lane;
       for (; v + 32 * (U - 1) < nv; v += 32 * U) {

@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(kThreads)
     }
     ss = group_sum<32>(ss);
     c.rstd = rstd_from_ss(ss, static_cast<float>(a.N), a.eps);
+    if (mode == MODE_FWD && a.rstd != nullptr && lane == 0) a.rstd[r] = c.rstd;
 
     if (mode != MODE_QK && a.y != nullptr)
       for (int j = lane; j < a.N; j += 32) {

@@ -82,6 +82,15 @@ int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, 
                    cudaStream_t stream);
 
 /*
+ * RMSNorm forward that also saves each row's rstd for the backward (the alternative to the Ch.17
+ * page's RMSNormTileLang, which saves only x and w and recomputes rstd in backward):
+ *   y as fq_rmsnorm_fwd;  rstd[i] = 1 / sqrt(sum_j x_ij^2 / N + eps)   (fp32, [M])
+ * rstd may be null (then this is fq_rmsnorm_fwd). Other arguments and errors as fq_rmsnorm_fwd.
+ */
+int fq_rmsnorm_fwd_rstd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N, int dtype,
+                        float eps, cudaStream_t stream);
+
+/*
  * RMSNorm + NeoX partial RoPE ("rmsnorm_rope_quant.py", rms_norm_rope_fused and the first two
  * steps of torch_reference_fused):
  *   normed_ij = dtype((x_ij * rstd_i) * w_j)
@@ -162,6 +171,17 @@ size_t fq_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N);
 int fq_rmsnorm_bwd(const void* x, const void* w, const void* grad_y, void* dx, void* dw, float* dw_f32,
                    void* workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype, float eps,
                    cudaStream_t stream);
+
+/*
+ * RMSNorm backward with the forward's saved rstd ("rmsnorm_tl.py", RMSNormTileLang.backward, with
+ * rstd taken from fq_rmsnorm_fwd_rstd instead of recomputed from x): the same dx and dw formulas and
+ * the same deterministic two-stage dw, with rstd[i] ([M] fp32, device, not null when M > 0) used for
+ * row i; the sum of squares of x is not computed (x is still read for xn = x * rstd). No eps argument:
+ * it is inside the saved rstd. Other arguments and errors as fq_rmsnorm_bwd.
+ */
+int fq_rmsnorm_bwd_rstd(const void* x, const void* w, const void* grad_y, const float* rstd, void* dx, void* dw,
+                        float* dw_f32, void* workspace, size_t workspace_bytes, int64_t M, int64_t N, int dtype,
+                        cudaStream_t stream);
 
 /* Size of the library's built-in scratch used by fq_rmsnorm_bwd_noalloc (4 MiB of device memory per
  * GPU that loads the library). It fits fq_rmsnorm_bwd_workspace_bytes(M, N) for N <= 4096 at any M,

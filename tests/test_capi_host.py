@@ -98,6 +98,14 @@ def test_shape_rules_rejected(lib):
                1e-6, 448.0, NULL)[0] == 1
 
 
+def test_saved_rstd_rules(lib):
+    p = ctypes.c_void_p(16)
+    rc, msg = _rc(lib, "fq_rmsnorm_bwd_rstd", p, p, p, NULL, p, p, NULL, p, 1 << 20, 8, 64, 0, NULL)
+    assert rc == 1 and "rstd" in msg
+    assert _rc(lib, "fq_rmsnorm_fwd_rstd", p, p, NULL, p, 4, 8, 0, 1e-6, NULL)[0] == 1  # null y
+    assert _rc(lib, "fq_rmsnorm_fwd_rstd", p, p, p, NULL, 0, 8, 0, 1e-6, NULL)[0] == 0  # empty
+
+
 def test_group_size_rules_rejected(lib):
     """Group-wise scales: group_size must be >= 1 and divide N; checked on the host."""
     p = ctypes.c_void_p(16)

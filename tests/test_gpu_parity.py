@@ -366,6 +366,59 @@ def test_rmsnorm_bwd_stream_matches_generic_bitwise(cuda_ok, monkeypatch):
         assert torch.equal(u, v)
 
 
+# saved rstd: shapes that reach every forward kernel (generic narrow and wide, TMA narrow and wide,
+# scalar) and every backward stage 1 (TMA-fed, global-load, scalar)
+RSTD_CASES = [
+    # M, N, dtype, misalign
+    (300, 256, "bf16", False),     # generic narrow rows
+    (129, 2048, "fp16", False),    # generic wide rows
+    (4100, 512, "bf16", False),    # TMA narrow rows
+    (4097, 4096, "bf16", False),   # TMA wide rows; TMA-fed backward
+    (77, 1024, "bf16", False),     # global-load backward
+    (45, 100, "bf16", False),      # odd width: scalar forward and backward
+    (60, 512, "bf16", True),       # misaligned: scalar
+]
+
+
+@pytest.mark.parametrize("case", RSTD_CASES, ids=lambda c: "M%d-N%d-%s-mis%d" % c)
+def test_rmsnorm_saved_rstd(orc, cuda_ok, case):
+    M, N, dt, mis = case
+    d = wl.rmsnorm_inputs(M, N, dt, seed=700 + M)
+    y_ref, r_ref = orc.rmsnorm_fwd_rstd(d["x"], d["w"])
+    g = cuda(d)
+    x = misalign(g["x"]) if mis else g["x"]
+    y, rstd = fq.rmsnorm_fwd_rstd(x, g["w"])
+    torch.cuda.synchronize()
+    assert_storage_close(y, y_ref)
+    rel = ((rstd.cpu().double() - r_ref.double()).abs() / r_ref.double()).max().item()
+    assert rel <= 1e-6, rel  # rstd differs from the oracle's only by the fp32 order of the sum of squares
+    assert torch.equal(y, fq.rmsnorm_fwd(x, g["w"]))  # the rstd output does not change y
+    # backward with the saved rstd: against the oracle given the same rstd, and against the recomputing one
+    dx, dw, dw32 = fq.rmsnorm_bwd_rstd(x, g["w"], g["g"], rstd)
+    dx_o, dw_o, dw32_o = orc.rmsnorm_bwd_rstd(d["x"], d["w"], d["g"], rstd.cpu())
+    assert_storage_close(dx, dx_o, "dx")
+    assert_dw_close(dw32, dw32_o)
+    assert_within_one_ulp(dw, dw_o)
+    dx_r, _, dw32_r = orc.rmsnorm_bwd(d["x"], d["w"], d["g"])
+    assert_storage_close(dx, dx_r, "dx")
+    assert_dw_close(dw32, dw32_r)
+    assert fq.device_status(clear=True) == 0
+
+
+def test_rmsnorm_autograd_save_rstd(cuda_ok):
+    d = cuda(wl.rmsnorm_inputs(96, 1024, "bf16", seed=710))
+    grads = []
+    for save in (False, True):
+        x = d["x"].clone().requires_grad_(True)
+        w = d["w"].clone().requires_grad_(True)
+        y = fq.rmsnorm(x, w, save_rstd=save)
+        (y.float() * d["g"].float()).sum().backward()
+        grads.append((y.detach(), x.grad, w.grad))
+    assert torch.equal(grads[0][0], grads[1][0])
+    assert_storage_close(grads[1][1], grads[0][1].cpu(), "dx")
+    assert_storage_close(grads[1][2], grads[0][2].cpu(), "dw")
+
+
 def test_rmsnorm_bwd_deterministic(cuda_ok):
     d = cuda(wl.rmsnorm_inputs(1000, 4096, "bf16", seed=550))
     a = fq.rmsnorm_bwd(d["x"], d["w"], d["g"])
