@@ -44,6 +44,8 @@ _SIGS = {
     "or_rmsnorm_bwd_rstd": [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int],
     "or_rmsnorm_fwd_rstd": [_vp, _vp, _vp, _vp, _i64, _i64, _int, _f32],
     "or_rmsnorm_f64": [_vp, _vp, _vp, _i64, _i64, _f64],
+    "or_layernorm_fwd": [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _f32],
+    "or_layernorm_f64": [_vp, _vp, _vp, _vp, _i64, _i64, _f64],
     "or_rope_f64": [_vp, _vp, _vp, _i64, _i64, _i64],
     "or_rmsnorm_bwd_f64": [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _f64],
 }
@@ -220,7 +222,28 @@ def rmsnorm_bwd_rstd(x, w, g, rstd):
     return dx, dw, dw32
 
 
+def layernorm_fwd(x, g, b=None, eps: float = 1e-5):
+    """LayerNorm forward: returns (y, mean fp32 [M], rstd fp32 [M])."""
+    M, N = x.shape
+    y = torch.empty_like(x)
+    mean = torch.empty((M,), dtype=torch.float32)
+    rstd = torch.empty((M,), dtype=torch.float32)
+    _check(lib().or_layernorm_fwd(_p(x), _p(g), _p(b), _p(y), _p(mean), _p(rstd), M, N, _FMT[x.dtype], eps),
+           "layernorm_fwd")
+    return y, mean, rstd
+
+
 # ------------------------------------------------------------------ fp64 twins (pins only)
+def layernorm_f64(x, g, b, eps: float):
+    x = x.double().contiguous()
+    M, N = x.shape
+    y = torch.empty_like(x)
+    gg = g.double().contiguous()
+    bb = None if b is None else b.double().contiguous()
+    _check(lib().or_layernorm_f64(_p(x), _p(gg), _p(bb), _p(y), M, N, eps), "layernorm_f64")
+    return y
+
+
 def rmsnorm_f64(x, w, eps: float):
     x = x.to(torch.float64).contiguous()
     w = w.to(torch.float64).contiguous()

@@ -34,6 +34,12 @@
  *   - dw is the fp64-accumulated column sum of the fp32 products g*xn, rounded once to fp32 and
  *     then to the storage dtype.
  *
+ *   - LayerNorm ("ledger.py", Ch.13 ledger, layer_norm: y = (x - mean) / sqrt(var + eps) * g + b, one
+ *     fused kernel reading x, g, b and writing y): the page gives the formula only; this follows the
+ *     RMSNorm conventions above -- the row's mean and variance (mean of (x - mean)^2) from exact
+ *     fp64 sums rounded once to fp32, rstd = 1/sqrt(var + eps) in fp32, then
+ *     y = dtype(((x - mean) * rstd) * g + b) with every fp32 step rounded.
+ *
  * Build: g++ -O2 -std=c++17 -ffp-contract=off -fno-fast-math -fPIC -shared (oracle/build.py).
  * -ffp-contract=off matters: every a*b+c below is two roundings, as in the fp32 tensor ops of the
  * pages' reference code.
@@ -372,6 +378,36 @@ int or_quant_groups(const void* y, uint8_t* q, float* scale, int64_t M, int64_t 
   return OR_OK;
 }
 
+// ---- LayerNorm forward ("ledger.py", Ch.13 ledger, layer_norm). b may be null (no bias). Also writes
+// each row's fp32 mean and rstd when those pointers are given.
+int or_layernorm_fwd(const void* x, const void* g, const void* b, void* y, float* mean_out, float* rstd_out,
+                     int64_t M, int64_t N, int dtype, float eps) {
+  if (!x || !g || !y || M < 0 || N <= 0 || !is_storage(dtype)) return OR_BAD_ARG;
+  std::vector<float> xr(N), gr(N), br(N, 0.0f);
+  for (int64_t j = 0; j < N; ++j) {
+    gr[j] = load_elem(dtype, g, j);
+    if (b) br[j] = load_elem(dtype, b, j);
+  }
+  for (int64_t i = 0; i < M; ++i) {
+    for (int64_t j = 0; j < N; ++j) xr[j] = load_elem(dtype, x, i * N + j);
+    double s = 0.0;
+    for (int64_t j = 0; j < N; ++j) s += static_cast<double>(xr[j]);
+    const double mean64 = s / static_cast<double>(N);
+    double v = 0.0;
+    for (int64_t j = 0; j < N; ++j) v += (static_cast<double>(xr[j]) - mean64) * (static_cast<double>(xr[j]) - mean64);
+    const float mean = static_cast<float>(mean64);
+    const float var = static_cast<float>(v / static_cast<double>(N));
+    const float rstd = 1.0f / std::sqrt(var + eps);
+    if (mean_out) mean_out[i] = mean;
+    if (rstd_out) rstd_out[i] = rstd;
+    for (int64_t j = 0; j < N; ++j) {
+      const float c = xr[j] - mean;
+      store_elem(dtype, y, i * N + j, ((c * rstd) * gr[j]) + br[j]);
+    }
+  }
+  return OR_OK;
+}
+
 // ---- The QK-Norm + RoPE + FP8 prologue ("case_norm_rope_quant.py", module docstring).
 // qk: [T, token_stride] storage elements; row (t, h) starts at t*token_stride + h*D, h < Hq+Hk.
 // Heads [0, Hq) use wq, heads [Hq, Hq+Hk) use wk. cos/sin: [T, R/2], one row per token.
@@ -475,6 +511,22 @@ int or_rmsnorm_fwd_rstd(const void* x, const void* w, void* y, float* rstd, int6
 
 // ---- fp64 twins of the same definitions: used only to pin the fp32 oracle (invariants that are
 // exact in real arithmetic, central finite differences for the backward).
+int or_layernorm_f64(const double* x, const double* g, const double* b, double* y, int64_t M, int64_t N,
+                     double eps) {
+  if (!x || !g || !y || M < 0 || N <= 0) return OR_BAD_ARG;
+  for (int64_t i = 0; i < M; ++i) {
+    const double* xr = x + i * N;
+    double s = 0.0;
+    for (int64_t j = 0; j < N; ++j) s += xr[j];
+    const double mean = s / static_cast<double>(N);
+    double v = 0.0;
+    for (int64_t j = 0; j < N; ++j) v += (xr[j] - mean) * (xr[j] - mean);
+    const double rstd = 1.0 / std::sqrt(v / static_cast<double>(N) + eps);
+    for (int64_t j = 0; j < N; ++j) y[i * N + j] = (xr[j] - mean) * rstd * g[j] + (b ? b[j] : 0.0);
+  }
+  return OR_OK;
+}
+
 int or_rmsnorm_f64(const double* x, const double* w, double* y, int64_t M, int64_t N, double eps) {
   if (!x || !w || !y || M < 0 || N <= 0) return OR_BAD_ARG;
   for (int64_t i = 0; i < M; ++i) {

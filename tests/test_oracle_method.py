@@ -268,6 +268,65 @@ def test_quant_custom_fp8_max(orc):
     assert orc.decode(q[:, 3:]).item() == 240.0
 
 
+# --------------------------------------------------------------------------- LayerNorm
+@pytest.mark.parametrize("case", ["layernorm_1_2_3_4", "layernorm_affine_index"])
+@pytest.mark.parametrize("dt", [BF16, FP16])
+def test_worked_layernorm(orc, case, dt):
+    c = G[case]
+    x = t(c["x"], dt)[None]
+    y, mean, rstd = orc.layernorm_fwd(x, t(c["g"], dt), t(c["b"], dt), eps=float(c["eps"]))
+    assert torch.equal(y.view(torch.int16), t(c["y"], dt)[None].view(torch.int16))
+    if "mean" in c:
+        assert mean.item() == np.float32(c["mean"]) and rstd.item() == np.float32(c["rstd"])
+
+
+def test_layernorm_shift_invariance_exact(orc):
+    """Adding a constant to a row changes nothing: with small integers the shifted row, its mean and
+    every deviation are exact, so y is identical bit for bit."""
+    gen = torch.Generator().manual_seed(51)
+    x = torch.randint(-8, 9, (9, 64), generator=gen).to(BF16)
+    d = wl.rmsnorm_inputs(9, 64, "bf16", seed=51)
+    y1, _, _ = orc.layernorm_fwd(x, d["w"], d["w"])
+    y2, _, _ = orc.layernorm_fwd((x.float() + 16).to(BF16), d["w"], d["w"])
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_layernorm_power_of_two_scale_invariance_exact(orc):
+    d = wl.rmsnorm_inputs(7, 256, "bf16", seed=52)
+    y1, _, _ = orc.layernorm_fwd(d["x"], d["w"], None, eps=0.0)
+    y2, _, _ = orc.layernorm_fwd((d["x"].float() * 8).to(BF16), d["w"], None, eps=0.0)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_layernorm_f64_zero_mean_unit_variance(orc):
+    x = torch.randn(5, 300, generator=torch.Generator().manual_seed(53), dtype=torch.float64) * 3 + 7
+    y = orc.layernorm_f64(x, torch.ones(300, dtype=torch.float64), None, 0.0)
+    assert y.mean(1).abs().max() < 1e-12
+    assert (y.pow(2).mean(1) - 1).abs().max() < 1e-12
+
+
+def test_layernorm_fp32_oracle_within_one_rounding_of_fp64(orc):
+    d = wl.rmsnorm_inputs(33, 1024, "bf16", seed=54)
+    b = (d["w"].float() - 1).to(BF16)
+    y, _, _ = orc.layernorm_fwd(d["x"], d["w"], b)
+    y64 = orc.layernorm_f64(d["x"].double(), d["w"].double(), b.double(), 1e-5)
+    err = (y.double() - y64).abs()
+    assert (err <= y64.abs() * 2.0 ** -8 * 1.01 + 1e-6).all()  # one bf16 rounding (plus fp32 noise)
+
+
+def test_layernorm_of_a_zero_mean_row_is_rmsnorm(orc):
+    """A row whose mean is exactly 0 has var = mean(x^2): LayerNorm without bias is RMSNorm (the two
+    round the statistic at slightly different points, so: within one storage rounding)."""
+    x = torch.randn(6, 128, generator=torch.Generator().manual_seed(55))
+    x = torch.cat([x, -x], 1).to(BF16)  # exact zero mean
+    w = wl.rmsnorm_inputs(1, 256, "bf16", seed=55)["w"]
+    y_ln, mean, _ = orc.layernorm_fwd(x, w, None, eps=1e-6)
+    assert (mean == 0).all()
+    y_rms = orc.rmsnorm_fwd(x, w, eps=1e-6)
+    err = (y_ln.double() - y_rms.double()).abs()
+    assert (err <= y_rms.double().abs() * 2.0 ** -7).all()
+
+
 # --------------------------------------------------------------------------- saved rstd
 def test_worked_rstd(orc):
     """[3, 4], eps = 0: mean(x^2) = 12.5, rstd = 1 / sqrt(12.5) = sqrt(2) / 5, rounded once to fp32."""
