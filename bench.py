@@ -252,6 +252,32 @@ class RmsnormBwdRstdCase(RmsnormBwdCase):
         self.fq.rmsnorm_bwd_rstd(s["x"], s["w"], s["g"], s["rstd"], workspace=s["ws"], want_dw_f32=False)
 
 
+class LayerNormCase(Case):
+    """LayerNorm forward with bias at the Ch.13 ledger's shape (4096 x 4096)."""
+
+    def __init__(self, dev, M=4096, N=4096, n_sets=8):
+        import torch
+
+        import fp8_quant_memory_gb300 as fq
+        from fp8_quant_memory_gb300 import workloads as wl
+
+        self.fq = fq
+        self.name = f"layernorm_fwd M={M} N={N} bf16 (with bias)"
+        h = wl.rmsnorm_inputs(M, N, "bf16", seed=20261202 + 5)
+        h = {"x": h["x"], "g": h["w"], "b": (h["w"].float() - 1.0).to(torch.bfloat16)}
+        self.sets = _make_sets(h, n_sets, dev)
+        for s in self.sets:
+            s["y"] = torch.empty_like(s["x"])
+        self._bytes = 2 * M * N * 2 + 2 * N * 2
+
+    def bytes_per_step(self):
+        return self._bytes
+
+    def launch(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.fq.layernorm_fwd(s["x"], s["g"], s["b"], out=s["y"])
+
+
 class RopeCase(Case):
     def __init__(self, dev, M=65536, N=192, R=64, n_sets=8):
         import torch
@@ -540,6 +566,7 @@ SECONDARY = {
     "rmsnorm_bwd_8k_4k": lambda dev: RmsnormBwdCase(dev),
     "rmsnorm_bwd_rstd_8k_4k": lambda dev: RmsnormBwdRstdCase(dev),
     "rope_fp16_64k": lambda dev: RopeCase(dev),
+    "layernorm_4k_4k": lambda dev: LayerNormCase(dev),
     "rope_quant_tiny": lambda dev: RopeQuantCase(dev, note=" (launch-bound)"),
     "rope_quant_groups_tiny": lambda dev: RopeQuantCase(dev, group_size=128, note=" (launch-bound)"),
     "rope_quant_ledger_4k": lambda dev: RopeQuantCase(dev, M=4096, N=4096, R=128, write_y=False, n_sets=8,

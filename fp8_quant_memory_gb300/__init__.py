@@ -22,7 +22,7 @@ import torch
 
 from . import _capi
 
-__all__ = ["rmsnorm_fwd", "rmsnorm_fwd_rstd", "rmsnorm_bwd_rstd", "rmsnorm_rope", "rmsnorm_rope_quant", "rmsnorm_rope_quant_groups", "qk_norm_rope_quant",
+__all__ = ["layernorm_fwd", "rmsnorm_fwd", "rmsnorm_fwd_rstd", "rmsnorm_bwd_rstd", "rmsnorm_rope", "rmsnorm_rope_quant", "rmsnorm_rope_quant_groups", "qk_norm_rope_quant",
            "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_bytes", "rmsnorm", "RMSNormFunction", "device_status", "check_bounded_wait",
            "FqError"]
@@ -96,6 +96,19 @@ def rmsnorm_fwd_rstd(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, out: t
     rstd = torch.empty((M,), dtype=torch.float32, device=dev) if rstd is None else rstd
     _capi.call("fq_rmsnorm_fwd_rstd", _ptr(x), _ptr(w), _ptr(y), _ptr(rstd), M, N, _dtype(name, x), eps, _stream(dev))
     return y, rstd
+
+
+def layernorm_fwd(x: torch.Tensor, gamma: torch.Tensor, beta: torch.Tensor | None = None, eps: float = 1e-5,
+                  out: torch.Tensor | None = None):
+    """y = dtype(((x - mean) * rsqrt(var + eps)) * gamma + beta) over the last dim of a 2-D x."""
+    name = "layernorm_fwd"
+    dev = _need_cuda(name, x, gamma, beta, out)
+    _contig(name, x=x, gamma=gamma, beta=beta, out=out)
+    M, N = x.shape
+    y = torch.empty_like(x) if out is None else out
+    _capi.call("fq_layernorm_fwd", _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y), M, N, _dtype(name, x), eps,
+               _stream(dev))
+    return y
 
 
 def rmsnorm_rope(x, w, cos, sin, eps: float = 1e-6, out: torch.Tensor | None = None):

@@ -24,6 +24,7 @@ SIGNATURES = {
     "fq_check_bounded_wait": (_int, [ctypes.c_uint, _vp]),
     "fq_rmsnorm_fwd": (_int, [_vp, _vp, _vp, _i64, _i64, _int, _f32, _vp]),
     "fq_rmsnorm_fwd_rstd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _int, _f32, _vp]),
+    "fq_layernorm_fwd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _int, _f32, _vp]),
     "fq_rmsnorm_rope": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _f32, _vp]),
     "fq_rmsnorm_rope_quant": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _int, _f32,
                                      _f32, _vp]),

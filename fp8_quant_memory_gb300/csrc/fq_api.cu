@@ -174,6 +174,32 @@ int fq_rmsnorm_fwd_rstd(const void* x, const void* w, void* y, float* rstd, int6
   return launch_rows(fn, a, fq::MODE_FWD, dtype, dtype, stream);
 }
 
+int fq_layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, int64_t M, int64_t N, int dtype,
+                     float eps, cudaStream_t stream) {
+  const char* fn = "fq_layernorm_fwd";
+  if (int rc = check_common(fn, dtype, eps)) return rc;
+  if (M < 0 || N < 1 || M > kMaxRows || N > kMaxWidth)
+    return fail(FQ_ERR_INVALID_ARG, "%s: need 0 <= M <= 2^31-1 and 1 <= N <= 2^24", fn);
+  if (M == 0) return ok();
+  if (x == nullptr || gamma == nullptr || y == nullptr) return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
+  cudaGetLastError();
+  fq::RowArgs a{};
+  a.x = x;
+  a.wq = a.wk = gamma;
+  a.bias = beta;
+  a.y = y;
+  a.rows = M;
+  a.token_stride = N;
+  a.H = a.Hq = 1;
+  a.N = static_cast<int32_t>(N);
+  a.eps = eps;
+  a.fp8_max = 448.0f;
+  const bool vec = (N % 8 == 0) && aligned(x, 16) && aligned(gamma, 16) && aligned(y, 16) &&
+                   (beta == nullptr || aligned(beta, 16));
+  fq::launch_layernorm(a, dtype, vec, stream);
+  return check_launch(fn);
+}
+
 int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, int dtype, float eps,
                    cudaStream_t stream) {
   return fq_rmsnorm_fwd_rstd(x, w, y, nullptr, M, N, dtype, eps, stream);

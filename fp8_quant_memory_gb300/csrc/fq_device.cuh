@@ -138,6 +138,19 @@ __device__ __forceinline__ float2 sub2(float2 a, float2 b) {
   return d;
 }
 __device__ __forceinline__ float2 splat2(float a) { return make_float2(a, a); }
+// a + b per component as its own rounded instruction (inline PTX: never fused with a preceding
+// product into an FMA, which would round once where the definition rounds twice).
+__device__ __forceinline__ float2 add2_rn(float2 a, float2 b) {
+  float2 d;
+  asm volatile("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
 
 // Quotient y / s rounded to nearest, given r = RN(1/s) (correctly rounded reciprocal):
 // q0 = RN(y*r) is within one ulp of y/s, the residual y - q0*s is exact in one FMA, and

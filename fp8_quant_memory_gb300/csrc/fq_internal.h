@@ -37,6 +37,7 @@ struct RowArgs {
   float fp8_max;
   int32_t group;  // MODE_ROPE_QUANT: columns per fp32 scale, scale[r * (N / group) + g]; 0: one per row
   float* rstd;    // MODE_FWD: each row's rstd (fp32) written here when not null
+  const void* bias;  // LayerNorm: the per-column bias b (nullable); wq holds the gain g
 };
 
 // Group-wise scales on the vectorised path: group % 8 == 0 and at most this many groups per row.
@@ -54,6 +55,13 @@ bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStrea
 // TMA-fed row-stream kernels for MODE_FWD and MODE_ROPE over contiguous rows (>= 4096 rows, the
 // vectorised-path layout rules). Returns false (launching nothing) when they do not apply.
 bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s);
+
+// LayerNorm forward, y = dtype(((x - mean) * rstd) * g + b) (a.wq = g, a.bias = b or null): the TMA-fed
+// wide-row kernel (>= 4096 contiguous rows, N >= 1024, vector layout) or false.
+bool launch_layernorm_tma(const RowArgs& a, int dtype, cudaStream_t s);
+// Every other shape: a register-resident warp-per-row kernel (N % 8 == 0, aligned, N <= 4096) or the
+// scalar kernel.
+void launch_layernorm(const RowArgs& a, int dtype, bool vec, cudaStream_t s);
 
 // Scalar path: any N >= 1, even R, any alignment, any dtype combination.
 void launch_rows_scalar(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s);

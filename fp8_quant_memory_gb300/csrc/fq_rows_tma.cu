@@ -43,6 +43,7 @@ struct StreamArgs {
   int32_t tab_block;    // bytes of one table block
   int32_t depth;        // the producer keeps at most this many stages in flight
   int32_t w_bytes;      // bytes of the weight row staged once per CTA (0: none)
+  int32_t b_bytes;      // bytes of a second row (the LayerNorm bias) staged right after it (0: none)
 };
 
 constexpr int kReq = 2;  // cluster-launch-control requests a producer keeps in flight
@@ -56,8 +57,9 @@ __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem
   const RowArgs& a = p.a;
   const int S = p.stages;
   if (p.w_bytes > 0) {
-    mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(p.w_bytes));
+    mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(p.w_bytes + p.b_bytes));
     bulk_g2s(wsm, a.wq, static_cast<uint32_t>(p.w_bytes), wbar);
+    if (p.b_bytes > 0) bulk_g2s(wsm + p.w_bytes, a.bias, static_cast<uint32_t>(p.b_bytes), wbar);
   }
   const uint32_t xrow = static_cast<uint32_t>(a.N) * esize;
   const uint32_t trow = static_cast<uint32_t>(a.R / 2) * tsize;
@@ -512,6 +514,97 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_rope_kernel(const 
   }
 }
 
+// ------------------------------------------------------------------ wide rows, LayerNorm
+// LayerNorm forward ("ledger.py" (Ch.13 ledger), layer_norm) for rows of N >= 1024: four consumer
+// warps, one row per warp per stage, the gain and bias rows staged once per CTA. Three passes over
+// the staged row: the mean, the variance of the deviations (no E[x^2] - E[x]^2 cancellation), then
+// y = dtype(((x - mean) * rstd) * g + b) with each step rounded as the definition's fp32 ops.
+template <typename T>
+__global__ void __launch_bounds__(kWideThreads) rows_tma_ln_kernel(const StreamArgs p) {
+  extern __shared__ unsigned char smem_raw[];
+  constexpr int SR = kWideWarps;
+  constexpr int U = kWideUnroll;
+  const Ring g = ring_setup(p, smem_raw, kWideWarps);
+  const RowArgs& a = p.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kWideWarps) {
+    if (lane == 0) produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, SR, sizeof(T), 2);
+    return;
+  }
+  const int N = a.N, nv = N >> 3;
+  const float fN = static_cast<float>(N);
+  const uint4* gs = reinterpret_cast<const uint4*>(g.w);
+  const uint4* bs = p.b_bytes > 0 ? reinterpret_cast<const uint4*>(g.w + p.w_bytes) : nullptr;
+  if (!mbar_wait(kWaitLimitNs, g.wbar, 0u)) {
+    flag_failure(p.status);
+    return;
+  }
+  int slot = 0;
+  uint32_t phase = 0;
+  for (;;) {
+    if (!mbar_wait(kWaitLimitNs, &g.full[slot], phase)) {
+      flag_failure(p.status);
+      return;
+    }
+    const int32_t rs = g.stage_row[slot];
+    if (rs < 0) break;  // end marker
+    const int32_t r = rs + warp;
+    if (r < static_cast<int32_t>(a.rows)) {  // warp-uniform
+      const uint4* xs = reinterpret_cast<const uint4*>(g.smem + static_cast<size_t>(slot) * p.stage_bytes +
+                                                       static_cast<size_t>(warp) * N * sizeof(T));
+      float2 acc[U];
+#pragma unroll
+      for (int j = 0; j < U; ++j) acc[j] = make_float2(0.f, 0.f);
+      for (int v = lane; v < nv; v += 32 * U) {
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          if (v + 32 * j >= nv) break;
+          const uint4 u = xs[v + 32 * j];
+          acc[j] = add2(acc[j], add2(add2(Elem<T>::unpack(u.x), Elem<T>::unpack(u.y)),
+                                     add2(Elem<T>::unpack(u.z), Elem<T>::unpack(u.w))));
+        }
+      }
+      const float2 s2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+      const float mean = __fdiv_rn(group_sum<32>(s2.x + s2.y), fN);
+      const float2 mean2 = splat2(mean);
+#pragma unroll
+      for (int j = 0; j < U; ++j) acc[j] = make_float2(0.f, 0.f);
+      for (int v = lane; v < nv; v += 32 * U) {
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          if (v + 32 * j >= nv) break;
+          const uint4 u = xs[v + 32 * j];
+          const float2 c0 = sub2(Elem<T>::unpack(u.x), mean2), c1 = sub2(Elem<T>::unpack(u.y), mean2);
+          const float2 c2 = sub2(Elem<T>::unpack(u.z), mean2), c3 = sub2(Elem<T>::unpack(u.w), mean2);
+          acc[j] = fma2(c0, c0, fma2(c1, c1, fma2(c2, c2, fma2(c3, c3, acc[j]))));
+        }
+      }
+      const float2 q2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+      const float var = __fdiv_rn(group_sum<32>(q2.x + q2.y), fN);
+      const float2 rstd2 = splat2(__fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, a.eps))));
+      uint4* yrow = reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N);
+      for (int v = lane; v < nv; v += 32) {
+        const uint4 u = xs[v], gv = gs[v];
+        const uint4 bv = bs != nullptr ? bs[v] : make_uint4(0u, 0u, 0u, 0u);
+        uint4 out;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 c = sub2(Elem<T>::unpack(rows::word(u, k)), mean2);
+          const float2 n = mul2(mul2(c, rstd2), Elem<T>::unpack(rows::word(gv, k)));
+          rows::set_word(out, k, Elem<T>::pack(add2_rn(n, Elem<T>::unpack(rows::word(bv, k)))));
+        }
+        st_stream16(yrow + v, out);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&g.empty[slot]);
+    if (++slot == p.stages) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------- host side
 template <typename K>
 bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_bytes, int tab_row_bytes,
@@ -575,6 +668,20 @@ bool dispatch_narrow(const RowArgs& a, cudaStream_t s) {
 }
 
 }  // namespace
+
+bool launch_layernorm_tma(const RowArgs& a, int dtype, cudaStream_t s) {
+  if (a.rows < 4096 || a.rows > 0x7fffffffLL - 256) return false;
+  if (a.token_stride != a.N || a.H != 1 || a.N < 1024) return false;
+  StreamArgs p{};
+  p.a = a;
+  p.a.R = 0;
+  const int xrow = a.N * 2;
+  p.w_bytes = xrow;                           // the gain row
+  p.b_bytes = a.bias != nullptr ? xrow : 0;   // the bias row, right after it
+  if (dtype == DT_BF16)
+    return launch_stream(rows_tma_ln_kernel<__nv_bfloat16>, kWideThreads, p, kWideWarps, xrow, 0, s, p.b_bytes);
+  return launch_stream(rows_tma_ln_kernel<__half>, kWideThreads, p, kWideWarps, xrow, 0, s, p.b_bytes);
+}
 
 bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s) {
   // Small problems are launch-bound: the generic kernel. Row indices and row + stage stay in int32.

@@ -91,6 +91,17 @@ int fq_rmsnorm_fwd_rstd(const void* x, const void* w, void* y, float* rstd, int6
                         float eps, cudaStream_t stream);
 
 /*
+ * LayerNorm forward, the fused kernel of "ledger.py" (Ch.13 ledger, layer_norm:
+ * y = (x - mean) / sqrt(var + eps) * g + b, one read of x, g, b and one write of y):
+ *   mean_i = sum_j x_ij / N;  var_i = sum_j (x_ij - mean_i)^2 / N;  rstd_i = 1/sqrt(var_i + eps) (fp32)
+ *   y_ij   = dtype(((x_ij - mean_i) * rstd_i) * gamma_j + beta_j)     (each fp32 step rounded)
+ * x, y: [M, N] dtype; gamma: [N] dtype; beta: [N] dtype or null (no bias). M >= 0 (0: no-op), N >= 1.
+ * The page gives the formula only (a byte ledger); the cast points follow the RMSNorm definitions.
+ */
+int fq_layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y, int64_t M, int64_t N, int dtype,
+                     float eps, cudaStream_t stream);
+
+/*
  * RMSNorm + NeoX partial RoPE ("rmsnorm_rope_quant.py", rms_norm_rope_fused and the first two
  * steps of torch_reference_fused):
  *   normed_ij = dtype((x_ij * rstd_i) * w_j)

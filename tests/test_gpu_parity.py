@@ -419,6 +419,34 @@ def test_rmsnorm_autograd_save_rstd(cuda_ok):
     assert_storage_close(grads[1][2], grads[0][2].cpu(), "dw")
 
 
+# LayerNorm: shapes that reach the register-resident, the TMA-fed and the scalar kernels
+LN_CASES = [
+    # M, N, dtype, bias, misalign
+    (300, 256, "bf16", True, False),
+    (129, 2048, "fp16", True, False),
+    (4097, 4096, "bf16", True, False),   # TMA-fed wide rows
+    (4100, 1024, "fp16", False, False),  # TMA-fed, no bias
+    (4096, 512, "bf16", True, False),    # many narrow rows: register-resident kernel
+    (77, 100, "bf16", True, False),      # odd width: scalar
+    (9, 5000, "bf16", True, False),      # wider than the register kernel: scalar
+    (60, 512, "fp16", True, True),       # misaligned: scalar
+]
+
+
+@pytest.mark.parametrize("case", LN_CASES, ids=lambda c: "M%d-N%d-%s-b%d-mis%d" % c)
+def test_layernorm_parity(orc, cuda_ok, case):
+    M, N, dt, bias, mis = case
+    d = wl.rmsnorm_inputs(M, N, dt, seed=800 + M)
+    b = (d["w"].float() - 1.0).to(d["w"].dtype) if bias else None
+    y_ref, _, _ = orc.layernorm_fwd(d["x"], d["w"], b)
+    g = cuda(d)
+    x = misalign(g["x"]) if mis else g["x"]
+    y = fq.layernorm_fwd(x, g["w"], None if b is None else b.cuda())
+    torch.cuda.synchronize()
+    assert_storage_close(y, y_ref)
+    assert fq.device_status(clear=True) == 0
+
+
 def test_rmsnorm_bwd_deterministic(cuda_ok):
     d = cuda(wl.rmsnorm_inputs(1000, 4096, "bf16", seed=550))
     a = fq.rmsnorm_bwd(d["x"], d["w"], d["g"])
