@@ -515,15 +515,16 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_rope_kernel(const 
 }
 
 // ------------------------------------------------------------------ wide rows, LayerNorm
-// LayerNorm forward ("ledger.py" (Ch.13 ledger), layer_norm) for rows of N >= 1024: four consumer
-// warps, one row per warp per stage, the gain and bias rows staged once per CTA. Three passes over
-// the staged row: the mean, the variance of the deviations (no E[x^2] - E[x]^2 cancellation), then
-// y = dtype(((x - mean) * rstd) * g + b) with each step rounded as the definition's fp32 ops.
-template <typename T>
+// LayerNorm forward ("ledger.py" (Ch.13 ledger), layer_norm) for rows of 1024 <= N <= 4096: four
+// consumer warps, one row per warp per stage, the gain and bias rows staged once per CTA. The warp
+// copies its row from the stage into registers (VPT 16-byte vectors per lane) and releases the stage
+// at once; then three passes over the registers: the mean, the variance of the deviations (no
+// E[x^2] - E[x]^2 cancellation), and y = dtype(((x - mean) * rstd) * g + b) with each step rounded
+// as the definition's fp32 ops.
+template <typename T, int VPT>
 __global__ void __launch_bounds__(kWideThreads) rows_tma_ln_kernel(const StreamArgs p) {
   extern __shared__ unsigned char smem_raw[];
   constexpr int SR = kWideWarps;
-  constexpr int U = kWideUnroll;
   const Ring g = ring_setup(p, smem_raw, kWideWarps);
   const RowArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -549,58 +550,56 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_ln_kernel(const StreamA
     const int32_t rs = g.stage_row[slot];
     if (rs < 0) break;  // end marker
     const int32_t r = rs + warp;
-    if (r < static_cast<int32_t>(a.rows)) {  // warp-uniform
-      const uint4* xs = reinterpret_cast<const uint4*>(g.smem + static_cast<size_t>(slot) * p.stage_bytes +
-                                                       static_cast<size_t>(warp) * N * sizeof(T));
-      float2 acc[U];
+    const bool live = r < static_cast<int32_t>(a.rows);  // warp-uniform
+    uint4 xv[VPT];
+    const uint4* xs = reinterpret_cast<const uint4*>(g.smem + static_cast<size_t>(slot) * p.stage_bytes +
+                                                     static_cast<size_t>(warp) * N * sizeof(T));
 #pragma unroll
-      for (int j = 0; j < U; ++j) acc[j] = make_float2(0.f, 0.f);
-      for (int v = lane; v < nv; v += 32 * U) {
-#pragma unroll
-        for (int j = 0; j < U; ++j) {
-          if (v + 32 * j >= nv) break;
-          const uint4 u = xs[v + 32 * j];
-          acc[j] = add2(acc[j], add2(add2(Elem<T>::unpack(u.x), Elem<T>::unpack(u.y)),
-                                     add2(Elem<T>::unpack(u.z), Elem<T>::unpack(u.w))));
-        }
-      }
-      const float2 s2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
-      const float mean = __fdiv_rn(group_sum<32>(s2.x + s2.y), fN);
-      const float2 mean2 = splat2(mean);
-#pragma unroll
-      for (int j = 0; j < U; ++j) acc[j] = make_float2(0.f, 0.f);
-      for (int v = lane; v < nv; v += 32 * U) {
-#pragma unroll
-        for (int j = 0; j < U; ++j) {
-          if (v + 32 * j >= nv) break;
-          const uint4 u = xs[v + 32 * j];
-          const float2 c0 = sub2(Elem<T>::unpack(u.x), mean2), c1 = sub2(Elem<T>::unpack(u.y), mean2);
-          const float2 c2 = sub2(Elem<T>::unpack(u.z), mean2), c3 = sub2(Elem<T>::unpack(u.w), mean2);
-          acc[j] = fma2(c0, c0, fma2(c1, c1, fma2(c2, c2, fma2(c3, c3, acc[j]))));
-        }
-      }
-      const float2 q2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
-      const float var = __fdiv_rn(group_sum<32>(q2.x + q2.y), fN);
-      const float2 rstd2 = splat2(__fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, a.eps))));
-      uint4* yrow = reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N);
-      for (int v = lane; v < nv; v += 32) {
-        const uint4 u = xs[v], gv = gs[v];
-        const uint4 bv = bs != nullptr ? bs[v] : make_uint4(0u, 0u, 0u, 0u);
-        uint4 out;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 c = sub2(Elem<T>::unpack(rows::word(u, k)), mean2);
-          const float2 n = mul2(mul2(c, rstd2), Elem<T>::unpack(rows::word(gv, k)));
-          rows::set_word(out, k, Elem<T>::pack(add2_rn(n, Elem<T>::unpack(rows::word(bv, k)))));
-        }
-        st_stream16(yrow + v, out);
-      }
-    }
+    for (int k = 0; k < VPT; ++k)
+      xv[k] = (live && lane + 32 * k < nv) ? xs[lane + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
-    if (lane == 0) mbar_arrive(&g.empty[slot]);
+    if (lane == 0) mbar_arrive(&g.empty[slot]);  // the row is in registers: release the stage
     if (++slot == p.stages) {
       slot = 0;
       phase ^= 1u;
+    }
+    if (!live) continue;
+    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      s0 = add2(s0, add2(Elem<T>::unpack(xv[k].x), Elem<T>::unpack(xv[k].y)));
+      s1 = add2(s1, add2(Elem<T>::unpack(xv[k].z), Elem<T>::unpack(xv[k].w)));
+    }
+    const float2 st = add2(s0, s1);
+    const float mean = __fdiv_rn(group_sum<32>(st.x + st.y), fN);
+    const float2 mean2 = splat2(mean);
+    float2 q0 = make_float2(0.f, 0.f), q1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      if (lane + 32 * k >= nv) continue;
+      const float2 c0 = sub2(Elem<T>::unpack(xv[k].x), mean2), c1 = sub2(Elem<T>::unpack(xv[k].y), mean2);
+      const float2 c2 = sub2(Elem<T>::unpack(xv[k].z), mean2), c3 = sub2(Elem<T>::unpack(xv[k].w), mean2);
+      q0 = fma2(c0, c0, fma2(c2, c2, q0));
+      q1 = fma2(c1, c1, fma2(c3, c3, q1));
+    }
+    const float2 qt = add2(q0, q1);
+    const float var = __fdiv_rn(group_sum<32>(qt.x + qt.y), fN);
+    const float2 rstd2 = splat2(__fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, a.eps))));
+    uint4* yrow = reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int v = lane + 32 * k;
+      if (v >= nv) continue;
+      const uint4 gv = gs[v];
+      const uint4 bv = bs != nullptr ? bs[v] : make_uint4(0u, 0u, 0u, 0u);
+      uint4 out;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 c = sub2(Elem<T>::unpack(rows::word(xv[k], e)), mean2);
+        const float2 n = mul2(mul2(c, rstd2), Elem<T>::unpack(rows::word(gv, e)));
+        rows::set_word(out, e, Elem<T>::pack(add2_rn(n, Elem<T>::unpack(rows::word(bv, e)))));
+      }
+      st_stream16(yrow + v, out);
     }
   }
 }
@@ -671,16 +670,22 @@ bool dispatch_narrow(const RowArgs& a, cudaStream_t s) {
 
 bool launch_layernorm_tma(const RowArgs& a, int dtype, cudaStream_t s) {
   if (a.rows < 4096 || a.rows > 0x7fffffffLL - 256) return false;
-  if (a.token_stride != a.N || a.H != 1 || a.N < 1024) return false;
+  if (a.token_stride != a.N || a.H != 1 || a.N < 1024 || a.N > 4096) return false;
   StreamArgs p{};
   p.a = a;
   p.a.R = 0;
   const int xrow = a.N * 2;
   p.w_bytes = xrow;                           // the gain row
   p.b_bytes = a.bias != nullptr ? xrow : 0;   // the bias row, right after it
-  if (dtype == DT_BF16)
-    return launch_stream(rows_tma_ln_kernel<__nv_bfloat16>, kWideThreads, p, kWideWarps, xrow, 0, s, p.b_bytes);
-  return launch_stream(rows_tma_ln_kernel<__half>, kWideThreads, p, kWideWarps, xrow, 0, s, p.b_bytes);
+#define FQ_LN(V)                                                                                             \
+  return dtype == DT_BF16                                                                                      \
+             ? launch_stream(rows_tma_ln_kernel<__nv_bfloat16, V>, kWideThreads, p, kWideWarps, xrow, 0, s, p.b_bytes) \
+             : launch_stream(rows_tma_ln_kernel<__half, V>, kWideThreads, p, kWideWarps, xrow, 0, s, p.b_bytes)
+  const int nv = a.N / 8;
+  if (nv <= 4 * 32) FQ_LN(4);
+  if (nv <= 8 * 32) FQ_LN(8);
+  FQ_LN(16);
+#undef FQ_LN
 }
 
 bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s) {
