@@ -182,6 +182,21 @@ class PrologueCase(Case):
                                    q_out=s["q"], scale=s["scale"])
 
 
+class PrologueDesignCase(PrologueCase):
+    """The 4k prologue computed as one of the Ch.28 page's designs: one CTA per block of `rpb` rows."""
+
+    def __init__(self, dev, rpb, label):
+        super().__init__(dev)
+        self.rpb = rpb
+        self.name = f"qk_norm_rope_quant T={self.T} Hq={self.Hq} Hk={self.Hk} D={self.D} as design {label} " \
+                    f"({rpb} rows per block)"
+
+    def launch(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.fq.qk_norm_rope_quant_blocks(s["qk"], s["wq"], s["wk"], s["cos"], s["sin"], self.Hq, self.Hk, self.rpb,
+                                          q_out=s["q"], scale=s["scale"])
+
+
 class RmsnormFwdCase(Case):
     def __init__(self, dev, M=8192, N=4096, n_sets=3):
         import torch
@@ -573,6 +588,9 @@ SECONDARY = {
                                                       note=" (Ch.13 ledger fused workload)"),
     "rope_quant_groups_ledger_4k": lambda dev: RopeQuantCase(dev, M=4096, N=4096, R=128, group_size=128,
                                                              write_y=False, n_sets=8),
+    "prologue_4k_design_a": lambda dev: PrologueDesignCase(dev, 1, "A"),
+    "prologue_4k_design_b": lambda dev: PrologueDesignCase(dev, 8, "B"),
+    "prologue_4k_design_c": lambda dev: PrologueDesignCase(dev, HQ + HK, "C"),
     "qk_prologue_32k": lambda dev: PrologueCase(dev, T=32768, Hq=64, Hk=8, std=1.0, theta=1e6, positions="uniform",
                                                 outlier_frac=0.01, n_sets=2, seed=20261202 + 4),
 }

@@ -22,7 +22,7 @@ import torch
 
 from . import _capi
 
-__all__ = ["layernorm_fwd", "rmsnorm_fwd", "rmsnorm_fwd_rstd", "rmsnorm_bwd_rstd", "rmsnorm_rope", "rmsnorm_rope_quant", "rmsnorm_rope_quant_groups", "qk_norm_rope_quant",
+__all__ = ["layernorm_fwd", "rmsnorm_fwd", "rmsnorm_fwd_rstd", "rmsnorm_bwd_rstd", "rmsnorm_rope", "rmsnorm_rope_quant", "rmsnorm_rope_quant_groups", "qk_norm_rope_quant", "qk_norm_rope_quant_blocks",
            "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_bytes", "rmsnorm", "RMSNormFunction", "device_status", "check_bounded_wait",
            "FqError"]
@@ -193,6 +193,25 @@ def qk_norm_rope_quant(qk, wq, wk, cos, sin, Hq: int, Hk: int, eps: float = 1e-6
     _capi.call("fq_qk_norm_rope_quant", _ptr(qk), token_stride, _ptr(wq), _ptr(wk), _ptr(cos), _ptr(sin),
                _ptr(q_out), _ptr(scale), T, Hq, Hk, D, R, _dtype(name, qk), _table_dtype(name, cos, sin), eps,
                fp8_max, _stream(dev))
+    return q_out, scale
+
+
+def qk_norm_rope_quant_blocks(qk, wq, wk, cos, sin, Hq: int, Hk: int, rows_per_block: int, eps: float = 1e-6,
+                              fp8_max: float = 448.0, q_out: torch.Tensor | None = None,
+                              scale: torch.Tensor | None = None):
+    """The prologue as the Ch.28 page's designs A / B / C: one CTA per block of rows_per_block rows
+    (1, 8, Hq + Hk). qk: [T, Hq+Hk, D] packed. Returns (q uint8 [T, H, D], scale fp32 [T, H])."""
+    name = "qk_norm_rope_quant_blocks"
+    dev = _need_cuda(name, qk, wq, wk, cos, sin, q_out, scale)
+    _contig(name, qk=qk, wq=wq, wk=wk, cos=cos, sin=sin, q_out=q_out, scale=scale)
+    H = Hq + Hk
+    D = wq.shape[0]
+    T = qk.shape[0]
+    q_out = torch.empty((T, H, D), dtype=torch.uint8, device=dev) if q_out is None else q_out
+    scale = torch.empty((T, H), dtype=torch.float32, device=dev) if scale is None else scale
+    _capi.call("fq_qk_norm_rope_quant_blocks", _ptr(qk), H * D, _ptr(wq), _ptr(wk), _ptr(cos), _ptr(sin),
+               _ptr(q_out), _ptr(scale), T, Hq, Hk, D, D, rows_per_block, _dtype(name, qk),
+               _table_dtype(name, cos, sin), eps, fp8_max, _stream(dev))
     return q_out, scale
 
 

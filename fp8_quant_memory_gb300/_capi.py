@@ -32,6 +32,8 @@ SIGNATURES = {
                                             _int, _f32, _f32, _vp]),
     "fq_qk_norm_rope_quant": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                      _int, _int, _f32, _f32, _vp]),
+    "fq_qk_norm_rope_quant_blocks": (_int, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                            _i64, _int, _int, _f32, _f32, _vp]),
     "fq_rmsnorm_bwd_workspace_bytes": (_sz, [_i64, _i64]),
     "fq_rmsnorm_bwd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _int, _f32, _vp]),
     "fq_rmsnorm_bwd_rstd": (_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _i64, _i64, _int, _vp]),

@@ -292,11 +292,16 @@ int fq_rmsnorm_rope_quant_groups(const void* x, const void* w, const void* cos, 
                     table_dtype, eps, fp8_max, stream);
 }
 
-int fq_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, const void* wk,
-                          const void* cos, const void* sin, uint8_t* q_out, float* scale, int64_t T,
-                          int64_t Hq, int64_t Hk, int64_t D, int64_t rope_dim, int dtype,
-                          int table_dtype, float eps, float fp8_max, cudaStream_t stream) {
-  const char* fn = "fq_qk_norm_rope_quant";
+}  // extern "C"
+
+namespace {
+
+// Validation and argument packing shared by the prologue entry points; returns FQ_OK and fills `a`
+// (a.rows == 0: nothing to launch).
+int prologue_args(const char* fn, const void* qk, int64_t token_stride, const void* wq, const void* wk,
+                  const void* cos, const void* sin, uint8_t* q_out, float* scale, int64_t T, int64_t Hq,
+                  int64_t Hk, int64_t D, int64_t rope_dim, int dtype, int table_dtype, float eps, float fp8_max,
+                  fq::RowArgs* a) {
   if (int rc = check_common(fn, dtype, eps)) return rc;
   if (int rc = check_fp8_max(fn, fp8_max)) return rc;
   if (T < 0 || Hq < 0 || Hk < 0 || Hq + Hk < 1 || D < 1 || D > kMaxWidth || Hq + Hk > kMaxWidth)
@@ -307,29 +312,69 @@ int fq_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, 
                 static_cast<long long>(token_stride), static_cast<long long>(H * D));
   if (T > kMaxRows / H) return fail(FQ_ERR_INVALID_ARG, "%s: T*(Hq+Hk) must be < 2^31", fn);
   if (int rc = check_rope(fn, D, rope_dim, cos, sin, table_dtype, T == 0)) return rc;
+  *a = fq::RowArgs{};
   if (T == 0) return ok();
   if (qk == nullptr || wq == nullptr || wk == nullptr || q_out == nullptr || scale == nullptr)
     return fail(FQ_ERR_INVALID_ARG, "%s: null pointer", fn);
-  fq::RowArgs a{};
-  a.x = qk;
-  a.wq = wq;
-  a.wk = wk;
-  a.cos = cos;
-  a.sin = sin;
-  a.y = nullptr;
-  a.q = q_out;
-  a.scale = scale;
-  a.rows = T * H;
-  a.token_stride = token_stride;
-  a.H = static_cast<int32_t>(H);
-  a.Hq = static_cast<int32_t>(Hq);
-  a.N = static_cast<int32_t>(D);
-  a.R = static_cast<int32_t>(rope_dim);
-  a.eps = eps;
-  a.fp8_max = fp8_max;
+  a->x = qk;
+  a->wq = wq;
+  a->wk = wk;
+  a->cos = cos;
+  a->sin = sin;
+  a->y = nullptr;
+  a->q = q_out;
+  a->scale = scale;
+  a->rows = T * H;
+  a->token_stride = token_stride;
+  a->H = static_cast<int32_t>(H);
+  a->Hq = static_cast<int32_t>(Hq);
+  a->N = static_cast<int32_t>(D);
+  a->R = static_cast<int32_t>(rope_dim);
+  a->eps = eps;
+  a->fp8_max = fp8_max;
+  return FQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fq_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, const void* wk,
+                          const void* cos, const void* sin, uint8_t* q_out, float* scale, int64_t T,
+                          int64_t Hq, int64_t Hk, int64_t D, int64_t rope_dim, int dtype,
+                          int table_dtype, float eps, float fp8_max, cudaStream_t stream) {
+  const char* fn = "fq_qk_norm_rope_quant";
+  fq::RowArgs a;
+  if (int rc = prologue_args(fn, qk, token_stride, wq, wk, cos, sin, q_out, scale, T, Hq, Hk, D, rope_dim, dtype,
+                             table_dtype, eps, fp8_max, &a))
+    return rc;
+  if (a.rows == 0) return ok();
   return launch_rows(fn, a, fq::MODE_QK, dtype, table_dtype, stream);
 }
 
+int fq_qk_norm_rope_quant_blocks(const void* qk, int64_t token_stride, const void* wq, const void* wk,
+                                 const void* cos, const void* sin, uint8_t* q_out, float* scale, int64_t T,
+                                 int64_t Hq, int64_t Hk, int64_t D, int64_t rope_dim, int64_t rows_per_block,
+                                 int dtype, int table_dtype, float eps, float fp8_max, cudaStream_t stream) {
+  const char* fn = "fq_qk_norm_rope_quant_blocks";
+  if (rows_per_block < 1 || rows_per_block > 128)
+    return fail(FQ_ERR_INVALID_ARG, "%s: rows_per_block must be in [1, 128], got %lld", fn,
+                static_cast<long long>(rows_per_block));
+  fq::RowArgs a;
+  if (int rc = prologue_args(fn, qk, token_stride, wq, wk, cos, sin, q_out, scale, T, Hq, Hk, D, rope_dim, dtype,
+                             table_dtype, eps, fp8_max, &a))
+    return rc;
+  if (a.rows == 0) return ok();
+  const int64_t tsize = (table_dtype == FQ_FP32) ? 4 : 2;
+  const bool vec = D == rope_dim && D % 16 == 0 && D <= 128 && aligned(qk, 16) && aligned(wq, 16) &&
+                   aligned(wk, 16) && aligned(cos, 16) && aligned(sin, 16) && (token_stride * 2) % 16 == 0 &&
+                   ((rope_dim / 2) * tsize) % 16 == 0 && aligned(q_out, 8) && aligned(scale, 4);
+  cudaGetLastError();
+  if (!vec || !fq::launch_prologue_blocks(a, static_cast<int32_t>(rows_per_block), dtype, table_dtype, stream))
+    return fail(FQ_ERR_UNSUPPORTED,
+                "%s: needs head_dim = rope_dim <= 128, a multiple of 16, and 16-byte aligned tensors", fn);
+  return check_launch(fn);
+}
 size_t fq_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N) {
   if (M <= 0 || N <= 0) return 0;
   return fq::bwd_workspace_bytes(M, N);

@@ -48,6 +48,10 @@ constexpr int kMaxVecGroups = 512;
 // Returns false (launching nothing) when the shape has no instantiation.
 bool launch_rows_vector(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s);
 
+// The prologue as one CTA per block of rows_per_block consecutive rows (the Ch.28 page's designs A,
+// B, C), for measuring what each design moves. head_dim <= 128 fully rotated, vector layout rules.
+bool launch_prologue_blocks(const RowArgs& a, int32_t rows_per_block, int dtype, int table_dtype, cudaStream_t s);
+
 // TMA-fed persistent prologue kernel (MODE_QK, N == R == 128, 16-byte aligned token stride, table
 // dtype fp32 or the storage dtype). Returns false (launching nothing) when it does not apply.
 bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s);

@@ -72,6 +72,47 @@ __global__ void __launch_bounds__(kThreads) rows_vec_kernel(const RowArgs a) {
   }
 }
 
+// The Ch.28 page's designs A / B / C ("case_norm_rope_quant.py", default_designs): one CTA per block
+// of `rpb` consecutive (token, head) rows -- 1 (A), 8 (B) or a whole token (C) -- each row one lane
+// group, the weight and the token's table row read through L1 by every row of the block (so each
+// block brings them from L2 once). A measurement device for the page's lookup-byte model, not a
+// fast path: the prologue's own kernel streams chunks through a TMA ring instead.
+template <typename T, typename TT, int LPR, int HS, int TS>
+__global__ void rows_block_kernel(const RowArgs a, int32_t rpb) {
+  constexpr int kV = HS + 2 * TS;
+  const int lane = threadIdx.x & (LPR - 1);
+  const int grp = threadIdx.x / LPR;
+  if (grp >= rpb) return;
+  const int N = a.N;
+  const int hv = (N - a.R) >> 3, th = a.R >> 4, half = a.R >> 1;
+  const float fN = static_cast<float>(N);
+  const int32_t r = blockIdx.x * rpb + grp;
+  const bool rv = r < static_cast<int32_t>(a.rows);
+  const int32_t t = rv ? r / a.H : 0;
+  const int32_t h = rv ? r - t * a.H : 0;
+  const T* xrow = static_cast<const T*>(a.x) + (static_cast<int64_t>(t) * a.token_stride + static_cast<int64_t>(h) * N);
+  uint4 xv[kV];
+#pragma unroll
+  for (int s = 0; s < kV; ++s)
+    xv[s] = (rv && slot_ok<LPR, HS, TS>(s, lane, hv, th)) ? ld_stream16(xrow + slot_col<LPR, HS, TS>(s, lane, hv, th))
+                                                         : make_uint4(0u, 0u, 0u, 0u);
+  row_body<T, TT, MODE_QK, LPR, HS, TS, false>(a, r, rv, h, xv, lane, hv, th, fN, a.cos, a.sin,
+                                               static_cast<int64_t>(t) * half);
+}
+
+template <typename T, typename TT>
+bool launch_block_t(const RowArgs& a, int32_t rpb, cudaStream_t s) {
+  const int hv = (a.N - a.R) / 8, th = a.R / 16;
+  // one lane group of 8 lanes per row for head_dim <= 128 with the whole head rotated
+  if (!(hv == 0 && th <= 8)) return false;
+  const int threads = ((rpb * 8 + 31) / 32) * 32;
+  if (threads > 1024) return false;
+  const int64_t grid = (a.rows + rpb - 1) / rpb;
+  if (grid > 0x7fffffffLL) return false;
+  rows_block_kernel<T, TT, 8, 0, 1><<<static_cast<unsigned>(grid), threads, 0, s>>>(a, rpb);
+  return true;
+}
+
 // Wide rows, RMSNorm forward: one warp per row in two passes. Pass 1 streams x (eight 16-byte
 // vectors per lane in flight) for the sum of squares; pass 2 reads the row again -- it was just
 // fetched, so it comes from L2, not HBM -- and writes y. Holding a 4096-wide row in registers
@@ -237,6 +278,15 @@ bool dispatch_mode(const RowArgs& a, int mode, int table_dtype, cudaStream_t s) 
 }
 
 }  // namespace
+
+bool launch_prologue_blocks(const RowArgs& a, int32_t rows_per_block, int dtype, int table_dtype, cudaStream_t s) {
+  if (table_dtype != DT_FP32 && table_dtype != dtype) return false;
+  if (dtype == DT_BF16)
+    return table_dtype == DT_FP32 ? launch_block_t<__nv_bfloat16, float>(a, rows_per_block, s)
+                                  : launch_block_t<__nv_bfloat16, __nv_bfloat16>(a, rows_per_block, s);
+  return table_dtype == DT_FP32 ? launch_block_t<__half, float>(a, rows_per_block, s)
+                                : launch_block_t<__half, __half>(a, rows_per_block, s);
+}
 
 bool launch_rows_vector(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s) {
   if (a.R > 0 && table_dtype != DT_FP32 && table_dtype != dtype) return false;

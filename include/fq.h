@@ -163,6 +163,21 @@ int fq_qk_norm_rope_quant(const void* qk, int64_t token_stride, const void* wq, 
                           int table_dtype, float eps, float fp8_max, cudaStream_t stream);
 
 /*
+ * The prologue computed as the Ch.28 page's designs ("case_norm_rope_quant.py", default_designs):
+ * one CTA per block of rows_per_block consecutive (token, head) rows -- 1 (design A), 8 (design B),
+ * Hq + Hk (design C: one whole token) -- each block reading the norm weight and the token's table
+ * row through its own L1, so the weight and table are brought from L2 once per block, which is what
+ * the page's modelled lookup bytes count. Same results as fq_qk_norm_rope_quant (same arithmetic as
+ * its generic kernel). A measurement device, not a fast path. rows_per_block in [1, 128]; needs
+ * head_dim = rope_dim <= 128, a multiple of 16, and 16-byte aligned tensors (else
+ * FQ_ERR_UNSUPPORTED). Other arguments and errors as fq_qk_norm_rope_quant.
+ */
+int fq_qk_norm_rope_quant_blocks(const void* qk, int64_t token_stride, const void* wq, const void* wk,
+                                 const void* cos, const void* sin, uint8_t* q_out, float* scale, int64_t T,
+                                 int64_t Hq, int64_t Hk, int64_t D, int64_t rope_dim, int64_t rows_per_block,
+                                 int dtype, int table_dtype, float eps, float fp8_max, cudaStream_t stream);
+
+/*
  * Bytes of caller-provided device workspace fq_rmsnorm_bwd needs for an [M, N] problem: the fp32
  * per-chunk partial column sums of the two-stage dw reduction. 0 when M == 0.
  */

@@ -535,6 +535,25 @@ def test_prologue_tma_writes_every_row(orc, cuda_ok, monkeypatch, case):
     assert fq.device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("rpb", [1, 8, 40, 128])
+@pytest.mark.parametrize("case", [(37, 32, 8, "bf16", "fp32"), (21, 6, 2, "fp16", "fp16"), (9, 3, 0, "bf16", "bf16")],
+                         ids=lambda c: "T%d-%d+%d-%s-%s" % c)
+def test_prologue_design_blocks(orc, cuda_ok, monkeypatch, case, rpb):
+    """The Ch.28 page's designs (one CTA per block of 1, 8, a token's 40, or 128 rows; ragged last
+    blocks): against the oracle, and bit for bit the generic prologue kernel (same arithmetic)."""
+    T, Hq, Hk, dt, tdt = case
+    d = wl.qk_inputs(T, Hq, Hk, 128, dt, tdt, seed=820 + T, std=2.0)
+    q_ref, s_ref = orc.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], Hq, Hk)
+    g = cuda(d)
+    q, s = fq.qk_norm_rope_quant_blocks(g["qk"], g["wq"], g["wk"], g["cos"], g["sin"], Hq, Hk, rpb)
+    torch.cuda.synchronize()
+    assert_scale_close(s, s_ref)
+    assert_codes_close(q, q_ref)
+    monkeypatch.setenv("FQ_PROLOGUE_KERNEL", "generic")
+    q2, s2 = fq.qk_norm_rope_quant(g["qk"], g["wq"], g["wk"], g["cos"], g["sin"], Hq, Hk)
+    assert torch.equal(q, q2) and torch.equal(s, s2)
+
+
 def test_prologue_tma_matches_generic_kernel(cuda_ok, monkeypatch):
     """Both kernels on identical inputs: scales within 1e-6 relative, codes at most one step apart."""
     d = cuda(wl.qk_inputs(777, 32, 8, 128, "bf16", "fp32", seed=790, std=2.0))
