@@ -200,11 +200,13 @@ __device__ __forceinline__ void prologue_row(const PrologueArgs& a, uint32_t st,
   }
   if (live) {
     // ql/qh[0..1] hold sub-chunk rev, [2..3] the other one (8 codes each)
+    // One 16-byte store per half: the sub-chunk order is put back into column order first (two
+    // store instructions instead of four: fewer L1 wavefronts per row, measurably faster).
     uint8_t* qrow = a.q + static_cast<int64_t>(r) * kD + 16 * j;
-    st_stream8(qrow + 8 * rev, make_uint2(ql[0], ql[1]));
-    st_stream8(qrow + 8 * (rev ^ 1), make_uint2(ql[2], ql[3]));
-    st_stream8(qrow + 64 + 8 * rev, make_uint2(qh[0], qh[1]));
-    st_stream8(qrow + 64 + 8 * (rev ^ 1), make_uint2(qh[2], qh[3]));
+    const uint4 lo16 = rev ? make_uint4(ql[2], ql[3], ql[0], ql[1]) : make_uint4(ql[0], ql[1], ql[2], ql[3]);
+    const uint4 hi16 = rev ? make_uint4(qh[2], qh[3], qh[0], qh[1]) : make_uint4(qh[0], qh[1], qh[2], qh[3]);
+    st_stream16(qrow, lo16);
+    st_stream16(qrow + 64, hi16);
     if (j == 0) a.scale[r] = sc;
   }
 }
