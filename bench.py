@@ -612,7 +612,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-extras", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    ap.add_argument("--workload", choices=["qk_prologue_4k", *SECONDARY], default="qk_prologue_4k",
+    ap.add_argument("--workload", choices=["qk_prologue_4k", "torch_eager_prologue", *SECONDARY], default="qk_prologue_4k",
                     help="time one secondary workload alone (for profiling) instead of the benchmark step")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -638,6 +638,22 @@ def main():
 
     _capi.load()
     stream = torch.cuda.Stream(dev)
+    if args.workload == "torch_eager_prologue":
+        # The unfused per-op torch sequence alone (no graphs), then one more step inside an NVTX range
+        # ("eager_step") so that a profiler can sum the DRAM bytes of exactly one step's kernels.
+        eager = TorchEagerPrologueCase(PrologueCase(dev))
+        ms, _ = time_case(eager, args.steps, args.warmup, stream, use_graph=False)
+        with torch.cuda.stream(stream):
+            torch.cuda.nvtx.range_push("eager_step")
+            eager.launch(0)
+            torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        if rank == 0:
+            us = ms * 1e3 / args.steps
+            print(json.dumps({"workload": eager.name, "us_per_step": round(us, 3),
+                              "GB/s_of_fused_ledger": round(eager.bytes_per_step() / (us * 1e-6) / 1e9, 1)}),
+                  flush=True)
+        return 0
     if args.workload != "qk_prologue_4k":
         res = time_secondary(SECONDARY[args.workload](dev), args.steps, args.warmup, stream, peaks()[0])
         if rank == 0:

@@ -58,3 +58,23 @@ def page_prologue_ideal_bytes(T: int, Hq: int, Hk: int, D: int, in_bytes: int = 
     payload = elems * in_bytes + elems * out_bytes + rows * 4
     lookup = 2 * D * in_bytes + 2 * T * D * table_bytes
     return payload + lookup
+
+
+def page_unfused_norm_rope_quant_bytes(m: int, n: int, rope_dim: int, in_bytes: int = 2, out_bytes: int = 1) -> int:
+    """The Ch.13 ledger's unfused plan for RMSNorm + RoPE + quantisation ("ledger.py",
+    fused_norm_rope_quant, `separate`): RMSNorm reads x, w and writes normed; RoPE reads normed, cos, sin
+    and writes rotated; quantisation reads rotated and writes q and one fp32 amax per row. cos and sin
+    are [m, rope_dim/2] in the input dtype, as the page's Buf declarations."""
+    x = m * n * in_bytes
+    w = n * in_bytes
+    table = 2 * m * (rope_dim // 2) * in_bytes
+    normed = m * n * in_bytes
+    rotated = m * n * in_bytes
+    q = m * n * out_bytes
+    amax = m * 4
+    return (x + w + normed) + (normed + table + rotated) + (rotated + q + amax)
+
+
+def page_fused_norm_rope_quant_bytes(m: int, n: int, rope_dim: int, in_bytes: int = 2, out_bytes: int = 1) -> int:
+    """The same ledger's fused plan: read x, w, cos, sin once; write q and amax once."""
+    return m * n * in_bytes + n * in_bytes + 2 * m * (rope_dim // 2) * in_bytes + m * n * out_bytes + m * 4

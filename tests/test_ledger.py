@@ -41,3 +41,13 @@ def test_rmsnorm_ledgers():
     assert ledger.rmsnorm_fwd_bytes(8192, 4096) == 134_225_920
     assert ledger.rmsnorm_bwd_bytes(8192, 4096) == 201_342_976
     assert ledger.rope_bytes(65536, 192, 64, "fp16", "fp16") == 2 * 65536 * 192 * 2 + 192 * 2 + 2 * 65536 * 32 * 2
+
+
+def test_page_norm_rope_quant_plans_at_the_page_shape():
+    """Ch.13 ledger, fused_norm_rope_quant at 4096 x 4096, rope 128, bf16: 185.62 MB unfused, 51.40 MB fused."""
+    from fp8_quant_memory_gb300 import ledger
+
+    assert round(ledger.page_unfused_norm_rope_quant_bytes(4096, 4096, 128) / 1e6, 2) == 185.62
+    assert round(ledger.page_fused_norm_rope_quant_bytes(4096, 4096, 128) / 1e6, 2) == 51.40
+    assert ledger.page_fused_norm_rope_quant_bytes(4096, 4096, 128) == ledger.rope_quant_bytes(
+        4096, 4096, 128, "bf16", "bf16", write_y=False)
