@@ -499,8 +499,7 @@ bool launch_stage1_stream_t(const BwdArgs& a, const BwdPlan& plan, cudaStream_t 
   if (p.depth > p.stages) p.depth = p.stages;
   const size_t smem = stream_smem_bytes(p.stages, p.stage_bytes);
   auto kern = bwd_stage1_stream_kernel<T, VPT, SAVED>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-    return false;
+  if (!ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem)) return false;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(plan.chunks));
   cfg.blockDim = dim3(kStreamThreads);
@@ -525,7 +524,7 @@ void launch_stage1(const BwdArgs& a, const BwdPlan& p, cudaStream_t s) {
   constexpr int G = kThreads / TPR;
   const size_t smem = (G > 1) ? static_cast<size_t>(G) * VPT * TPR * 8 * sizeof(float) : 0;
   auto kern = bwd_stage1_kernel<T, TPR, VPT, RB>;
-  if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem);
   kern<<<static_cast<unsigned>(p.chunks), kThreads, smem, s>>>(a, p.rows_per_chunk);
 }
 

@@ -102,6 +102,11 @@ cudaError_t launch_wait_probe(unsigned int limit_ms, cudaStream_t s);
 
 int sm_count();
 
+// Raises `kernel`'s dynamic shared-memory limit to at least `bytes` on the current device. The limit
+// belongs to the device's context, so it is remembered per (device, kernel); thread-safe. False if
+// the driver refuses.
+bool ensure_dynamic_smem(const void* kernel, size_t bytes);
+
 // Records a printf-style message for fq_last_error() on this thread and returns `code`.
 int set_error(int code, const char* fmt, ...);
 

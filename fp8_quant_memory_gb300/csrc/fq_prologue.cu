@@ -485,14 +485,7 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
                       : prologue_tma_kernel<__nv_bfloat16, __nv_bfloat16, SR>;
   else
     kern = (tsz == 4) ? prologue_tma_kernel<__half, float, SR> : prologue_tma_kernel<__half, __half, SR>;
-  static int configured[4] = {0, 0, 0, 0};
-  const int key = (dtype == DT_BF16 ? 0 : 2) + (tsz == 4 ? 0 : 1);
-  if (configured[key] < static_cast<int>(smem)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
-      return false;
-    configured[key] = static_cast<int>(smem);
-  }
+  if (!ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem)) return false;
   // One CTA per chunk of SR rows. Only the CTAs that fit on the GPU at once start; they take over
   // the rest of the grid chunk by chunk (cluster launch control), so the grid is not a wave count.
   const int grid = static_cast<int>((a.rows + SR - 1) / SR);

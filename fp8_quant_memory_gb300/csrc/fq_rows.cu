@@ -220,13 +220,7 @@ bool launch_one(const RowArgs& a, cudaStream_t s) {
   size_t smem = 0;
   if (MODE == MODE_ROPE_QUANT && a.group > 0) {
     smem = static_cast<size_t>(kThreads / LPR) * (a.N / a.group) * sizeof(uint32_t);
-    static size_t configured = 48 * 1024;
-    if (smem > configured) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-          cudaSuccess)
-        return false;
-      configured = smem;
-    }
+    if (!ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem)) return false;
   }
   kern<<<grid, kThreads, smem, s>>>(a);
   return true;

@@ -625,8 +625,7 @@ bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_
   if (p.depth > p.stages) p.depth = p.stages;
   const size_t smem = ring_bytes(p.stages, p.stage_bytes, p.w_bytes) + extra_bytes;
   if (smem > 227 * 1024) return false;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
-    return false;
+  if (!ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem)) return false;
   // One CTA per stage of rows. Only the CTAs that fit on the GPU at once start; they take over the
   // rest of the grid stage by stage (cluster launch control), so the grid is not a wave count.
   cudaLaunchConfig_t cfg{};

@@ -1,12 +1,32 @@
 // fq_status.cu -- the device status word. Kernels that wait on something (a bounded mbarrier wait
 // in a pipelined kernel) set bit 0 here instead of trapping when a wait gives up, so the context
 // stays usable and the host can read the failure with fq_device_status().
+#include <map>
+#include <mutex>
+#include <utility>
+
 #include "fq_internal.h"
 #include "fq_sync.cuh"
 
 namespace fq {
 
 __device__ unsigned int g_device_status = 0u;
+
+bool ensure_dynamic_smem(const void* kernel, size_t bytes) {
+  if (bytes <= 48 * 1024) return true;  // the default limit
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  static std::mutex mu;
+  static std::map<std::pair<int, const void*>, size_t> done;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = done[{dev, kernel}];
+  if (have >= bytes) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)) !=
+      cudaSuccess)
+    return false;
+  have = bytes;
+  return true;
+}
 
 unsigned int* device_status_ptr() {
   void* p = nullptr;
