@@ -18,6 +18,9 @@
 //     16-byte vectors deep; the weight row is copied into shared memory once per CTA. Two CTAs
 //     share an SM, so a stage is four rows and the ring fills and drains in small steps.
 // y is written with 16-byte evict-first stores. x and the tables are read from HBM exactly once.
+#include <cstdlib>
+#include <string>
+
 #include "fq_device.cuh"
 #include "fq_internal.h"
 #include "fq_rows.cuh"
@@ -49,11 +52,11 @@ struct StreamArgs {
 constexpr int kReq = 2;  // cluster-launch-control requests a producer keeps in flight
 
 // Producer: one lane streams the stages this CTA takes (its own first, then those of CTAs it takes
-// over), posts an end marker, and returns. `issued` work requests were started before the dependency
-// wait (ring_setup).
+// over), posts `markers` end markers (one per group of consumer warps that take stages in turn), and
+// returns. `issued` work requests were started before the dependency wait (ring_setup).
 __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem, uint64_t* full, uint64_t* empty,
                                         uint64_t* wbar, unsigned char* wsm, uint4* resp, uint64_t* cbar,
-                                        int32_t* stage_row, int SR, int esize, int tsize) {
+                                        int32_t* stage_row, int SR, int esize, int tsize, int markers = 1) {
   const RowArgs& a = p.a;
   const int S = p.stages;
   if (p.w_bytes > 0) {
@@ -124,13 +127,21 @@ __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem
     }
     ++answered;
   }
-  // End marker (every consumer warp reads every stage).
-  if (ok && k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) ok = false;
-  if (ok) {
+  // End markers: one stage each, so that every group of consumer warps meets one.
+  for (int e = 0; ok && e < markers; ++e) {
+    if (k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) {
+      ok = false;
+      break;
+    }
     stage_row[slot] = -1;
     mbar_arrive(&full[slot]);
-    return;
+    ++k;
+    if (++slot == S) {
+      slot = 0;
+      phase ^= 1u;
+    }
   }
+  if (ok) return;
   flag_failure(p.status);
   for (int j = max(0, k - S); j < k; ++j)
     if (!mbar_wait(kWaitLimitNs, &full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
@@ -158,7 +169,10 @@ __host__ __device__ constexpr size_t ring_bytes(int stages, int stage_bytes, int
          stages * sizeof(int32_t) + 128 + w_bytes;
 }
 
-__device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* smem_raw, int consumers) {
+// `consumers`: warps that release each stage; the producer is warp `producer_warp` (default: the
+// warp after `consumers`).
+__device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* smem_raw, int consumers,
+                                           int producer_warp = -1) {
   Ring g;
   const uint32_t raw = smem_addr(smem_raw);
   g.smem = smem_raw + ((128u - (raw & 127u)) & 127u);
@@ -183,7 +197,7 @@ __device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* s
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // The work requests touch no data of the previous kernel: the producer lane starts them before the
   // dependency wait. Every global access comes after it.
-  if (threadIdx.x == consumers * 32)
+  if (threadIdx.x == (producer_warp < 0 ? consumers : producer_warp) * 32)
     for (int c = 0; c < kReq; ++c) clc_try_cancel(&g.resp[c], &g.cbar[c]);
   asm volatile("griddepcontrol.wait;" ::: "memory");
   return g;
@@ -514,6 +528,191 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_rope_kernel(const 
   }
 }
 
+// ------------------------------------------------------- wide rows, FP8, register-resident rows
+// RMSNorm + NeoX partial RoPE + FP8 codes with one scale per row or per group of columns
+// ("rmsnorm_rope_quant.py" (Ch.13 fusion), rms_norm_rope_quant_fused) for rows of N = 256 * VPT
+// elements, rope_dim <= 256, group sizes that are powers of two. Twelve consumer warps in three
+// groups of four take the stages in turn (one CTA per SM, so a stage of four rows and its table rows
+// fit six times); each warp copies its row -- VPT 16-byte vectors per lane, vector v = lane + 32k --
+// into registers, and with it, on the lanes that hold rotary vectors (all in the last slot, since
+// N / 8 is a multiple of 32 and rope_dim / 8 <= 32), the rotation partner's vector and the eight
+// cos and sin entries of its pairs; then it releases the stage. Everything after that runs on
+// registers: the sum of squares; y = dtype(x * rstd * w) per vector, the rotary lanes rotating
+// their own and their partner's normalised values (each lane computes its own output: lo' = lo*c -
+// hi*s on the lo side, hi' = hi*c + lo*s on the hi side, the same rounded operations as the
+// definition); the |y| maxima (per row over the warp; per group over the group's lanes of a slot,
+// then across slots for groups of more than 32 vectors); and the codes as correctly rounded
+// quotients. The warp's rows and the stage ring are independent, so the copy of the next stages
+// overlaps this work, and at most three rows per SM wait for data at a time.
+// Rows per stage = warps per consumer group. Consumer groups take the stages in turn: three for
+// rows of up to 3072 (13 warps: registers are allotted for 16, so 128 per thread), two for rows of
+// 4096, whose 64 registers of row data need more room (168 per thread).
+constexpr int kRegRows = 4;
+__host__ __device__ constexpr int reg_groups(int vpt) { return vpt <= 12 ? 3 : 2; }
+__host__ __device__ constexpr int reg_threads(int vpt) { return (kRegRows * reg_groups(vpt) + 1) * 32; }
+
+// RN(m / fmax) from rcp = RN(1 / fmax): one product and Markstein's correction (the residual
+// m - s0 * fmax is exact in one FMA). m >= 1e-4 and fmax a normal float keep every step normal.
+__device__ __forceinline__ float scale_of(float m, float fmax, float rcp) {
+  const float s0 = __fmul_rn(m, rcp);
+  return __fmaf_rn(__fmaf_rn(-s0, fmax, m), rcp, s0);
+}
+
+template <typename T>
+__device__ __forceinline__ uint2 codes8(uint4 y, float s, float r, bool clamp, float fmax) {
+  float2 q[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    q[e] = div2_by(Elem<T>::unpack(rows::word(y, e)), s, r);
+    if (clamp) q[e] = make_float2(clamp_abs(q[e].x, fmax), clamp_abs(q[e].y, fmax));
+  }
+  return pack_e4m3x8(q[0], q[1], q[2], q[3]);
+}
+
+template <typename T>
+__device__ __forceinline__ float absmax8(uint4 y) {
+  return absmax4(absmax4(0.f, Elem<T>::unpack(y.x), Elem<T>::unpack(y.y)), Elem<T>::unpack(y.z),
+                 Elem<T>::unpack(y.w));
+}
+
+template <typename T, typename TT, int VPT, bool GROUPED>
+__global__ void __launch_bounds__(reg_threads(VPT), 1) rows_tma_wide_quant_kernel(const StreamArgs p) {
+  extern __shared__ unsigned char smem_raw[];
+  constexpr int kRegGroups = reg_groups(VPT);
+  constexpr int kRegWarps = kRegRows * kRegGroups;
+  const Ring g = ring_setup(p, smem_raw, kRegRows, kRegWarps);
+  const RowArgs& a = p.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kRegWarps) {
+    if (lane == 0)
+      produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, kRegRows, sizeof(T), sizeof(TT),
+              kRegGroups);
+    return;
+  }
+  const int grp = warp / kRegRows, wr = warp % kRegRows;  // consumer group, row within the stage
+  constexpr int N = 256 * VPT;
+  const int hr = a.R >> 4;             // rotary vectors per half
+  const bool rot = lane >= 32 - 2 * hr;  // this lane's last-slot vector is a rotary one
+  const bool is_lo = lane < 32 - hr;
+  const int partner = is_lo ? lane + hr : lane - hr;
+  const int pblk = is_lo ? lane - (32 - 2 * hr) : lane - (32 - hr);  // pairs 8 pblk .. 8 pblk + 7
+  const int half = a.R >> 1;
+  const uint4* ws = reinterpret_cast<const uint4*>(g.w);
+  const int lg = GROUPED ? __ffs(a.group) - 1 : 0;  // log2 of the group size
+  const int gv = GROUPED ? a.group >> 3 : 32 * VPT;  // vectors per group
+  const int G = GROUPED ? N >> lg : 1;
+  const float fmax = a.fp8_max, rcp = __frcp_rn(a.fp8_max);
+  const bool clamp = a.fp8_max != 448.0f;
+  if (!mbar_wait(kWaitLimitNs, g.wbar, 0u)) {
+    flag_failure(p.status);
+    return;
+  }
+  int slot = grp;  // stage k lives in slot k % S; this group takes stages grp, grp + 3, ...
+  uint32_t phase = 0;
+  for (;;) {
+    if (!mbar_wait(kWaitLimitNs, &g.full[slot], phase)) {
+      flag_failure(p.status);
+      return;
+    }
+    const int32_t rs = g.stage_row[slot];
+    if (rs < 0) break;  // end marker
+    const int32_t r = rs + wr;
+    const bool live = r < static_cast<int32_t>(a.rows);  // warp-uniform
+    const unsigned char* st = g.smem + static_cast<size_t>(slot) * p.stage_bytes;
+    const uint4* xs = reinterpret_cast<const uint4*>(st + static_cast<size_t>(wr) * N * sizeof(T));
+    const int rel_slot = slot;
+    slot += kRegGroups;
+    if (slot >= p.stages) {
+      slot -= p.stages;
+      phase ^= 1u;
+    }
+    if (!live) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&g.empty[rel_slot]);
+      continue;
+    }
+    uint4 xv[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) xv[k] = xs[lane + 32 * k];
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; k += 2) {
+      acc0 = sq_acc<T>(xv[k], acc0);
+      acc1 = sq_acc<T>(xv[k + 1], acc1);
+    }
+    const float2 acc = add2(acc0, acc1);
+    const float2 rstd2 = splat2(rstd_from_ss(group_sum<32>(acc.x + acc.y), static_cast<float>(N), a.eps));
+    // The last slot first: its rotary lanes read their partner's vector and their cos / sin entries
+    // from the stage, which is released right after.
+    {
+      constexpr int k = VPT - 1;
+      uint4 y = norm8<T>(xv[k], ws[lane + 32 * k], rstd2);
+      if (rot) {
+        const uint4 yp = norm8<T>(xs[32 * k + partner], ws[32 * k + partner], rstd2);
+        float2 c[4], sn[4];
+        const int64_t off = static_cast<int64_t>(wr) * half + 8 * pblk;
+        rows::load_table8<TT, true>(st + p.tab_off, off, c);
+        rows::load_table8<TT, true>(st + p.tab_off + p.tab_block, off, sn);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 own = Elem<T>::unpack(rows::word(y, e)), other = Elem<T>::unpack(rows::word(yp, e));
+          const float2 s2 = is_lo ? neg2(sn[e]) : sn[e];  // lo' = lo*c + hi*(-s), hi' = hi*c + lo*s
+          rows::set_word(y, e, Elem<T>::pack(add2(mul2(own, c[e]), mul2(other, s2))));
+        }
+      }
+      xv[k] = y;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&g.empty[rel_slot]);  // everything this warp needs is in registers
+    uint4* yrow = a.y != nullptr ? reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N)
+                                 : nullptr;
+    // Per row: one running |y| maximum; per group: one per slot.
+    float mk[GROUPED ? VPT : 1];
+    mk[0] = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      if (k < VPT - 1) xv[k] = norm8<T>(xv[k], ws[lane + 32 * k], rstd2);
+      if (yrow != nullptr) st_stream16(yrow + lane + 32 * k, xv[k]);
+      if constexpr (GROUPED)
+        mk[k] = absmax8<T>(xv[k]);
+      else
+        mk[0] = fmaxf(mk[0], absmax8<T>(xv[k]));
+    }
+    uint2* qrow = reinterpret_cast<uint2*>(a.q + static_cast<int64_t>(r) * N);
+    if constexpr (!GROUPED) {
+      const float sc = scale_of(fmaxf(group_max<32>(mk[0]), 1e-4f), fmax, rcp);
+      const float rc = __frcp_rn(sc);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) st_stream8(qrow + lane + 32 * k, codes8<T>(xv[k], sc, rc, clamp, fmax));
+      if (lane == 0) a.scale[r] = sc;
+    } else {
+      // Group maxima: within a slot a group is gv consecutive lanes (gv <= 32) ...
+#pragma unroll
+      for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1)
+          if (o < gv) mk[k] = fmaxf(mk[k], __shfl_xor_sync(0xffffffffu, mk[k], o));
+      // ... and a group of more than 32 vectors spans gv / 32 consecutive slots.
+#pragma unroll
+      for (int d = 1; d < VPT; d <<= 1)
+        if (32 * d < gv) {
+#pragma unroll
+          for (int k = 0; k < VPT; ++k)
+            if ((k & d) == 0 && (k | d) < VPT) mk[k] = mk[k | d] = fmaxf(mk[k], mk[k | d]);
+        }
+      float* srow = a.scale + static_cast<int64_t>(r) * G;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        const float sg = scale_of(fmaxf(mk[k], 1e-4f), fmax, rcp);
+        const float rg = __frcp_rn(sg);
+        st_stream8(qrow + lane + 32 * k, codes8<T>(xv[k], sg, rg, clamp, fmax));
+        const int col = 8 * (lane + 32 * k);
+        if ((col & (a.group - 1)) == 0) srow[col >> lg] = sg;  // the group's first vector
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ wide rows, LayerNorm
 // LayerNorm forward ("ledger.py" (Ch.13 ledger), layer_norm) for rows of 1024 <= N <= 4096: four
 // consumer warps, one row per warp per stage, the gain and bias rows staged once per CTA. The warp
@@ -605,9 +804,12 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_ln_kernel(const StreamA
 }
 
 // ---------------------------------------------------------------------------------- host side
+// `budget`: shared-memory bytes for the ring (0: two CTAs per SM when stages are small, else one);
+// `inflight`: bytes the producer keeps in flight.
 template <typename K>
 bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_bytes, int tab_row_bytes,
-                   cudaStream_t s, int extra_bytes = 0) {
+                   cudaStream_t s, int extra_bytes = 0, int budget = 0, int inflight = 48 * 1024,
+                   int min_stages = 2) {
   const RowArgs& a = p.a;
   p.status = device_status_ptr();
   p.tab_block = ((stage_rows * tab_row_bytes) + 127) & ~127;
@@ -615,12 +817,12 @@ bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_
   p.stage_bytes = p.tab_off + 2 * p.tab_block;
   // Two CTAs per SM when stages are small (a four-row stage of 4096-wide rows with its table rows
   // still fits three times); as many stages as fit, at most 8.
-  const int budget = p.stage_bytes <= 36 * 1024 ? 110 * 1024 : 220 * 1024;
+  if (budget == 0) budget = p.stage_bytes <= 36 * 1024 ? 110 * 1024 : 220 * 1024;
   p.stages = (budget - static_cast<int>(ring_bytes(0, 0, p.w_bytes)) - extra_bytes - 8) / (p.stage_bytes + 20);
   if (p.stages > 8) p.stages = 8;
-  if (p.stages < 2) return false;
-  // Keep about 48 KB in flight per CTA (at least two stages), never more than the ring.
-  p.depth = (48 * 1024 + p.stage_bytes - 1) / p.stage_bytes;
+  if (p.stages < min_stages) return false;
+  // Keep about `inflight` bytes in flight per CTA (at least two stages), never more than the ring.
+  p.depth = (inflight + p.stage_bytes - 1) / p.stage_bytes;
   if (p.depth < 2) p.depth = 2;
   if (p.depth > p.stages) p.depth = p.stages;
   const size_t smem = ring_bytes(p.stages, p.stage_bytes, p.w_bytes) + extra_bytes;
@@ -702,6 +904,38 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
     const int trow = (a.R / 2) * tsz;
     const int extra = (mode == MODE_ROPE_QUANT && a.group > 0) ? kWideWarps * 3 * (a.N / a.group) * 4 : 0;
     const bool quant = mode == MODE_ROPE_QUANT;
+    // Quantising rows of 1024, 2048, 3072 or 4096 with rope_dim <= 256 and a power-of-two group
+    // size (or one scale per row): the register-resident kernel, one CTA per SM.
+    const int vpt = a.N / 256;
+    const bool pow2_group = a.group == 0 || (a.group >= 8 && (a.group & (a.group - 1)) == 0 && a.N % a.group == 0);
+    const bool grouped = a.group > 0 && a.group < a.N;  // a group of the whole row is the per-row scale
+    // FQ_ROWS_KERNEL=staged keeps these on the shared-memory kernel below (diagnostic switch: both
+    // compute the same result).
+    const char* sel = getenv("FQ_ROWS_KERNEL");
+    const bool staged = sel != nullptr && std::string(sel) == "staged";
+    if (quant && !staged && a.N % 256 == 0 && (vpt == 4 || vpt == 8 || vpt == 12 || vpt == 16) && a.R <= 256 &&
+        a.R % 16 == 0 && pow2_group) {
+#define FQ_REG(T, TT, V)                                                                                      \
+  if (vpt == (V))                                                                                             \
+    return grouped ? launch_stream(rows_tma_wide_quant_kernel<T, TT, V, true>, reg_threads(V), p, kRegRows, xrow, \
+                                   trow, s, 0, 220 * 1024, 96 * 1024, reg_groups(V))                            \
+                   : launch_stream(rows_tma_wide_quant_kernel<T, TT, V, false>, reg_threads(V), p, kRegRows,      \
+                                   xrow, trow, s, 0, 220 * 1024, 96 * 1024, reg_groups(V));
+#define FQ_REG_T(T, TT) FQ_REG(T, TT, 4) FQ_REG(T, TT, 8) FQ_REG(T, TT, 12) FQ_REG(T, TT, 16)
+      if (dtype == DT_BF16) {
+        if (tsz == 4) {
+          FQ_REG_T(__nv_bfloat16, float)
+        } else {
+          FQ_REG_T(__nv_bfloat16, __nv_bfloat16)
+        }
+      } else if (tsz == 4) {
+        FQ_REG_T(__half, float)
+      } else {
+        FQ_REG_T(__half, __half)
+      }
+#undef FQ_REG_T
+#undef FQ_REG
+    }
 #define FQ_WIDE(T, TT)                                                                                      \
   return quant ? launch_stream(rows_tma_wide_rope_kernel<T, TT, true>, kWideThreads, p, kWideWarps, xrow, trow, s, \
                                extra)                                                                       \

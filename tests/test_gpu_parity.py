@@ -209,13 +209,18 @@ WIDE_QUANT_CASES = [
     (4099, 1024, 64, 8, "fp16", "fp32", True),        # 128 groups per row, ragged last stage
     (4100, 2048, 0, None, "bf16", "bf16", True),      # no rotation
     (4097, 1536, 256, 512, "bf16", "fp32", False),    # groups spanning head and tail
+    (4096, 3072, 128, 1024, "bf16", "fp32", True),    # a group spans four 32-vector slots
+    (4098, 4096, 256, 512, "fp16", "fp32", False),    # every last-slot lane rotary; groups of two slots
+    (4096, 2048, 32, 2048, "bf16", "bf16", True),     # one group per row through the group entry point
+    (4101, 3072, 16, None, "fp16", "fp16", False),    # one rotary pair block per half
 ]
 
 
-@pytest.mark.parametrize("kernel", ["tma", "generic"])
+@pytest.mark.parametrize("kernel", ["tma", "staged", "generic"])
 @pytest.mark.parametrize("case", WIDE_QUANT_CASES, ids=lambda c: "M%d-N%d-R%d-g%s-%s-%s-y%d" % c)
 def test_wide_rows_quant_stream_kernel(orc, cuda_ok, monkeypatch, case, kernel):
-    """RMSNorm + RoPE + FP8 on >= 4096 rows of >= 1024 elements (the TMA-fed wide-row kernel, and the
+    """RMSNorm + RoPE + FP8 on >= 4096 rows of >= 1024 elements (the TMA-fed register-resident kernel
+    where the width, rope_dim and group size allow it, the TMA-fed shared-memory kernel, and the
     generic kernel on the same inputs): y against the oracle, codes and scales exactly the quantiser
     of the kernel's own y."""
     _rows_kernel(monkeypatch, kernel)
@@ -588,8 +593,8 @@ def test_bounded_wait_gives_up_and_context_stays_usable(orc, cuda_ok):
 
 # ----------------------------------------------------------------------------------- TMA row-stream kernels
 def _rows_kernel(monkeypatch, kernel):
-    if kernel == "generic":
-        monkeypatch.setenv("FQ_ROWS_KERNEL", "generic")
+    if kernel in ("generic", "staged"):
+        monkeypatch.setenv("FQ_ROWS_KERNEL", kernel)
     else:
         monkeypatch.delenv("FQ_ROWS_KERNEL", raising=False)
 
