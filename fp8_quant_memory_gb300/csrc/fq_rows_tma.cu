@@ -569,57 +569,107 @@ __device__ __forceinline__ uint2 codes8(uint4 y, float s, float r, bool clamp, f
   return pack_e4m3x8(q[0], q[1], q[2], q[3]);
 }
 
+// Reduce-scatter of per-slot maxima over segments of SEG lanes (VPT values per lane, both powers of
+// two): at each level the lanes of a pair (lane mask O) keep opposite halves of their values and take
+// the maximum with the partner's copy of the half they keep; once a lane is down to one value the
+// remaining levels are plain max-reductions. Afterwards lane j of a segment holds in m[i]
+// (i < max(1, VPT / SEG)) the segment's maximum of slot i + floor(j * VPT / SEG).
+template <int N, int O, int VPT>
+__device__ __forceinline__ void seg_reduce_scatter(float (&m)[VPT], int lane) {
+  const bool upper = (lane & O) != 0;
+  if constexpr (N > 1) {
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) {
+      const float keep = upper ? m[i + N / 2] : m[i];
+      const float send = upper ? m[i] : m[i + N / 2];
+      m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, O));
+    }
+  } else {
+    m[0] = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], O));
+  }
+  if constexpr (O > 1) seg_reduce_scatter<(N > 1 ? N / 2 : 1), O / 2, VPT>(m, lane);
+}
+
 template <typename T>
 __device__ __forceinline__ float absmax8(uint4 y) {
   return absmax4(absmax4(0.f, Elem<T>::unpack(y.x), Elem<T>::unpack(y.y)), Elem<T>::unpack(y.z),
                  Elem<T>::unpack(y.w));
 }
 
-template <typename T, typename TT, int VPT, bool GROUPED>
-__global__ void __launch_bounds__(reg_threads(VPT), 1) rows_tma_wide_quant_kernel(const StreamArgs p) {
-  extern __shared__ unsigned char smem_raw[];
-  constexpr int kRegGroups = reg_groups(VPT);
+// Barrier of the TPR warps that share a row (named barrier 1 + team); team_all also ANDs a predicate
+// over them, so a failed wait in one warp stops its partner at the same point instead of leaving it
+// at a later barrier.
+__device__ __forceinline__ void team_sync(int team, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + team), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ bool team_all(bool v, int team, int threads) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred pi, po;\n\tsetp.ne.u32 pi, %1, 0;\n\tbar.red.and.pred po, %2, %3, pi;\n\tselp.u32 %0, 1, 0, po;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(1 + team), "r"(threads)
+      : "memory");
+  return r != 0;
+}
+
+// GV: 0 = one scale per row; > 0 = groups of GV vectors (8 * GV columns, GV <= 32) reduced by a
+// reduce-scatter; -1 = any power-of-two group size, reduced per slot.
+// TPR: warps per row. With two, each warp holds one contiguous half of the row (VPT / 2 slots), the
+// pair adds its sums of squares and takes the larger |y| maximum through shared memory, and a group
+// never spans the two halves (the host sends groups wider than half a row elsewhere).
+template <typename T, typename TT, int VPT, int GV, int TPR>
+__global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_wide_quant_kernel(const StreamArgs p) {
+  constexpr bool GROUPED = GV != 0;
+  constexpr int VW = VPT / TPR;                  // slots per warp
+  constexpr int kRegGroups = reg_groups(VW);
   constexpr int kRegWarps = kRegRows * kRegGroups;
+  constexpr int SR = kRegRows / TPR;             // rows per stage
+  static_assert(TPR == 1 || TPR == 2, "one or two warps per row");
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ float xch[kRegWarps][2];  // per warp: partial sum of squares, partial |y| maximum
   const Ring g = ring_setup(p, smem_raw, kRegRows, kRegWarps);
   const RowArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (warp == kRegWarps) {
     if (lane == 0)
-      produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, kRegRows, sizeof(T), sizeof(TT),
+      produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, SR, sizeof(T), sizeof(TT),
               kRegGroups);
     return;
   }
-  const int grp = warp / kRegRows, wr = warp % kRegRows;  // consumer group, row within the stage
+  const int grp = warp / kRegRows, wg = warp % kRegRows;  // consumer group, warp within the group
+  const int wr = wg / TPR, hh = wg % TPR;                  // row within the stage, part of the row
+  const int team = warp / TPR;
   constexpr int N = 256 * VPT;
-  const int hr = a.R >> 4;             // rotary vectors per half
-  const bool rot = lane >= 32 - 2 * hr;  // this lane's last-slot vector is a rotary one
+  const int vb = hh * 32 * VW;           // first vector of this warp's part of the row
+  const int hr = a.R >> 4;               // rotary vectors per half of the rotary block
+  const bool rot = hh == TPR - 1 && lane >= 32 - 2 * hr;  // this lane's last-slot vector is a rotary one
   const bool is_lo = lane < 32 - hr;
   const int partner = is_lo ? lane + hr : lane - hr;
   const int pblk = is_lo ? lane - (32 - 2 * hr) : lane - (32 - hr);  // pairs 8 pblk .. 8 pblk + 7
   const int half = a.R >> 1;
-  const uint4* ws = reinterpret_cast<const uint4*>(g.w);
+  const uint4* ws = reinterpret_cast<const uint4*>(g.w) + vb;
   const int lg = GROUPED ? __ffs(a.group) - 1 : 0;  // log2 of the group size
-  const int gv = GROUPED ? a.group >> 3 : 32 * VPT;  // vectors per group
+  const int gv = GROUPED ? a.group >> 3 : 32 * VW;   // vectors per group
   const int G = GROUPED ? N >> lg : 1;
   const float fmax = a.fp8_max, rcp = __frcp_rn(a.fp8_max);
   const bool clamp = a.fp8_max != 448.0f;
-  if (!mbar_wait(kWaitLimitNs, g.wbar, 0u)) {
-    flag_failure(p.status);
-    return;
-  }
+  bool ok = mbar_wait(kWaitLimitNs, g.wbar, 0u);
   int slot = grp;  // stage k lives in slot k % S; this group takes stages grp, grp + 3, ...
   uint32_t phase = 0;
   for (;;) {
-    if (!mbar_wait(kWaitLimitNs, &g.full[slot], phase)) {
+    ok = ok && mbar_wait(kWaitLimitNs, &g.full[slot], phase);
+    if constexpr (TPR > 1) ok = team_all(ok, team, 32 * TPR);  // the partner looks at the stage only if both can
+    if (!ok) {
       flag_failure(p.status);
       return;
     }
     const int32_t rs = g.stage_row[slot];
     if (rs < 0) break;  // end marker
     const int32_t r = rs + wr;
-    const bool live = r < static_cast<int32_t>(a.rows);  // warp-uniform
+    const bool live = r < static_cast<int32_t>(a.rows);  // uniform over the row's warps
     const unsigned char* st = g.smem + static_cast<size_t>(slot) * p.stage_bytes;
-    const uint4* xs = reinterpret_cast<const uint4*>(st + static_cast<size_t>(wr) * N * sizeof(T));
+    const uint4* xs = reinterpret_cast<const uint4*>(st + static_cast<size_t>(wr) * N * sizeof(T)) + vb;
     const int rel_slot = slot;
     slot += kRegGroups;
     if (slot >= p.stages) {
@@ -631,21 +681,27 @@ __global__ void __launch_bounds__(reg_threads(VPT), 1) rows_tma_wide_quant_kerne
       if (lane == 0) mbar_arrive(&g.empty[rel_slot]);
       continue;
     }
-    uint4 xv[VPT];
+    uint4 xv[VW];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) xv[k] = xs[lane + 32 * k];
+    for (int k = 0; k < VW; ++k) xv[k] = xs[lane + 32 * k];
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int k = 0; k < VPT; k += 2) {
+    for (int k = 0; k < VW; k += 2) {
       acc0 = sq_acc<T>(xv[k], acc0);
       acc1 = sq_acc<T>(xv[k + 1], acc1);
     }
     const float2 acc = add2(acc0, acc1);
-    const float2 rstd2 = splat2(rstd_from_ss(group_sum<32>(acc.x + acc.y), static_cast<float>(N), a.eps));
+    float ss = group_sum<32>(acc.x + acc.y);
+    if constexpr (TPR > 1) {
+      if (lane == 0) xch[warp][0] = ss;
+      team_sync(team, 32 * TPR);
+      ss = xch[team * TPR][0] + xch[team * TPR + 1][0];  // the same order in both warps
+    }
+    const float2 rstd2 = splat2(rstd_from_ss(ss, static_cast<float>(N), a.eps));
     // The last slot first: its rotary lanes read their partner's vector and their cos / sin entries
     // from the stage, which is released right after.
     {
-      constexpr int k = VPT - 1;
+      constexpr int k = VW - 1;
       uint4 y = norm8<T>(xv[k], ws[lane + 32 * k], rstd2);
       if (rot) {
         const uint4 yp = norm8<T>(xs[32 * k + partner], ws[32 * k + partner], rstd2);
@@ -664,49 +720,89 @@ __global__ void __launch_bounds__(reg_threads(VPT), 1) rows_tma_wide_quant_kerne
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&g.empty[rel_slot]);  // everything this warp needs is in registers
-    uint4* yrow = a.y != nullptr ? reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N)
-                                 : nullptr;
+    uint4* yrow = a.y != nullptr
+                      ? reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N) + vb
+                      : nullptr;
     // Per row: one running |y| maximum; per group: one per slot.
-    float mk[GROUPED ? VPT : 1];
+    float mk[GROUPED ? VW : 1];
     mk[0] = 0.f;
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      if (k < VPT - 1) xv[k] = norm8<T>(xv[k], ws[lane + 32 * k], rstd2);
+    for (int k = 0; k < VW; ++k) {
+      if (k < VW - 1) xv[k] = norm8<T>(xv[k], ws[lane + 32 * k], rstd2);
       if (yrow != nullptr) st_stream16(yrow + lane + 32 * k, xv[k]);
       if constexpr (GROUPED)
         mk[k] = absmax8<T>(xv[k]);
       else
         mk[0] = fmaxf(mk[0], absmax8<T>(xv[k]));
     }
-    uint2* qrow = reinterpret_cast<uint2*>(a.q + static_cast<int64_t>(r) * N);
+    uint2* qrow = reinterpret_cast<uint2*>(a.q + static_cast<int64_t>(r) * N) + vb;
     if constexpr (!GROUPED) {
-      const float sc = scale_of(fmaxf(group_max<32>(mk[0]), 1e-4f), fmax, rcp);
+      float m = group_max<32>(mk[0]);
+      if constexpr (TPR > 1) {
+        if (lane == 0) xch[warp][1] = m;
+        team_sync(team, 32 * TPR);
+        m = fmaxf(xch[team * TPR][1], xch[team * TPR + 1][1]);
+      }
+      const float sc = scale_of(fmaxf(m, 1e-4f), fmax, rcp);
       const float rc = __frcp_rn(sc);
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) st_stream8(qrow + lane + 32 * k, codes8<T>(xv[k], sc, rc, clamp, fmax));
-      if (lane == 0) a.scale[r] = sc;
+      for (int k = 0; k < VW; ++k) st_stream8(qrow + lane + 32 * k, codes8<T>(xv[k], sc, rc, clamp, fmax));
+      if (hh == 0 && lane == 0) a.scale[r] = sc;
+    } else if constexpr (GV > 0) {
+      // One group per (slot, segment of GV lanes). The slots are reduced in blocks of BLK (the
+      // largest power of two dividing VW); after a block's reduce-scatter every lane owns NF of its
+      // groups: it computes their scales and reciprocals once and writes the scales; each lane then
+      // fetches its slots' scale and reciprocal from the owner.
+      static_assert(GV <= 32 && (GV & (GV - 1)) == 0, "reduce-scatter shape");
+      constexpr int BLK = VW & -VW, NB = VW / BLK;
+      constexpr int NF = BLK >= GV ? BLK / GV : 1;
+      const int j = lane & (GV - 1), sgm = lane / GV;
+      float* srow = a.scale + static_cast<int64_t>(r) * (N / (8 * GV)) + hh * (VW * 32 / GV);
+      float sgv[NB][NF], rgv[NB][NF];
+#pragma unroll
+      for (int bk = 0; bk < NB; ++bk) {
+        float m[BLK];
+#pragma unroll
+        for (int i = 0; i < BLK; ++i) m[i] = mk[bk * BLK + i];
+        if constexpr (GV > 1) seg_reduce_scatter<BLK, GV / 2, BLK>(m, lane);
+#pragma unroll
+        for (int i = 0; i < NF; ++i) {
+          sgv[bk][i] = scale_of(fmaxf(m[i], 1e-4f), fmax, rcp);
+          rgv[bk][i] = __frcp_rn(sgv[bk][i]);
+          const int k = bk * BLK + (BLK >= GV ? i + NF * j : (j * BLK) / GV);
+          if (BLK >= GV || (j & (GV / BLK - 1)) == 0) srow[k * (32 / GV) + sgm] = sgv[bk][i];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < VW; ++k) {
+        const int bk = k / BLK, kb = k % BLK;
+        const int src = sgm * GV + (BLK >= GV ? kb / NF : kb * (GV / BLK));
+        const float sg = __shfl_sync(0xffffffffu, sgv[bk][kb % NF], src);
+        const float rg = __shfl_sync(0xffffffffu, rgv[bk][kb % NF], src);
+        st_stream8(qrow + lane + 32 * k, codes8<T>(xv[k], sg, rg, clamp, fmax));
+      }
     } else {
       // Group maxima: within a slot a group is gv consecutive lanes (gv <= 32) ...
 #pragma unroll
-      for (int k = 0; k < VPT; ++k)
+      for (int k = 0; k < VW; ++k)
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1)
           if (o < gv) mk[k] = fmaxf(mk[k], __shfl_xor_sync(0xffffffffu, mk[k], o));
       // ... and a group of more than 32 vectors spans gv / 32 consecutive slots.
 #pragma unroll
-      for (int d = 1; d < VPT; d <<= 1)
+      for (int d = 1; d < VW; d <<= 1)
         if (32 * d < gv) {
 #pragma unroll
-          for (int k = 0; k < VPT; ++k)
-            if ((k & d) == 0 && (k | d) < VPT) mk[k] = mk[k | d] = fmaxf(mk[k], mk[k | d]);
+          for (int k = 0; k < VW; ++k)
+            if ((k & d) == 0 && (k | d) < VW) mk[k] = mk[k | d] = fmaxf(mk[k], mk[k | d]);
         }
       float* srow = a.scale + static_cast<int64_t>(r) * G;
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) {
+      for (int k = 0; k < VW; ++k) {
         const float sg = scale_of(fmaxf(mk[k], 1e-4f), fmax, rcp);
         const float rg = __frcp_rn(sg);
         st_stream8(qrow + lane + 32 * k, codes8<T>(xv[k], sg, rg, clamp, fmax));
-        const int col = 8 * (lane + 32 * k);
+        const int col = 8 * (vb + lane + 32 * k);
         if ((col & (a.group - 1)) == 0) srow[col >> lg] = sg;  // the group's first vector
       }
     }
@@ -915,12 +1011,23 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
     const bool staged = sel != nullptr && std::string(sel) == "staged";
     if (quant && !staged && a.N % 256 == 0 && (vpt == 4 || vpt == 8 || vpt == 12 || vpt == 16) && a.R <= 256 &&
         a.R % 16 == 0 && pow2_group) {
-#define FQ_REG(T, TT, V)                                                                                      \
-  if (vpt == (V))                                                                                             \
-    return grouped ? launch_stream(rows_tma_wide_quant_kernel<T, TT, V, true>, reg_threads(V), p, kRegRows, xrow, \
-                                   trow, s, 0, 220 * 1024, 96 * 1024, reg_groups(V))                            \
-                   : launch_stream(rows_tma_wide_quant_kernel<T, TT, V, false>, reg_threads(V), p, kRegRows,      \
-                                   xrow, trow, s, 0, 220 * 1024, 96 * 1024, reg_groups(V));
+#define FQ_REG_K2(T, TT, V, GV, TPR)                                                                         \
+  return launch_stream(rows_tma_wide_quant_kernel<T, TT, V, GV, TPR>, reg_threads((V) / (TPR)), p,              \
+                       kRegRows / (TPR), xrow, trow, s, 0, 220 * 1024, 96 * 1024, reg_groups((V) / (TPR)));
+// Rows of 4096: two warps per row, so that three consumer groups fit the registers.
+#define FQ_REG_K(T, TT, V, GV)                                                      \
+  {                                                                                 \
+    if constexpr ((V) == 16) {                                                      \
+      if (a.group <= a.N / 2) FQ_REG_K2(T, TT, V, GV, 2)                            \
+    }                                                                               \
+    FQ_REG_K2(T, TT, V, GV, 1)                                                      \
+  }
+#define FQ_REG(T, TT, V)                                         \
+  if (vpt == (V)) {                                              \
+    if (!grouped) FQ_REG_K(T, TT, V, 0)                          \
+    if (a.group == 128) FQ_REG_K(T, TT, V, 16)                   \
+    FQ_REG_K(T, TT, V, -1)                                       \
+  }
 #define FQ_REG_T(T, TT) FQ_REG(T, TT, 4) FQ_REG(T, TT, 8) FQ_REG(T, TT, 12) FQ_REG(T, TT, 16)
       if (dtype == DT_BF16) {
         if (tsz == 4) {
@@ -935,6 +1042,8 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
       }
 #undef FQ_REG_T
 #undef FQ_REG
+#undef FQ_REG_K
+#undef FQ_REG_K2
     }
 #define FQ_WIDE(T, TT)                                                                                      \
   return quant ? launch_stream(rows_tma_wide_rope_kernel<T, TT, true>, kWideThreads, p, kWideWarps, xrow, trow, s, \

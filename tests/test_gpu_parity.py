@@ -213,6 +213,10 @@ WIDE_QUANT_CASES = [
     (4098, 4096, 256, 512, "fp16", "fp32", False),    # every last-slot lane rotary; groups of two slots
     (4096, 2048, 32, 2048, "bf16", "bf16", True),     # one group per row through the group entry point
     (4101, 3072, 16, None, "fp16", "fp16", False),    # one rotary pair block per half
+    (4102, 1024, 64, 128, "fp16", "fp32", True),      # groups of 128, four slots per lane
+    (4096, 2048, 128, 128, "bf16", "fp32", False),    # groups of 128, eight slots per lane
+    (4097, 4096, 64, 64, "bf16", "bf16", False),      # groups of 64 on the widest rows
+    (4099, 3072, 128, 128, "bf16", "bf16", True),     # groups of 128, twelve slots per lane (3 blocks)
 ]
 
 
