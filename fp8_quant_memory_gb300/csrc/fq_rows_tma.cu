@@ -810,81 +810,110 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_wide_quant
 }
 
 // ------------------------------------------------------------------ wide rows, LayerNorm
-// LayerNorm forward ("ledger.py" (Ch.13 ledger), layer_norm) for rows of 1024 <= N <= 4096: four
-// consumer warps, one row per warp per stage, the gain and bias rows staged once per CTA. The warp
-// copies its row from the stage into registers (VPT 16-byte vectors per lane) and releases the stage
-// at once; then three passes over the registers: the mean, the variance of the deviations (no
-// E[x^2] - E[x]^2 cancellation), and y = dtype(((x - mean) * rstd) * g + b) with each step rounded
-// as the definition's fp32 ops.
-template <typename T, int VPT>
-__global__ void __launch_bounds__(kWideThreads) rows_tma_ln_kernel(const StreamArgs p) {
+// LayerNorm forward ("ledger.py" (Ch.13 ledger), layer_norm) for rows of 1024 <= N <= 4096, with the
+// consumer layout of the FP8 kernel above: consumer groups of four warps take the stages in turn (one
+// CTA per SM), TPR warps per row (two for rows longer than 2048, each holding one contiguous half),
+// the gain and bias rows staged once per CTA. A warp copies its part of the row into registers
+// (VPT / TPR 16-byte vectors per lane) and releases the stage at once; then three passes over the
+// registers: the mean, the variance of the deviations (no E[x^2] - E[x]^2 cancellation), and
+// y = dtype(((x - mean) * rstd) * g + b) with each step rounded as the definition's fp32 ops. With
+// two warps per row their partial sums meet in shared memory, added in the same order by both.
+template <typename T, int VPT, int TPR>
+__global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_ln_kernel(const StreamArgs p) {
+  constexpr int VW = VPT / TPR;
+  constexpr int kRegGroups = reg_groups(VW);
+  constexpr int kRegWarps = kRegRows * kRegGroups;
+  constexpr int SR = kRegRows / TPR;
+  static_assert(TPR == 1 || TPR == 2, "one or two warps per row");
   extern __shared__ unsigned char smem_raw[];
-  constexpr int SR = kWideWarps;
-  const Ring g = ring_setup(p, smem_raw, kWideWarps);
+  __shared__ float xch[kRegWarps][2];  // per warp: partial sum, partial sum of squared deviations
+  const Ring g = ring_setup(p, smem_raw, kRegRows, kRegWarps);
   const RowArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (warp == kWideWarps) {
-    if (lane == 0) produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, SR, sizeof(T), 2);
+  if (warp == kRegWarps) {
+    if (lane == 0)
+      produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, SR, sizeof(T), 2, kRegGroups);
     return;
   }
+  const int grp = warp / kRegRows, wg = warp % kRegRows;
+  const int wr = wg / TPR, hh = wg % TPR;
+  const int team = warp / TPR;
   const int N = a.N, nv = N >> 3;
+  const int vb = hh * 32 * VW;  // first vector of this warp's part of the row
   const float fN = static_cast<float>(N);
-  const uint4* gs = reinterpret_cast<const uint4*>(g.w);
-  const uint4* bs = p.b_bytes > 0 ? reinterpret_cast<const uint4*>(g.w + p.w_bytes) : nullptr;
-  if (!mbar_wait(kWaitLimitNs, g.wbar, 0u)) {
-    flag_failure(p.status);
-    return;
-  }
-  int slot = 0;
+  const uint4* gs = reinterpret_cast<const uint4*>(g.w) + vb;
+  const uint4* bs = p.b_bytes > 0 ? reinterpret_cast<const uint4*>(g.w + p.w_bytes) + vb : nullptr;
+  bool ok = mbar_wait(kWaitLimitNs, g.wbar, 0u);
+  int slot = grp;
   uint32_t phase = 0;
   for (;;) {
-    if (!mbar_wait(kWaitLimitNs, &g.full[slot], phase)) {
+    ok = ok && mbar_wait(kWaitLimitNs, &g.full[slot], phase);
+    if constexpr (TPR > 1) ok = team_all(ok, team, 32 * TPR);
+    if (!ok) {
       flag_failure(p.status);
       return;
     }
     const int32_t rs = g.stage_row[slot];
     if (rs < 0) break;  // end marker
-    const int32_t r = rs + warp;
-    const bool live = r < static_cast<int32_t>(a.rows);  // warp-uniform
-    uint4 xv[VPT];
+    const int32_t r = rs + wr;
+    const bool live = r < static_cast<int32_t>(a.rows);  // uniform over the row's warps
     const uint4* xs = reinterpret_cast<const uint4*>(g.smem + static_cast<size_t>(slot) * p.stage_bytes +
-                                                     static_cast<size_t>(warp) * N * sizeof(T));
+                                                     static_cast<size_t>(wr) * N * sizeof(T)) + vb;
+    uint4 xv[VW];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k)
-      xv[k] = (live && lane + 32 * k < nv) ? xs[lane + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
+    for (int k = 0; k < VW; ++k)
+      xv[k] = (live && vb + lane + 32 * k < nv) ? xs[lane + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
     __syncwarp();
     if (lane == 0) mbar_arrive(&g.empty[slot]);  // the row is in registers: release the stage
-    if (++slot == p.stages) {
-      slot = 0;
+    slot += kRegGroups;
+    if (slot >= p.stages) {
+      slot -= p.stages;
       phase ^= 1u;
     }
     if (!live) continue;
-    float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
+    // Sums with four independent chains (the absent vectors are zeros and add nothing).
+    float2 s0 = make_float2(0.f, 0.f), s1 = s0, s2 = s0, s3 = s0;
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      s0 = add2(s0, add2(Elem<T>::unpack(xv[k].x), Elem<T>::unpack(xv[k].y)));
-      s1 = add2(s1, add2(Elem<T>::unpack(xv[k].z), Elem<T>::unpack(xv[k].w)));
+    for (int k = 0; k < VW; ++k) {
+      float2& sa = (k & 1) ? s1 : s0;
+      float2& sb = (k & 1) ? s3 : s2;
+      sa = add2(sa, add2(Elem<T>::unpack(xv[k].x), Elem<T>::unpack(xv[k].y)));
+      sb = add2(sb, add2(Elem<T>::unpack(xv[k].z), Elem<T>::unpack(xv[k].w)));
     }
-    const float2 st = add2(s0, s1);
-    const float mean = __fdiv_rn(group_sum<32>(st.x + st.y), fN);
+    const float2 st = add2(add2(s0, s1), add2(s2, s3));
+    float sum = group_sum<32>(st.x + st.y);
+    if constexpr (TPR > 1) {
+      if (lane == 0) xch[warp][0] = sum;
+      team_sync(team, 32 * TPR);
+      sum = xch[team * TPR][0] + xch[team * TPR + 1][0];
+    }
+    const float mean = __fdiv_rn(sum, fN);
     const float2 mean2 = splat2(mean);
-    float2 q0 = make_float2(0.f, 0.f), q1 = make_float2(0.f, 0.f);
+    float2 q0 = make_float2(0.f, 0.f), q1 = q0, q2 = q0, q3 = q0;
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      if (lane + 32 * k >= nv) continue;
+    for (int k = 0; k < VW; ++k) {
+      if (vb + lane + 32 * k >= nv) continue;
       const float2 c0 = sub2(Elem<T>::unpack(xv[k].x), mean2), c1 = sub2(Elem<T>::unpack(xv[k].y), mean2);
       const float2 c2 = sub2(Elem<T>::unpack(xv[k].z), mean2), c3 = sub2(Elem<T>::unpack(xv[k].w), mean2);
-      q0 = fma2(c0, c0, fma2(c2, c2, q0));
-      q1 = fma2(c1, c1, fma2(c3, c3, q1));
+      float2& qa = (k & 1) ? q1 : q0;
+      float2& qb = (k & 1) ? q3 : q2;
+      qa = fma2(c0, c0, fma2(c1, c1, qa));
+      qb = fma2(c2, c2, fma2(c3, c3, qb));
     }
-    const float2 qt = add2(q0, q1);
-    const float var = __fdiv_rn(group_sum<32>(qt.x + qt.y), fN);
+    const float2 qt = add2(add2(q0, q1), add2(q2, q3));
+    float qs = group_sum<32>(qt.x + qt.y);
+    if constexpr (TPR > 1) {
+      if (lane == 0) xch[warp][1] = qs;
+      team_sync(team, 32 * TPR);
+      qs = xch[team * TPR][1] + xch[team * TPR + 1][1];
+    }
+    const float var = __fdiv_rn(qs, fN);
     const float2 rstd2 = splat2(__fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, a.eps))));
-    uint4* yrow = reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N);
+    uint4* yrow = reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N) + vb;
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
+    for (int k = 0; k < VW; ++k) {
       const int v = lane + 32 * k;
-      if (v >= nv) continue;
+      if (vb + v >= nv) continue;
       const uint4 gv = gs[v];
       const uint4 bv = bs != nullptr ? bs[v] : make_uint4(0u, 0u, 0u, 0u);
       uint4 out;
@@ -974,15 +1003,17 @@ bool launch_layernorm_tma(const RowArgs& a, int dtype, cudaStream_t s) {
   const int xrow = a.N * 2;
   p.w_bytes = xrow;                           // the gain row
   p.b_bytes = a.bias != nullptr ? xrow : 0;   // the bias row, right after it
-#define FQ_LN(V)                                                                                             \
-  return dtype == DT_BF16                                                                                      \
-             ? launch_stream(rows_tma_ln_kernel<__nv_bfloat16, V>, kWideThreads, p, kWideWarps, xrow, 0, s, p.b_bytes) \
-             : launch_stream(rows_tma_ln_kernel<__half, V>, kWideThreads, p, kWideWarps, xrow, 0, s, p.b_bytes)
+#define FQ_LN_K(T, V, TPR)                                                                                 \
+  launch_stream(rows_tma_ln_kernel<T, V, TPR>, reg_threads((V) / (TPR)), p, kRegRows / (TPR), xrow, 0, s,     \
+                p.b_bytes, 220 * 1024, 96 * 1024, reg_groups((V) / (TPR)))
+#define FQ_LN(V)                                                                                      \
+  return dtype == DT_BF16 ? FQ_LN_K(__nv_bfloat16, V, (V) == 16 ? 2 : 1) : FQ_LN_K(__half, V, (V) == 16 ? 2 : 1)
   const int nv = a.N / 8;
   if (nv <= 4 * 32) FQ_LN(4);
   if (nv <= 8 * 32) FQ_LN(8);
   FQ_LN(16);
 #undef FQ_LN
+#undef FQ_LN_K
 }
 
 bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cudaStream_t s) {

@@ -435,6 +435,9 @@ LN_CASES = [
     (129, 2048, "fp16", True, False),
     (4097, 4096, "bf16", True, False),   # TMA-fed wide rows
     (4100, 1024, "fp16", False, False),  # TMA-fed, no bias
+    (4099, 3000, "bf16", True, False),   # TMA-fed, two warps per row, ragged last vectors
+    (4097, 2056, "fp16", False, False),  # two warps per row, the second holding one vector
+    (4096, 1536, "bf16", True, False),   # TMA-fed, one warp per row, partly filled slots
     (4096, 512, "bf16", True, False),    # many narrow rows: register-resident kernel
     (77, 100, "bf16", True, False),      # odd width: scalar
     (9, 5000, "bf16", True, False),      # wider than the register kernel: scalar
