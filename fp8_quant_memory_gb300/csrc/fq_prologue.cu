@@ -476,6 +476,12 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
   // k - depth, whose slot must not have been refilled yet.
   p.depth = 128 / SR;
   if (p.depth > p.stages) p.depth = p.stages;
+  // The two consumer halves take alternate stages and wait for stage k on its slot's full barrier by
+  // phase parity, which is only sound once the slot's previous use (stage k - S) has completed. With
+  // S even that stage was the same half's; with S odd it was the other half's, and it has completed
+  // if the producer, which issues stage j only after stage j - depth completed, keeps
+  // depth <= S - 2 (the half consumed stage k - 2, issued after stage k - 2 - depth completed).
+  if (p.stages % 2 != 0 && p.depth > p.stages - 2) p.depth = p.stages - 2;
   const size_t smem = prologue_smem_bytes(p.stages, p.stage_bytes);
   if (smem > 227 * 1024) return false;
 

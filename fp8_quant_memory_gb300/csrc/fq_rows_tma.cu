@@ -809,6 +809,85 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_wide_quant
   }
 }
 
+// ------------------------------------------------------------------ wide rows, RMSNorm, registers
+// RMSNorm forward for rows of 1024 <= N <= 4096 with the consumer layout of the LayerNorm kernel
+// below (consumer groups taking stages in turn, one CTA per SM, two warps per row above 2048
+// columns): the warp copies its part of the row into registers and releases the stage, adds its
+// squares in four chains, and writes y = dtype((x * rstd) * w) from the registers.
+template <typename T, int VPT, int TPR>
+__global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_reg_fwd_kernel(const StreamArgs p) {
+  constexpr int VW = VPT / TPR;
+  constexpr int kRegGroups = reg_groups(VW);
+  constexpr int kRegWarps = kRegRows * kRegGroups;
+  constexpr int SR = kRegRows / TPR;
+  static_assert(TPR == 1 || TPR == 2, "one or two warps per row");
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ float xch[kRegWarps];  // per warp: partial sum of squares
+  const Ring g = ring_setup(p, smem_raw, kRegRows, kRegWarps);
+  const RowArgs& a = p.a;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kRegWarps) {
+    if (lane == 0)
+      produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, SR, sizeof(T), 2, kRegGroups);
+    return;
+  }
+  const int grp = warp / kRegRows, wg = warp % kRegRows;
+  const int wr = wg / TPR, hh = wg % TPR;
+  const int team = warp / TPR;
+  const int N = a.N, nv = N >> 3;
+  const int vb = hh * 32 * VW;  // first vector of this warp's part of the row
+  const float fN = static_cast<float>(N);
+  const uint4* ws = reinterpret_cast<const uint4*>(g.w) + vb;
+  bool ok = mbar_wait(kWaitLimitNs, g.wbar, 0u);
+  int slot = grp;
+  uint32_t phase = 0;
+  for (;;) {
+    ok = ok && mbar_wait(kWaitLimitNs, &g.full[slot], phase);
+    if constexpr (TPR > 1) ok = team_all(ok, team, 32 * TPR);
+    if (!ok) {
+      flag_failure(p.status);
+      return;
+    }
+    const int32_t rs = g.stage_row[slot];
+    if (rs < 0) break;  // end marker
+    const int32_t r = rs + wr;
+    const bool live = r < static_cast<int32_t>(a.rows);  // uniform over the row's warps
+    const uint4* xs = reinterpret_cast<const uint4*>(g.smem + static_cast<size_t>(slot) * p.stage_bytes +
+                                                     static_cast<size_t>(wr) * N * sizeof(T)) + vb;
+    uint4 xv[VW];
+#pragma unroll
+    for (int k = 0; k < VW; ++k)
+      xv[k] = (live && vb + lane + 32 * k < nv) ? xs[lane + 32 * k] : make_uint4(0u, 0u, 0u, 0u);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&g.empty[slot]);  // the row is in registers: release the stage
+    slot += kRegGroups;
+    if (slot >= p.stages) {
+      slot -= p.stages;
+      phase ^= 1u;
+    }
+    if (!live) continue;
+    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int k = 0; k < VW; ++k) acc[k & 3] = sq_acc<T>(xv[k], acc[k & 3]);
+    const float2 sum = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
+    float ss = group_sum<32>(sum.x + sum.y);
+    if constexpr (TPR > 1) {
+      if (lane == 0) xch[warp] = ss;
+      team_sync(team, 32 * TPR);
+      ss = xch[team * TPR] + xch[team * TPR + 1];  // the same order in both warps
+    }
+    const float rstd = rstd_from_ss(ss, fN, a.eps);
+    if (a.rstd != nullptr && hh == 0 && lane == 0) a.rstd[r] = rstd;
+    const float2 rstd2 = splat2(rstd);
+    uint4* yrow = reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N) + vb;
+#pragma unroll
+    for (int k = 0; k < VW; ++k) {
+      const int v = lane + 32 * k;
+      if (vb + v < nv) st_stream16(yrow + v, norm8<T>(xv[k], ws[v], rstd2));
+    }
+  }
+}
+
 // ------------------------------------------------------------------ wide rows, LayerNorm
 // LayerNorm forward ("ledger.py" (Ch.13 ledger), layer_norm) for rows of 1024 <= N <= 4096, with the
 // consumer layout of the FP8 kernel above: consumer groups of four warps take the stages in turn (one
@@ -930,11 +1009,17 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_ln_kernel(
 
 // ---------------------------------------------------------------------------------- host side
 // `budget`: shared-memory bytes for the ring (0: two CTAs per SM when stages are small, else one);
-// `inflight`: bytes the producer keeps in flight.
+// `inflight`: bytes the producer keeps in flight; `groups`: consumer groups that take the stages in
+// turn (stage k goes to group k % groups).
+//
+// With several groups the ring holds a multiple of `groups` stages, so that a slot always belongs to
+// the same group. A consumer waits for stage k on its slot's full barrier by phase parity, which
+// cannot tell the phase of stage k from that of stage k - 2S: the wait is only sound if the slot's
+// previous use, stage k - S, has completed. The group consumed stage k - S itself, in order, before
+// it waits for stage k, so it has.
 template <typename K>
 bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_bytes, int tab_row_bytes,
-                   cudaStream_t s, int extra_bytes = 0, int budget = 0, int inflight = 48 * 1024,
-                   int min_stages = 2) {
+                   cudaStream_t s, int extra_bytes = 0, int budget = 0, int inflight = 48 * 1024, int groups = 1) {
   const RowArgs& a = p.a;
   p.status = device_status_ptr();
   p.tab_block = ((stage_rows * tab_row_bytes) + 127) & ~127;
@@ -944,8 +1029,10 @@ bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_
   // still fits three times); as many stages as fit, at most 8.
   if (budget == 0) budget = p.stage_bytes <= 36 * 1024 ? 110 * 1024 : 220 * 1024;
   p.stages = (budget - static_cast<int>(ring_bytes(0, 0, p.w_bytes)) - extra_bytes - 8) / (p.stage_bytes + 20);
-  if (p.stages > 8) p.stages = 8;
-  if (p.stages < min_stages) return false;
+  const int cap = groups > 1 ? 12 : 8;
+  if (p.stages > cap) p.stages = cap;
+  p.stages -= p.stages % groups;
+  if (p.stages < 2 || p.stages < groups) return false;
   // Keep about `inflight` bytes in flight per CTA (at least two stages), never more than the ring.
   p.depth = (inflight + p.stage_bytes - 1) / p.stage_bytes;
   if (p.depth < 2) p.depth = 2;
@@ -1095,6 +1182,20 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
     p.a.R = 0;
     const int xrow = a.N * 2;
     p.w_bytes = xrow;  // N % 8 == 0 and a 16-byte aligned w: a legal bulk copy
+    const char* sel = getenv("FQ_ROWS_KERNEL");
+    if (a.N <= 4096 && !(sel != nullptr && std::string(sel) == "staged")) {
+#define FQ_RF_K(T, V, TPR)                                                                                 \
+  launch_stream(rows_tma_reg_fwd_kernel<T, V, TPR>, reg_threads((V) / (TPR)), p, kRegRows / (TPR), xrow, 0, s, \
+                0, 220 * 1024, 96 * 1024, reg_groups((V) / (TPR)))
+#define FQ_RF(V)                                                                                                  \
+  return dtype == DT_BF16 ? FQ_RF_K(__nv_bfloat16, V, (V) == 16 ? 2 : 1) : FQ_RF_K(__half, V, (V) == 16 ? 2 : 1)
+      const int nv = a.N / 8;
+      if (nv <= 4 * 32) FQ_RF(4);
+      if (nv <= 8 * 32) FQ_RF(8);
+      FQ_RF(16);
+#undef FQ_RF
+#undef FQ_RF_K
+    }
     if (dtype == DT_BF16)
       return launch_stream(rows_tma_wide_fwd_kernel<__nv_bfloat16>, kWideThreads, p, kWideWarps, xrow, 0, s);
     return launch_stream(rows_tma_wide_fwd_kernel<__half>, kWideThreads, p, kWideWarps, xrow, 0, s);

@@ -382,7 +382,8 @@ RSTD_CASES = [
     (300, 256, "bf16", False),     # generic narrow rows
     (129, 2048, "fp16", False),    # generic wide rows
     (4100, 512, "bf16", False),    # TMA narrow rows
-    (4097, 4096, "bf16", False),   # TMA wide rows; TMA-fed backward
+    (4097, 4096, "bf16", False),   # TMA wide rows (two warps per row); TMA-fed backward
+    (4099, 1536, "fp16", False),   # TMA wide rows, one warp per row
     (77, 1024, "bf16", False),     # global-load backward
     (45, 100, "bf16", False),      # odd width: scalar forward and backward
     (60, 512, "bf16", True),       # misaligned: scalar
@@ -606,9 +607,10 @@ def _rows_kernel(monkeypatch, kernel):
         monkeypatch.delenv("FQ_ROWS_KERNEL", raising=False)
 
 
-@pytest.mark.parametrize("kernel", ["tma", "generic"])
+@pytest.mark.parametrize("kernel", ["tma", "staged", "generic"])
 @pytest.mark.parametrize("case", [(4099, 256, "bf16"), (4500, 1024, "bf16"), (4097, 4096, "fp16"), (5000, 64, "fp16"),
-                                  (4608, 2048, "bf16"), (4103, 8192, "bf16"), (4096, 1032, "fp16")],
+                                  (4608, 2048, "bf16"), (4103, 8192, "bf16"), (4096, 1032, "fp16"),
+                                  (4097, 3000, "bf16"), (4098, 2056, "fp16")],
                          ids=lambda c: "M%d-N%d-%s" % c)
 def test_rmsnorm_fwd_stream_kernel(orc, cuda_ok, monkeypatch, case, kernel):
     _rows_kernel(monkeypatch, kernel)
