@@ -13,6 +13,12 @@ graphs and replayed, CUDA events on the launching stream, a barrier + synchroniz
 max over ranks. N > 1 (torchrun, one process per GPU): every rank runs its own batch (weak
 scaling, no data-path collective; the process group only carries the barrier and the max).
 
+Beside the number (rank 0): `roofline.size_matched_copy`, the same byte counts streamed by a copy
+kernel with the same work distribution and no arithmetic (`fq.stream_floor`), and the prologue's
+fraction of it; `cold_launch`, one launch after 256 MB of writes have evicted L2; `e2e`, the same
+metric through the public API with host buffers; `cpu_baseline` (one core) and
+`cpu_baseline_all_cores` (one token slice per core), the oracle on bounded samples.
+
 --impl reference times the oracle (plain single-threaded C++) on this machine's host cores over
 bounded samples of the same workload.
 """
@@ -195,6 +201,52 @@ class PrologueDesignCase(PrologueCase):
         s = self.sets[i % len(self.sets)]
         self.fq.qk_norm_rope_quant_blocks(s["qk"], s["wq"], s["wk"], s["cos"], s["sin"], self.Hq, self.Hk, self.rpb,
                                           q_out=s["q"], scale=s["scale"])
+
+
+class StreamFloorCase(Case):
+    """The size-matched streaming floor (`fq.stream_floor`): the prologue's x bytes read and codes
+    bytes written, no arithmetic, the same chunked work distribution and launch attributes."""
+
+    def __init__(self, dev, rows=T_TOK * (HQ + HK), n_sets=8):
+        import torch
+
+        import fp8_quant_memory_gb300 as fq
+
+        self.fq = fq
+        n16 = rows * D * 2 // 16
+        self.name = f"size-matched streaming floor: {n16 * 16 / 1e6:.2f} MB read, {n16 * 8 / 1e6:.2f} MB written"
+        self.sets = []
+        for i in range(n_sets):
+            inp = torch.randint(0, 256, (n16 * 16,), dtype=torch.uint8, device=dev)
+            self.sets.append({"in": inp, "out": torch.empty(n16 * 8, dtype=torch.uint8, device=dev)})
+        self._bytes = n16 * 24
+
+    def bytes_per_step(self):
+        return self._bytes
+
+    def launch(self, i):
+        s = self.sets[i % len(self.sets)]
+        self.fq.stream_floor(s["in"], out=s["out"])
+
+
+def cold_launch_us(case: Case, stream, runs: int = 5) -> dict:
+    """One launch right after 256 MB of writes have evicted the 129 MB L2, timed alone with events."""
+    import torch
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=stream.device)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(runs):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            case.launch(i)
+            b.record(stream)
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b) * 1e3)
+    times.sort()
+    return {"us_median": round(times[len(times) // 2], 3), "runs": runs,
+            "flush": "256 MB written before each launch (L2 is 129 MB)"}
 
 
 class RmsnormFwdCase(Case):
@@ -562,6 +614,41 @@ def cpu_oracle_sample(budget_s: float = 12.0):
             "sample": f"{reps} full batches of {T_TOK} tokens x {HQ + HK} heads x {D} in {el:.1f} s"}
 
 
+def cpu_oracle_all_cores(budget_s: float = 10.0):
+    """The same oracle, unchanged, on every host core: the 4096 tokens split into one slice per core,
+    the slices run on a thread pool (the oracle is a C library called through ctypes, which releases
+    the interpreter lock, and it keeps no global state). Whole batches repeated until the budget is
+    spent; GB/s of the same ledger."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    from fp8_quant_memory_gb300 import ledger
+    from fp8_quant_memory_gb300 import workloads as wl
+
+    d = wl.qk_inputs(T_TOK, HQ, HK, D, "bf16", "fp32", seed=20261202 + 2, std=2.0)
+    oracle.lib()
+    cores = max(1, os.cpu_count() or 1)
+    bounds = [(T_TOK * i // cores, T_TOK * (i + 1) // cores) for i in range(cores)]
+    slices = [{k: d[k][a:b].contiguous() for k in ("qk", "cos", "sin")} for a, b in bounds if b > a]
+
+    def run(sl):
+        oracle.qk_norm_rope_quant(sl["qk"], d["wq"], d["wk"], sl["cos"], sl["sin"], HQ, HK)
+
+    bytes_per = ledger.qk_prologue_bytes(T_TOK, HQ, HK, D)
+    reps = 0
+    with ThreadPoolExecutor(len(slices)) as ex:
+        t0 = time.perf_counter()
+        while True:
+            list(ex.map(run, slices))
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+    return {"value": round(bytes_per * reps / el / 1e9, 4), "unit": UNIT, "cores": len(slices), "kind": "oracle",
+            "sample": f"{reps} full batches of {T_TOK} tokens x {HQ + HK} heads x {D}, one token slice per core, "
+                      f"in {el:.1f} s"}
+
+
 def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
@@ -717,6 +804,16 @@ def main():
         "device_status": status,
     }
     if rank == 0:
+        # Context for the fraction: the size-matched streaming floor and one cold launch.
+        fl = StreamFloorCase(dev)
+        floor = time_secondary(fl, 2048, 64, stream, peak)
+        del fl
+        torch.cuda.empty_cache()
+        line["roofline"]["size_matched_copy"] = {"us_per_launch": floor["us_per_step"], "GB/s": floor["GB/s"],
+                                                 "bytes": floor["bytes_per_step"],
+                                                 "kernel": "stream_floor_kernel (fq_stream_floor)"}
+        line["roofline"]["frac_of_size_matched_copy"] = round(achieved / floor["GB/s"], 4)
+        line["cold_launch"] = cold_launch_us(case, stream)
         line["e2e"] = e2e_prologue(case, min(args.steps, 200), stream)
         if not args.no_extras:
             extras = []
@@ -734,6 +831,7 @@ def main():
             line["also"] = extras
         if world == 1 and not args.no_cpu:
             line["cpu_baseline"] = cpu_oracle_sample()
+            line["cpu_baseline_all_cores"] = cpu_oracle_all_cores()
         print(json.dumps(line), flush=True)
     if _PG is not None:
         import torch.distributed as dist

@@ -25,7 +25,7 @@ from . import _capi
 __all__ = ["layernorm_fwd", "rmsnorm_fwd", "rmsnorm_fwd_rstd", "rmsnorm_bwd_rstd", "rmsnorm_rope", "rmsnorm_rope_quant", "rmsnorm_rope_quant_groups", "qk_norm_rope_quant", "qk_norm_rope_quant_blocks",
            "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_bytes", "rmsnorm", "RMSNormFunction", "device_status", "check_bounded_wait",
-           "FqError"]
+           "stream_floor", "FqError"]
 
 FqError = _capi.FqError
 
@@ -269,6 +269,24 @@ def check_bounded_wait(limit_ms: int = 50, device=None) -> int:
     device_status(clear=True, device=dev)
     _capi.call("fq_check_bounded_wait", ctypes.c_uint(limit_ms), _stream(dev))
     return device_status(clear=True, device=dev)
+
+
+def stream_floor(inp: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """The size-matched streaming floor (a measurement aid, not a step of the method): `inp` is a
+    contiguous device tensor whose byte size is a multiple of 16; returns (or fills) a uint8 tensor of
+    half that size whose 8-byte word i is the XOR of the two 8-byte halves of 16-byte vector i."""
+    if not (inp.is_cuda and inp.is_contiguous()):
+        raise ValueError("stream_floor: inp must be a contiguous CUDA tensor")
+    nbytes = inp.numel() * inp.element_size()
+    if nbytes % 16:
+        raise ValueError("stream_floor: the input size must be a multiple of 16 bytes")
+    n16 = nbytes // 16
+    if out is None:
+        out = torch.empty(n16 * 8, dtype=torch.uint8, device=inp.device)
+    elif not (out.is_cuda and out.is_contiguous() and out.numel() * out.element_size() == n16 * 8):
+        raise ValueError("stream_floor: out must be a contiguous CUDA tensor of half the input's bytes")
+    _capi.call("fq_stream_floor", _ptr(inp), _ptr(out), n16, _stream(inp.device))
+    return out
 
 
 class RMSNormFunction(torch.autograd.Function):

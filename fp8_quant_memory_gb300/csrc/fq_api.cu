@@ -151,6 +151,19 @@ int fq_check_bounded_wait(unsigned int limit_ms, cudaStream_t stream) {
   return ok();
 }
 
+int fq_stream_floor(const void* in, void* out, int64_t n16, cudaStream_t stream) {
+  if (n16 < 0 || n16 > (static_cast<int64_t>(1) << 40))
+    return fail(FQ_ERR_INVALID_ARG, "fq_stream_floor: need 0 <= n16 <= 2^40, got %lld", static_cast<long long>(n16));
+  if (n16 == 0) return ok();
+  if (in == nullptr || out == nullptr) return fail(FQ_ERR_INVALID_ARG, "fq_stream_floor: null pointer");
+  if (!aligned(in, 16) || !aligned(out, 8))
+    return fail(FQ_ERR_INVALID_ARG, "fq_stream_floor: in must be 16-byte and out 8-byte aligned");
+  cudaGetLastError();
+  const cudaError_t e = fq::launch_stream_floor(in, out, n16, stream);
+  if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "fq_stream_floor: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 int fq_rmsnorm_fwd_rstd(const void* x, const void* w, void* y, float* rstd, int64_t M, int64_t N, int dtype,
                         float eps, cudaStream_t stream) {
   const char* fn = rstd != nullptr ? "fq_rmsnorm_fwd_rstd" : "fq_rmsnorm_fwd";

@@ -100,6 +100,9 @@ unsigned int* device_status_ptr();
 // Launches the bounded-wait probe (one block, one wait that can only give up after limit_ms).
 cudaError_t launch_wait_probe(unsigned int limit_ms, cudaStream_t s);
 
+// The size-matched streaming floor (fq_floor.cu): n16 16-byte vectors in, 8 bytes per vector out.
+cudaError_t launch_stream_floor(const void* in, void* out, int64_t n16, cudaStream_t s);
+
 int sm_count();
 
 // Raises `kernel`'s dynamic shared-memory limit to at least `bytes` on the current device. The limit

@@ -72,6 +72,18 @@ int fq_device_status(unsigned int* word, int clear, cudaStream_t stream);
  * FQ_ERR_CUDA. The tutorial pages have no counterpart (they have no pipelined kernel). */
 int fq_check_bounded_wait(unsigned int limit_ms, cudaStream_t stream);
 
+/* Measurement aid, not a step of the method: the size-matched streaming floor. Reads n16 16-byte
+ * vectors from `in` (device, 16-byte aligned) once each and writes 8 bytes per vector to `out`
+ * (device, 8-byte aligned, n16 * 8 bytes): out[i] = (low 8 bytes of in[i]) XOR (high 8 bytes of
+ * in[i]), i.e. 32-bit word k of out[i] is word k XOR word k + 2 of in[i]. That is the traffic shape of the
+ * QK-norm prologue ("case_norm_rope_quant.py" (Ch.28), `Design.payload_bytes`: 2 bytes read and 1
+ * written per element) with no arithmetic, the same work distribution (cluster launch control over
+ * 512-vector chunks) and the same programmatic dependent launch, so its time at the prologue's byte
+ * counts is what a streaming kernel of that size reaches on the GPU. 0 <= n16 <= 2^40 (n16 = 0 is a
+ * no-op). Caller-owned memory, asynchronous on `stream`. Returns FQ_OK, FQ_ERR_INVALID_ARG (null,
+ * misaligned, out of range) or FQ_ERR_CUDA. */
+int fq_stream_floor(const void* in, void* out, int64_t n16, cudaStream_t stream);
+
 /*
  * RMSNorm forward ("rmsnorm_tl.py", _rmsnorm_fwd):
  *   rstd_i = 1 / sqrt(sum_j x_ij^2 / N + eps)   (fp32)

@@ -145,3 +145,14 @@ def test_binding_rejects_host_tensors():
     x = torch.zeros(4, 8, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         fq.rmsnorm_fwd(x, torch.ones(8, dtype=torch.bfloat16))
+
+
+def test_stream_floor_rules(lib):
+    p, odd = ctypes.c_void_p(16), ctypes.c_void_p(24)
+    assert _rc(lib, "fq_stream_floor", p, p, 0, NULL)[0] == 0          # nothing to stream: no-op
+    rc, msg = _rc(lib, "fq_stream_floor", NULL, p, 4, NULL)
+    assert rc == 1 and "null" in msg
+    assert _rc(lib, "fq_stream_floor", p, p, -1, NULL)[0] == 1
+    rc, msg = _rc(lib, "fq_stream_floor", odd, p, 4, NULL)             # input not 16-byte aligned
+    assert rc == 1 and "aligned" in msg
+    assert _rc(lib, "fq_stream_floor", p, ctypes.c_void_p(20), 4, NULL)[0] == 1

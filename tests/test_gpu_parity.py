@@ -637,3 +637,17 @@ def test_rmsnorm_rope_stream_kernel(orc, cuda_ok, monkeypatch, case, kernel):
     assert_rope_close(y, orc.rmsnorm_rope(d["x"], d["w"], d["cos"], d["sin"]),
                       orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
     assert fq.device_status(clear=True) == 0
+
+
+# ----------------------------------------------------------------------------------- streaming floor
+@pytest.mark.parametrize("n16", [1, 511, 513, 5000, 163840 * 16])
+def test_stream_floor_output(cuda_ok, n16):
+    """The size-matched copy the benchmark times beside the prologue does exactly its stated work:
+    every input vector read once, out word k = in word k XOR in word k + 2 (ragged last chunk too)."""
+    g = torch.Generator().manual_seed(n16)
+    x = torch.randint(-2 ** 31, 2 ** 31 - 1, (n16, 4), dtype=torch.int32, generator=g)
+    out = fq.stream_floor(x.cuda())
+    torch.cuda.synchronize()
+    expect = torch.stack([x[:, 0] ^ x[:, 2], x[:, 1] ^ x[:, 3]], 1)
+    assert torch.equal(out.cpu().view(torch.int32).view(n16, 2), expect)
+    assert fq.device_status(clear=True) == 0
