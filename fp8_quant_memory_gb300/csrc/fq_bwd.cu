@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_stage1_kernel(const BwdArgs a
     }
 #pragma unroll
     for (int b = 0; b < RB; ++b) {
-      const float rstd = (a.rstd_in != nullptr) ? (rv[b] ? a.rstd_in[row[b]] : 1.f) : rstd_from_ss(ss[b], fN, a.eps);
+      const float rstd = (a.rstd_in != nullptr) ? (rv[b] ? a.rstd_in[row[b]] : 1.f) : rstd_approx(ss[b], fN, a.eps);
       const float c = __fdiv_rn(__fmul_rn(sg[b], rstd), fN);
       const float2 rstd2 = splat2(rstd), c2 = splat2(c);
 #pragma unroll
@@ -281,7 +281,7 @@ __global__ void __launch_bounds__(kThreads) bwd_stage1_scalar_kernel(const BwdAr
       sg += red[w][1];
     }
     __syncthreads();
-    const float rstd = (a.rstd_in != nullptr) ? a.rstd_in[r] : rstd_from_ss(ss, static_cast<float>(N), a.eps);
+    const float rstd = (a.rstd_in != nullptr) ? a.rstd_in[r] : rstd_approx(ss, static_cast<float>(N), a.eps);
     const float c = __fdiv_rn(__fmul_rn(sg, rstd), static_cast<float>(N));
     for (int j = tid; j < N; j += kThreads) {
       const float gf = Elem<T>::load1(a.g, r * N + j);
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) bwd_stage1_stream_kernel(co
       ss += rb[2 * w];
       sg += rb[2 * w + 1];
     }
-    const float rstd = SAVED ? a.rstd_in[c0 + k] : rstd_from_ss(ss, fN, a.eps);
+    const float rstd = SAVED ? a.rstd_in[c0 + k] : rstd_approx(ss, fN, a.eps);
     const float c = __fdiv_rn(__fmul_rn(sg, rstd), fN);
     const float2 rstd2 = splat2(rstd), c2 = splat2(c);
     T* dxrow = static_cast<T*>(a.dx) + (c0 + k) * N;

@@ -210,8 +210,18 @@ __device__ __forceinline__ float absmax4(float m, float2 a, float2 b) {
 }
 
 // rstd from the row's sum of squares: 1/sqrt(ss/N + eps), every step correctly rounded in fp32.
+// Used where an FP8 code or a saved rstd depends on it.
 __device__ __forceinline__ float rstd_from_ss(float ss, float n, float eps) {
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n), eps)));
+}
+
+// The same with the hardware reciprocal square root and the approximate quotient (each within 2 ulp
+// for the normal range), the pages' rsqrt read as the hardware instruction: a few fp32 ulps from
+// rstd_from_ss, far inside the storage-dtype tolerance of the outputs that use it (y of RMSNorm +
+// RoPE without quantisation, dx and dw of the backward). About thirty instructions shorter, which
+// counts on narrow rows (a 192-element row is 24 elements per lane).
+__device__ __forceinline__ float rstd_approx(float ss, float n, float eps) {
+  return rsqrtf(__fadd_rn(__fdividef(ss, n), eps));
 }
 
 }  // namespace fq

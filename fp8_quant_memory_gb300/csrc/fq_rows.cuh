@@ -113,7 +113,7 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
   }
   const float2 acc = add2(acc0, acc1);
   const float ss = group_sum<LPR>(acc.x + acc.y);
-  const float rstd = rstd_from_ss(ss, fN, a.eps);
+  const float rstd = MODE == MODE_ROPE ? rstd_approx(ss, fN, a.eps) : rstd_from_ss(ss, fN, a.eps);
   if (MODE == MODE_FWD && a.rstd != nullptr && rv && lane == 0) a.rstd[r] = rstd;
   const float2 rstd2 = splat2(rstd);
   const T* wrow = static_cast<const T*>((MODE == MODE_QK && h >= a.Hq) ? a.wk : a.wq);

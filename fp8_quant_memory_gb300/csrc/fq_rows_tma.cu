@@ -416,7 +416,8 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_rope_kernel(const 
         acc1 = fma2(f3, f3, acc1);
       }
       const float2 acc = add2(acc0, acc1);
-      const float2 rstd2 = splat2(rstd_from_ss(group_sum<32>(acc.x + acc.y), fN, a.eps));
+      const float ssr = group_sum<32>(acc.x + acc.y);
+      const float2 rstd2 = splat2(QUANT ? rstd_from_ss(ssr, fN, a.eps) : rstd_approx(ssr, fN, a.eps));
       T* yrow = a.y != nullptr ? static_cast<T*>(a.y) + static_cast<int64_t>(r) * N : nullptr;
       float amax = 0.f;
       if (grouped) {

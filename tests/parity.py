@@ -6,7 +6,8 @@
   (assert_rope_close: the definition rounds the normalised row before rotating it)
 - fp32 scales:  relative difference <= 1e-5
 - fp8 codes:    identical, or one e4m3 step apart on at most 0.1% of the elements
-- dw (fp32 sums): |gpu - ref| <= 1e-3 * max(|ref|, rms(ref)); bf16/fp16 dw within one ulp
+- dw (fp32 sums): |gpu - ref| <= 1e-3 * max(|ref|, rms(ref)); bf16/fp16 dw within one ulp, or
+  within 1e-3 * rms(ref) where the column's sum nearly cancels
 """
 from __future__ import annotations
 
@@ -94,10 +95,19 @@ def assert_dw_close(gpu_f32: torch.Tensor, ref_f32: torch.Tensor, rel: float = 1
     assert not bool(bad.any()), f"dw_f32: {int(bad.sum())} columns outside 1e-3 * max(|ref|, rms)"
 
 
-def assert_within_one_ulp(gpu: torch.Tensor, ref: torch.Tensor, what: str = "dw"):
-    a = gpu.detach().cpu().view(torch.int16).to(torch.int32)
+def assert_within_one_ulp(gpu: torch.Tensor, ref: torch.Tensor, what: str = "dw", rms_floor: float = 1e-3):
+    """bf16/fp16 dw within one ulp of the oracle's, or within rms_floor * rms(ref) of it. A column
+    whose sum over rows nearly cancels (|dw| far below the rms of dw) moves by several of its own ulps
+    when rstd moves by one fp32 ulp -- which any fp32 order of the sum of squares other than the
+    oracle's does -- so there the fp32 rule's rms floor applies (tests/test_parity_rules.py pins this
+    on the oracle alone)."""
+    gc = gpu.detach().cpu()
+    a = gc.view(torch.int16).to(torch.int32)
     b = ref.view(torch.int16).to(torch.int32)
     # same-sign patterns are ordered like integers; treat +-0 as equal
     ord_a = torch.where(a < 0, -(a & 0x7FFF), a)
     ord_b = torch.where(b < 0, -(b & 0x7FFF), b)
-    assert int((ord_a - ord_b).abs().max()) <= 1, f"{what}: more than one ulp apart"
+    rb = ref.double()
+    floor = rms_floor * float(rb.pow(2).mean().sqrt()) if rb.numel() else 0.0
+    bad = ((ord_a - ord_b).abs() > 1) & ((gc.double() - rb).abs() > floor)
+    assert not bool(bad.any()), f"{what}: {int(bad.sum())} columns more than one ulp apart and above the rms floor"

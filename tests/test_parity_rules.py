@@ -50,3 +50,26 @@ def test_rope_rule_rejects_a_wrong_rotation(orc, mistake):
     y = _emulate(d, **{mistake: True})
     with pytest.raises(AssertionError):
         assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
+
+
+def test_dw_one_ulp_rule_needs_the_rms_floor(orc):
+    """The dtype dw of a column whose sum over rows nearly cancels moves by more than one of its own
+    ulps when rstd moves by a single fp32 ulp (a different fp32 order of the sum of squares does
+    that), so 'within one ulp' alone cannot hold; with the rms floor of the fp32 rule it does, and a
+    wrong dw (a dropped row) is still rejected."""
+    from parity import assert_within_one_ulp
+
+    d = wl.rmsnorm_inputs(513, 4096, "fp16", seed=580 + 513)
+    _, r = orc.rmsnorm_fwd_rstd(d["x"], d["w"])
+    _, dw0, dw32 = orc.rmsnorm_bwd_rstd(d["x"], d["w"], d["g"], r)
+    r1 = torch.from_numpy(np.nextafter(r.numpy(), np.float32(np.inf)).astype(np.float32))
+    _, dw1, _ = orc.rmsnorm_bwd_rstd(d["x"], d["w"], d["g"], r1)
+    a, b = dw1.view(torch.int16).to(torch.int32), dw0.view(torch.int16).to(torch.int32)
+    ulps = (torch.where(a < 0, -(a & 0x7FFF), a) - torch.where(b < 0, -(b & 0x7FFF), b)).abs()
+    assert int(ulps.max()) > 1  # one fp32 ulp of rstd: several fp16 ulps on a near-zero column
+    j = int(ulps.argmax())
+    assert abs(float(dw32[j])) < 1e-3 * float(dw32.pow(2).mean().sqrt())  # ... which is such a column
+    assert_within_one_ulp(dw1, dw0)  # the rule with the rms floor accepts it
+    _, dw_bad, _ = orc.rmsnorm_bwd_rstd(d["x"][1:], d["w"], d["g"][1:], r[1:])
+    with pytest.raises(AssertionError):
+        assert_within_one_ulp(dw_bad, dw0)
