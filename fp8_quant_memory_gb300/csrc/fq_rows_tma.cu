@@ -1,6 +1,7 @@
-// fq_rows_tma.cu -- TMA-fed persistent kernels for RMSNorm forward and RMSNorm + NeoX partial RoPE
-// over contiguous rows ("rmsnorm_tl.py" (Ch.17), _rmsnorm_fwd; "rmsnorm_rope_quant.py" (Ch.13
-// fusion), rms_norm_rope_fused / torch_reference_fused).
+// fq_rows_tma.cu -- TMA-fed persistent kernels for RMSNorm forward, RMSNorm + NeoX partial RoPE
+// (+ FP8) and LayerNorm forward over contiguous rows ("rmsnorm_tl.py" (Ch.17), _rmsnorm_fwd;
+// "rmsnorm_rope_quant.py" (Ch.13 fusion), rms_norm_rope_fused / rms_norm_rope_quant_fused /
+// torch_reference_fused; "ledger.py" (Ch.13 ledger), layer_norm).
 //
 // The rows are cut into stages of SR consecutive rows, one per CTA of the grid. The CTAs that are
 // resident take over the stages of CTAs that have not started yet through cluster launch control (a
@@ -13,10 +14,13 @@
 // the stage:
 //   - narrow rows: eight consumer warps with the lane-group layout and arithmetic of the generic row
 //     kernel (fq_rows.cuh), one row per lane group per stage, tables read from the stage;
-//   - wide rows (RMSNorm forward, N >= 1024): four consumer warps, one row per warp per stage, two
-//     passes over the staged row (sum of squares, then normalise and store), each unrolled four
-//     16-byte vectors deep; the weight row is copied into shared memory once per CTA. Two CTAs
-//     share an SM, so a stage is four rows and the ring fills and drains in small steps.
+//   - wide rows, shared memory (RMSNorm forward beyond 4096 columns, RMSNorm + RoPE, the quantising
+//     shapes the register kernels do not take): four consumer warps, one row per warp per stage,
+//     two or three passes over the staged row; the weight row is copied into shared memory once per
+//     CTA. Two CTAs share an SM, so a stage is four rows and the ring fills and drains in small steps;
+//   - wide rows, registers (RMSNorm forward, RMSNorm + RoPE + FP8 and LayerNorm on rows of 1024 to
+//     4096): one CTA per SM, three consumer groups of four warps taking the stages in turn, one or
+//     two warps per row; a warp copies its row into registers and releases the stage at once.
 // y is written with 16-byte evict-first stores. x and the tables are read from HBM exactly once.
 #include <cstdlib>
 #include <string>
