@@ -782,6 +782,9 @@ def main():
 
     per_launch_us = ms * 1e3 / args.steps
     bytes_step = case.bytes_per_step()
+    from fp8_quant_memory_gb300 import ledger as _ledger
+
+    ledger_flops = _ledger.qk_prologue_flops(T_TOK, HQ, HK, D)
     value = job_throughput_gbs(bytes_step, args.steps, ms, world)
     achieved = bytes_step / (per_launch_us * 1e-6) / 1e9
     peak, peak_kind = peaks()
@@ -799,6 +802,8 @@ def main():
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": profiled_traffic(), "kernel": "prologue_tma_kernel<bf16,float,32>",
                      "us_per_launch": round(per_launch_us, 3)},
+        "rows_per_s": round(T_TOK * (HQ + HK) * args.steps * world / (ms * 1e-3), 1),
+        "flops_per_step": ledger_flops, "arithmetic_intensity_flop_per_byte": round(ledger_flops / bytes_step, 3),
         "gpu_launches": args.steps * case.kernels_per_step,
         "clocks": clocks,
         "device_status": status,

@@ -24,6 +24,15 @@ def qk_prologue_bytes(T: int, Hq: int, Hk: int, D: int, R: int | None = None, dt
     return x + q + scale + table + weights
 
 
+def qk_prologue_flops(T: int, Hq: int, Hk: int, D: int) -> int:
+    """The Ch.28 page's FLOP ledger of the prologue ("case_norm_rope_quant.py", ``Design.flops``): per
+    row of head_dim D, 2D for the sum of squares, 3 for rsqrt and the two scalings, 2D for the
+    weight multiply, 6 per RoPE pair (D/2 pairs: four products, two sums), D for the absmax and 2D
+    for scale-and-convert. Reported beside the byte ledger; bytes are what bind."""
+    rows = T * (Hq + Hk)
+    return rows * (2 * D + 3 + 2 * D + 6 * (D // 2) + D + 2 * D)
+
+
 def rope_quant_bytes(M: int, N: int, R: int, dtype: str = "bf16", table_dtype: str = "bf16",
                      write_y: bool = True, group_size: int | None = None) -> int:
     """x, w, cos/sin read; y (optional), codes and the fp32 scales written (one per row, or one per

@@ -51,3 +51,14 @@ def test_page_norm_rope_quant_plans_at_the_page_shape():
     assert round(ledger.page_fused_norm_rope_quant_bytes(4096, 4096, 128) / 1e6, 2) == 51.40
     assert ledger.page_fused_norm_rope_quant_bytes(4096, 4096, 128) == ledger.rope_quant_bytes(
         4096, 4096, 128, "bf16", "bf16", write_y=False)
+
+
+def test_prologue_flops_match_the_pages_ledger():
+    """10 * head_dim + 3 FLOP per row: 210.2 MFLOP for the 4096-token prologue and 3027 MFLOP for the
+    32768-token one, as the Ch.28 page's ledger gives for these shapes (about 3.2 FLOP per byte)."""
+    from fp8_quant_memory_gb300 import ledger
+
+    assert ledger.qk_prologue_flops(4096, 32, 8, 128) == 4096 * 40 * 1283 == 210206720
+    assert ledger.qk_prologue_flops(32768, 64, 8, 128) == 3026976768
+    ai = ledger.qk_prologue_flops(4096, 32, 8, 128) / ledger.qk_prologue_bytes(4096, 32, 8, 128)
+    assert 3.1 < ai < 3.3
