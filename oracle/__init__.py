@@ -199,6 +199,32 @@ def qk_norm_rope_quant(qk, wq, wk, cos, sin, hq: int, hk: int, eps: float = 1e-6
     return q, scale
 
 
+def qk_norm_rope_quant_rounded(qk, wq, wk, cos, sin, hq: int, hk: int, eps: float = 1e-6,
+                               fp8_max: float = 448.0):
+    """The prologue under the other reading of its cast points: the fusion page's definition
+    ("rmsnorm_rope_quant.py", torch_reference_fused) rounds the normalised row and the rotated row to
+    the storage dtype, where the prologue statement ("case_norm_rope_quant.py", module docstring)
+    names no intermediates and qk_norm_rope_quant keeps fp32 from load to quantiser. Composed from
+    rmsnorm_rope_quant: every (token, head) row with its head's weight (wq for the first hq heads,
+    wk for the rest) and its token's cos/sin row. qk: contiguous [T, hq+hk, D]. Returns (q, scale)."""
+    T, H, D = qk.shape
+    if H != hq + hk or not qk.is_contiguous():
+        raise ValueError("qk must be a contiguous [T, hq+hk, D]")
+    q = torch.empty((T, H, D), dtype=torch.uint8)
+    scale = torch.empty((T, H), dtype=torch.float32)
+    for h0, h1, w in ((0, hq, wq), (hq, H, wk)):
+        nh = h1 - h0
+        if nh == 0:
+            continue
+        x = qk[:, h0:h1].reshape(T * nh, D).contiguous()
+        c = cos.repeat_interleave(nh, dim=0).contiguous()  # row t*nh + j: token t's table row
+        s = sin.repeat_interleave(nh, dim=0).contiguous()
+        _, qq, ss = rmsnorm_rope_quant(x, w, c, s, eps, fp8_max, want_y=False)
+        q[:, h0:h1] = qq.view(T, nh, D)
+        scale[:, h0:h1] = ss.view(T, nh)
+    return q, scale
+
+
 # ------------------------------------------------------------------ backward
 def rmsnorm_bwd(x, w, g, eps: float = 1e-6):
     """Returns (dx, dw, dw_f32)."""
