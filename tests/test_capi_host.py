@@ -156,3 +156,29 @@ def test_stream_floor_rules(lib):
     rc, msg = _rc(lib, "fq_stream_floor", odd, p, 4, NULL)             # input not 16-byte aligned
     assert rc == 1 and "aligned" in msg
     assert _rc(lib, "fq_stream_floor", p, ctypes.c_void_p(20), 4, NULL)[0] == 1
+
+
+def test_layernorm_rules(lib):
+    p = ctypes.c_void_p(16)
+    assert _rc(lib, "fq_layernorm_fwd", p, p, NULL, p, 0, 64, 0, 1e-5, NULL)[0] == 0    # M = 0: no-op
+    rc, msg = _rc(lib, "fq_layernorm_fwd", p, NULL, NULL, p, 4, 64, 0, 1e-5, NULL)      # no gain
+    assert rc == 1 and "null" in msg
+    assert _rc(lib, "fq_layernorm_fwd", p, p, NULL, p, 4, 0, 0, 1e-5, NULL)[0] == 1     # N = 0
+    assert _rc(lib, "fq_layernorm_fwd", p, p, NULL, p, 4, 64, 2, 1e-5, NULL)[0] == 2    # fp32 storage
+    assert _rc(lib, "fq_layernorm_fwd", p, p, NULL, p, 4, 64, 0, -1.0, NULL)[0] == 1    # eps < 0
+
+
+def test_prologue_blocks_rules(lib):
+    p = ctypes.c_void_p(16)
+    args = (p, 1024, p, p, p, p, p, p, 2, 4, 4, 128, 128)
+    for rpb in (0, 129):
+        rc, msg = _rc(lib, "fq_qk_norm_rope_quant_blocks", *args, rpb, 0, 2, 1e-6, 448.0, NULL)
+        assert rc == 1 and "rows_per_block" in msg
+    assert _rc(lib, "fq_qk_norm_rope_quant_blocks", p, 1024, p, p, p, p, p, p, 0, 4, 4, 128, 128, 8, 0, 2, 1e-6,
+               448.0, NULL)[0] == 0                                                        # T = 0: no-op
+
+
+def test_bounded_wait_limit_rules(lib):
+    for ms in (0, 10001):
+        rc, msg = _rc(lib, "fq_check_bounded_wait", ms, NULL)
+        assert rc == 1 and "limit_ms" in msg
