@@ -1137,13 +1137,16 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
 #define FQ_REG_K2(T, TT, V, GV, TPR)                                                                         \
   return launch_stream(rows_tma_wide_quant_kernel<T, TT, V, GV, TPR>, reg_threads((V) / (TPR)), p,              \
                        kRegRows / (TPR), xrow, trow, s, 0, 220 * 1024, 96 * 1024, reg_groups((V) / (TPR)));
-// Rows of 4096: two warps per row, so that three consumer groups fit the registers.
+// Rows of 4096: two warps per row, so that three consumer groups fit the registers. (A power-of-two
+// group narrower than the row is at most half of it, so no group spans the two warps; a group of the
+// whole row takes the per-row kernel, which does not read the group size.)
 #define FQ_REG_K(T, TT, V, GV)                                                      \
   {                                                                                 \
     if constexpr ((V) == 16) {                                                      \
-      if (a.group <= a.N / 2) FQ_REG_K2(T, TT, V, GV, 2)                            \
+      FQ_REG_K2(T, TT, V, GV, 2)                                                    \
+    } else {                                                                        \
+      FQ_REG_K2(T, TT, V, GV, 1)                                                    \
     }                                                                               \
-    FQ_REG_K2(T, TT, V, GV, 1)                                                      \
   }
 #define FQ_REG(T, TT, V)                                         \
   if (vpt == (V)) {                                              \
