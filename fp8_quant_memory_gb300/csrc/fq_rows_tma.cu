@@ -549,9 +549,10 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_rope_kernel(const 
 // then across slots for groups of more than 32 vectors); and the codes as correctly rounded
 // quotients. The warp's rows and the stage ring are independent, so the copy of the next stages
 // overlaps this work, and at most three rows per SM wait for data at a time.
-// Rows per stage = warps per consumer group. Consumer groups take the stages in turn: three for
-// rows of up to 3072 (13 warps: registers are allotted for 16, so 128 per thread), two for rows of
-// 4096, whose 64 registers of row data need more room (168 per thread).
+// Warps per consumer group (a stage holds kRegRows / TPR rows). Consumer groups take the stages in
+// turn: three when a warp holds up to 12 vector slots (13 warps: registers are allotted for 16, so
+// 128 per thread), two for 16 slots, whose 64 registers of row data need more room (168 per
+// thread). Rows of 4096 are split over two warps of 8 slots each, so they run with three groups.
 constexpr int kRegRows = 4;
 __host__ __device__ constexpr int reg_groups(int vpt) { return vpt <= 12 ? 3 : 2; }
 __host__ __device__ constexpr int reg_threads(int vpt) { return (kRegRows * reg_groups(vpt) + 1) * 32; }
