@@ -1,36 +1,43 @@
 // fq_prologue.cu -- the QK-Norm + RoPE + FP8 attention prologue ("case_norm_rope_quant.py" (Ch.28),
 // module docstring) for head_dim 128 with the whole head rotated, as a TMA-fed persistent kernel.
 //
-// Data movement. The rows are cut into chunks of SR consecutive (token, head) rows, one per CTA of
-// the grid. The CTAs that are resident take over the chunks of CTAs that have not started yet
-// through cluster launch control (a hardware work queue: no counter in global memory), so every
-// SM keeps streaming until the last chunk is taken and the CTAs finish together. One producer
-// lane streams its chunks through a ring of shared-memory stages, one chunk per stage: two 2-D
-// tensor TMA loads (cp.async.bulk.tensor, 128-byte swizzle) bring the first and second halves of
-// the SR rows (the NeoX "lo" and "hi" halves) and two 1-D bulk copies bring the cos and sin rows
-// of the tokens those rows belong to; an mbarrier counts the bytes. Bytes in flight do not depend
-// on registers or occupancy. x is read from HBM once; each table row once per stage that needs it
-// (L2 serves repeats); the two norm weights once per CTA (shared memory, fp32, in a lane-permuted
-// layout). Codes and scales go straight to global memory with evict-first stores.
+// Data movement. The rows of the packed [T, H, 128] input are cut into chunks of SR consecutive
+// (token, head) rows, one per CTA of the grid. The CTAs that are resident take over the chunks of
+// CTAs that have not started yet through cluster launch control (a hardware work queue: no counter
+// in global memory), so every SM keeps streaming until the last chunk is taken. One producer lane
+// streams its chunks through a ring of shared-memory stages, one chunk per stage: two 2-D tensor
+// TMA loads (128-byte swizzle) bring the first and second halves of the SR rows (the NeoX "lo" and
+// "hi" halves) and two 1-D bulk copies bring the cos and sin rows of the tokens those rows belong
+// to; an mbarrier counts the bytes. x is read from HBM once, each table row once per stage that
+// needs it (L2 serves the token a stage shares with its neighbour), the two norm weights once per
+// CTA straight into registers. Codes and scales go to global memory with evict-first stores.
 //
-// Work layout. Eight consumer warps, four lanes per row (eight rows per warp, one row per lane group
-// per stage). Lane j of a row holds the NeoX pairs 16j..16j+15 of both halves, so every pair
-// (p, p+64) sits in one thread: no shuffle and no shared-memory round trip for the rotation. The
-// swizzle makes the four lanes' 16-byte reads of two neighbouring rows hit disjoint banks. Each
-// lane stores its 16 contiguous codes of each half with one 16-byte store.
+// Work layout. Eight consumer warps in two halves that take alternate stages; four lanes per row,
+// eight rows per warp instruction. Lane j of a row holds the NeoX pairs 16j..16j+15 of both halves,
+// so every pair (p, p+64) sits in one thread and the rotation needs no data exchange. The lane keeps
+// its weights -- sixteen pairs of q weights and sixteen of k weights, still packed as the 16-bit
+// storage type -- in registers for the whole kernel; per row it reads its 64 bytes of x (the swizzle
+// makes the eight rows of a warp instruction hit disjoint banks) and its sixteen cos and sixteen
+// sin entries (lanes 2 and 3 walk their two sub-chunks of eight pairs in the opposite order, so the
+// four lanes of a row read disjoint banks; the rows of a warp instruction share the token).
 //
-// Arithmetic (the oracle's cast points, with two hardware shortcuts that stay far inside the
-// parity tolerances -- scale within 1e-5 relative, codes at most one step apart on at most 0.1%):
-//   ss = sum x^2 (fp32) -> rstd = rsqrt(ss/128 + eps) with the hardware rsqrt approximation (at
-//   most 2 ulp, as torch's own CUDA rsqrt; ss/128 is exact as ss * 2^-7); n = (x*rstd)*w;
-//   lo' = lo*c - hi*s, hi' = hi*c + lo*s (the compiler may fuse a product into the sum);
-//   scale = RN(max(amax, 1e-4)/fp8_max) (correctly rounded); q = e4m3(RN(y * RN(1/scale))).
-// A perturbation of one or two fp32 ulps moves a code only when y/scale sits at an e4m3 rounding
-// boundary, so the codes match the oracle's true division except on a vanishing fraction.
+// Arithmetic (the oracle's definition with the normalisation moved past the rotation; every
+// difference is a few fp32 roundings, far inside the parity tolerances -- scale within 1e-5
+// relative, codes at most one step apart on at most 0.1%):
+//   u = x*w, computed exactly in fp32 straight from the 16-bit operands (fma.rn.f32.bf16 / .f16:
+//   two 8- or 11-bit significands); ss = sum x^2 the same way; z = rope(u): z_lo = u_lo*c - u_hi*s,
+//   z_hi = u_hi*c + u_lo*s; rstd = rsqrt(ss/128 + eps) with the hardware rsqrt approximation (as
+//   torch's CUDA rsqrt; ss/128 is exact as ss * 2^-7). The definition's y = rope(x*rstd*w) equals
+//   rstd*z up to rounding, and |y| is largest where |z| is, so amax = max(RN(rstd * max|z|), 1e-4),
+//   scale = RN(amax / fp8_max) (correctly rounded), and the codes are e4m3(RN(z * m)) with
+//   m = rstd * (1/scale) (hardware reciprocal): the quotient y/scale to within a few ulps, which moves
+//   a code only when it sits at an e4m3 rounding boundary.
+// Signed zeros come out as in the definition (x = -0 gives the code 0x80 where y is -0): products
+// keep the sign of zero, and a fused u_lo*c - u_hi*s rounds an exact zero like the unfused form.
 //
 // Waits are bounded: a wait that has not completed after ~1 s of %globaltimer time sets bit 0 of
 // the device status word and the kernel stops issuing and consuming work (waiting, again bounded,
-// for the copies it has in flight) instead of trapping.
+// for the copies and work requests it has in flight) instead of trapping.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -45,12 +52,13 @@ namespace {
 
 constexpr int kD = 128;                                  // head_dim handled here
 constexpr int kLPR = 4;                                  // lanes per row
+constexpr int kPassRows = 32 / kLPR;                     // rows one warp instruction covers
 constexpr int kConsumerWarps = 8;
+constexpr int kHalfWarps = kConsumerWarps / 2;           // warps of one consumer half
 constexpr int kThreads = (kConsumerWarps + 1) * 32;      // + one producer warp
-constexpr int kGroupsPerHalf = (kConsumerWarps / 2) * (32 / kLPR);  // lane groups in one consumer half
-// Rows per stage (SR) is a template parameter: 64 for long row ranges per CTA, 32 when a CTA has
-// only a few stages to do (shorter pipeline fill and drain). Each lane group takes SR / 32 rows of
-// every stage its half consumes. One half of a stage's x (the NeoX lo or hi half) is SR * 128 bytes.
+constexpr int kReq = 2;                                  // work requests a producer keeps in flight
+
+// One half of a stage's x (the NeoX lo or hi columns of SR rows, 128 bytes per row).
 template <int SR>
 __host__ __device__ constexpr int half_tile() { return SR * (kD / 2) * 2; }
 
@@ -66,7 +74,6 @@ struct PrologueArgs {
   int32_t shift;
   int32_t rows;          // T * H
   int32_t H, Hq;
-  float inv_h;           // RN(1/H), for floor(x / H) with x < 2^21
   float eps, fp8_max, rcp_fp8_max;
   int32_t stages;        // ring depth
   int32_t stage_bytes;   // 2 half tiles + 2 table blocks, multiple of 1024
@@ -80,9 +87,9 @@ __device__ __forceinline__ uint4 lds16(uint32_t addr) {
   return v;
 }
 
-__device__ __forceinline__ float4 lds16f(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+__device__ __forceinline__ uint4 ldg_nc16(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
   return v;
 }
 
@@ -90,147 +97,179 @@ __device__ __forceinline__ uint32_t word(const uint4& v, int k) {
   return k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
 }
 
-// Table entries 8m..8m+7 of the lane's 16 (pairs 16j+8m..16j+8m+7 of one table row) -> 4 float2.
+__device__ __forceinline__ float rcp_approx(float v) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t token_of(uint32_t r, uint64_t magic, int32_t shift) {
+  return static_cast<uint32_t>((static_cast<uint64_t>(r) * magic) >> shift);
+}
+
+// Products of 16-bit storage operands rounded once to fp32 (fma.rn.f32.{bf16,f16}: sm_100 and
+// later). Two packed elements (low half first) per call.
+template <typename T>
+struct Mixed;
+
+template <>
+struct Mixed<__nv_bfloat16> {
+  // (x0*w0, x1*w1), exact: the product of two 8-bit significands fits fp32; -0 + p keeps p's sign.
+  static __device__ __forceinline__ float2 mul(uint32_t x, uint32_t w) {
+    float2 r;
+    asm("{\n\t.reg .b16 x0, x1, w0, w1;\n\tmov.b32 {x0, x1}, %2;\n\tmov.b32 {w0, w1}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, x0, w0, %4;\n\tfma.rn.f32.bf16 %1, x1, w1, %4;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "r"(w), "f"(-0.0f));
+    return r;
+  }
+  // (a.x + x0^2, a.y + x1^2)
+  static __device__ __forceinline__ float2 sq_add(uint32_t x, float2 a) {
+    float2 r;
+    asm("{\n\t.reg .b16 x0, x1;\n\tmov.b32 {x0, x1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, x0, x0, %3;\n\tfma.rn.f32.bf16 %1, x1, x1, %4;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "f"(a.x), "f"(a.y));
+    return r;
+  }
+};
+
+template <>
+struct Mixed<__half> {
+  static __device__ __forceinline__ float2 mul(uint32_t x, uint32_t w) {
+    float2 r;
+    asm("{\n\t.reg .b16 x0, x1, w0, w1;\n\tmov.b32 {x0, x1}, %2;\n\tmov.b32 {w0, w1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, x0, w0, %4;\n\tfma.rn.f32.f16 %1, x1, w1, %4;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "r"(w), "f"(-0.0f));
+    return r;
+  }
+  static __device__ __forceinline__ float2 sq_add(uint32_t x, float2 a) {
+    float2 r;
+    asm("{\n\t.reg .b16 x0, x1;\n\tmov.b32 {x0, x1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, x0, x0, %3;\n\tfma.rn.f32.f16 %1, x1, x1, %4;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "f"(a.x), "f"(a.y));
+    return r;
+  }
+};
+
+// Table entries of one sub-chunk (eight pairs) of one table row in shared memory -> 4 float2.
 template <typename TT>
-__device__ __forceinline__ void lds_table8(uint32_t addr, int m, float2 (&v)[4]) {
+__device__ __forceinline__ void lds_table8(uint32_t addr, float2 (&v)[4]) {
   if constexpr (sizeof(TT) == 4) {
-    const float4 f0 = lds16f(addr + 32 * m), f1 = lds16f(addr + 32 * m + 16);
-    v[0] = make_float2(f0.x, f0.y);
-    v[1] = make_float2(f0.z, f0.w);
-    v[2] = make_float2(f1.x, f1.y);
-    v[3] = make_float2(f1.z, f1.w);
+    const uint4 a = lds16(addr), b = lds16(addr + 16);
+    v[0] = make_float2(__uint_as_float(a.x), __uint_as_float(a.y));
+    v[1] = make_float2(__uint_as_float(a.z), __uint_as_float(a.w));
+    v[2] = make_float2(__uint_as_float(b.x), __uint_as_float(b.y));
+    v[3] = make_float2(__uint_as_float(b.z), __uint_as_float(b.w));
   } else {
-    const uint4 u = lds16(addr + 16 * m);
+    const uint4 u = lds16(addr);
 #pragma unroll
     for (int e = 0; e < 4; ++e) v[e] = Elem<TT>::unpack(word(u, e));
   }
 }
 
-// One (token, head) row of a stage, by the four lanes of a lane group: shared-memory x, table and
-// weight entries in, e4m3 codes and the fp32 scale out. `l` is the row within the stage.
-template <typename T, typename TT, int SR>
-__device__ __forceinline__ void prologue_row(const PrologueArgs& a, uint32_t st, int l, int j, int rev,
-                                             uint32_t wbase, int32_t rs, int32_t r1, int32_t tf, bool clamp) {
-  constexpr int kTabRow = (kD / 2) * static_cast<int>(sizeof(TT));
-  const int sw = l & 7;  // 128-byte swizzle phase of this row
-  const bool live = l < r1 - rs;
-  const int32_t xh = (rs - tf * a.H) + l;                                             // head index from token tf
-  const int32_t dt = static_cast<int32_t>((static_cast<float>(xh) + 0.5f) * a.inv_h);  // floor(xh / H)
-  const int32_t h = xh - dt * a.H;
-  const int32_t r = rs + l;
-  const uint32_t xrow = st + l * 128;
-  const uint4 xl0 = lds16(xrow + (((2 * j + rev) ^ sw) << 4));
-  const uint4 xl1 = lds16(xrow + (((2 * j + (rev ^ 1)) ^ sw) << 4));
-  const uint4 xh0 = lds16(xrow + half_tile<SR>() + (((2 * j + rev) ^ sw) << 4));
-  const uint4 xh1 = lds16(xrow + half_tile<SR>() + (((2 * j + (rev ^ 1)) ^ sw) << 4));
-  const uint32_t tcos = st + 2 * half_tile<SR>() + dt * kTabRow + j * (16 * static_cast<int>(sizeof(TT)));
-  const uint32_t wa = wbase + (h >= a.Hq ? 512u : 0u);  // the k weights follow the q weights
+// The lane's weights of one head type in processing order: [m][0..3] the lo pairs of sub-chunk
+// m ^ rev (eight 16-bit values), [m][4..7] the matching hi pairs.
+struct LaneWeights {
+  uint32_t v[2][8];
+};
 
-  float2 lo[8], hi[8];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    lo[e] = Elem<T>::unpack(word(xl0, e));
-    lo[4 + e] = Elem<T>::unpack(word(xl1, e));
-    hi[e] = Elem<T>::unpack(word(xh0, e));
-    hi[4 + e] = Elem<T>::unpack(word(xh1, e));
-  }
-  // Sum of squares with four independent accumulators (short dependency chains).
-  float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-  for (int i = 0; i < 8; i += 2) {
-    acc[0] = fma2(lo[i], lo[i], acc[0]);
-    acc[1] = fma2(lo[i + 1], lo[i + 1], acc[1]);
-    acc[2] = fma2(hi[i], hi[i], acc[2]);
-    acc[3] = fma2(hi[i + 1], hi[i + 1], acc[3]);
-  }
-  const float2 acc2 = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
-  const float ss = group_sum<kLPR>(acc2.x + acc2.y);
-  // ss/128 is exact as a multiplication by 2^-7; rsqrt is the hardware approximation.
-  const float rstd = rsqrtf(__fadd_rn(__fmul_rn(ss, 0.0078125f), a.eps));
-  const float2 rstd2 = splat2(rstd);
-  float pm[4];  // partial |y| maxima (four independent chains)
-  // Normalise and rotate eight pairs at a time (weights and table entries loaded per sub-chunk).
+// One (token, head) row, by the four lanes of a lane group. `xrow`: the row's lo half in the stage
+// (its hi half is one half tile further), `tab`: the lane's entries of the row's cos row (the sin row
+// is one table block further).
+template <typename T, typename TT, int SR, bool kClamp>
+__device__ __forceinline__ void quant_row(const PrologueArgs& a, uint32_t xrow, int sw, int j, int rev,
+                                          uint32_t tab, const LaneWeights& w, uint8_t* qrow, float* srow,
+                                          bool live) {
+  constexpr int kTabSub = 8 * static_cast<int>(sizeof(TT));  // bytes of one sub-chunk's table entries
+  float2 zl[2][4], zh[2][4];
+  float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+  float pm[2];
 #pragma unroll
   for (int m = 0; m < 2; ++m) {
     const int sm = m ^ rev;  // the sub-chunk this step works on
-    float2 wl[4], wh[4], c[4], s[4];
-#pragma unroll
-    for (int q4 = 0; q4 < 2; ++q4) {
-      const float4 fl = lds16f(wa + (2 * sm + q4) * 64);
-      const float4 fh = lds16f(wa + 256 + (2 * sm + q4) * 64);
-      wl[2 * q4] = make_float2(fl.x, fl.y);
-      wl[2 * q4 + 1] = make_float2(fl.z, fl.w);
-      wh[2 * q4] = make_float2(fh.x, fh.y);
-      wh[2 * q4 + 1] = make_float2(fh.z, fh.w);
-    }
-    lds_table8<TT>(tcos, sm, c);
-    lds_table8<TT>(tcos + a.tab_block, sm, s);
+    const uint32_t off = static_cast<uint32_t>(((2 * j + sm) ^ sw) << 4);
+    const uint4 xl = lds16(xrow + off), xh = lds16(xrow + half_tile<SR>() + off);
+    float2 c[4], s[4];
+    lds_table8<TT>(tab + sm * kTabSub, c);
+    lds_table8<TT>(tab + a.tab_block + sm * kTabSub, s);
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const int i = 4 * m + e;
-      const float2 nl = mul2(mul2(lo[i], rstd2), wl[e]);
-      const float2 nh = mul2(mul2(hi[i], rstd2), wh[e]);
-      lo[i] = sub2(mul2(nl, c[e]), mul2(nh, s[e]));
-      hi[i] = add2(mul2(nh, c[e]), mul2(nl, s[e]));
+      acc0 = Mixed<T>::sq_add(word(xl, e), acc0);
+      acc1 = Mixed<T>::sq_add(word(xh, e), acc1);
+      const float2 ul = Mixed<T>::mul(word(xl, e), w.v[m][e]);
+      const float2 uh = Mixed<T>::mul(word(xh, e), w.v[m][4 + e]);
+      zl[m][e] = fma2(neg2(uh), s[e], mul2(ul, c[e]));
+      zh[m][e] = fma2(ul, s[e], mul2(uh, c[e]));
     }
-    pm[2 * m] = absmax4(absmax4(0.f, lo[4 * m], hi[4 * m]), lo[4 * m + 1], hi[4 * m + 1]);
-    pm[2 * m + 1] = absmax4(absmax4(0.f, lo[4 * m + 2], hi[4 * m + 2]), lo[4 * m + 3], hi[4 * m + 3]);
+    pm[m] = fmaxf(absmax4(absmax4(0.f, zl[m][0], zh[m][0]), zl[m][1], zh[m][1]),
+                  absmax4(absmax4(0.f, zl[m][2], zh[m][2]), zl[m][3], zh[m][3]));
   }
-  float amax;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(amax) : "f"(pm[0]), "f"(pm[1]), "f"(pm[2]));
-  amax = fmaxf(amax, pm[3]);
-  amax = fmaxf(group_max<kLPR>(amax), 1e-4f);
-  // scale = RN(amax / fp8_max) via the correctly rounded reciprocal and one correction.
+  const float2 a01 = add2(acc0, acc1);
+  float ss = a01.x + a01.y;
+  float am = fmaxf(pm[0], pm[1]);
+  // the row's sum of squares and max |z| over its four lanes (two interleaved chains)
+#pragma unroll
+  for (int o = kLPR / 2; o > 0; o >>= 1) {
+    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, o));
+  }
+  const float rstd = rsqrtf(__fadd_rn(__fmul_rn(ss, 0.0078125f), a.eps));
+  const float amax = fmaxf(__fmul_rn(rstd, am), 1e-4f);
+  // scale = RN(amax / fp8_max): one product by RN(1/fp8_max) and Markstein's correction
   const float s0 = __fmul_rn(amax, a.rcp_fp8_max);
   const float sc = __fmaf_rn(__fmaf_rn(-s0, a.fp8_max, amax), a.rcp_fp8_max, s0);
-  const float rc = __frcp_rn(sc);
-  uint32_t ql[4], qh[4];
+  const float2 m2 = splat2(__fmul_rn(rstd, rcp_approx(sc)));
+  uint32_t cl[2][2], ch[2][2];  // [step][word]: eight codes of each half per step
 #pragma unroll
-  for (int i = 0; i < 8; i += 2) {
-    float2 a0 = mul2(lo[i], splat2(rc)), a1 = mul2(lo[i + 1], splat2(rc));
-    float2 b0 = mul2(hi[i], splat2(rc)), b1 = mul2(hi[i + 1], splat2(rc));
-    if (clamp) {
-      a0 = make_float2(clamp_abs(a0.x, a.fp8_max), clamp_abs(a0.y, a.fp8_max));
-      a1 = make_float2(clamp_abs(a1.x, a.fp8_max), clamp_abs(a1.y, a.fp8_max));
-      b0 = make_float2(clamp_abs(b0.x, a.fp8_max), clamp_abs(b0.y, a.fp8_max));
-      b1 = make_float2(clamp_abs(b1.x, a.fp8_max), clamp_abs(b1.y, a.fp8_max));
+  for (int m = 0; m < 2; ++m) {
+#pragma unroll
+    for (int e = 0; e < 4; e += 2) {
+      float2 l0 = mul2(zl[m][e], m2), l1 = mul2(zl[m][e + 1], m2);
+      float2 h0 = mul2(zh[m][e], m2), h1 = mul2(zh[m][e + 1], m2);
+      if constexpr (kClamp) {
+        l0 = make_float2(clamp_abs(l0.x, a.fp8_max), clamp_abs(l0.y, a.fp8_max));
+        l1 = make_float2(clamp_abs(l1.x, a.fp8_max), clamp_abs(l1.y, a.fp8_max));
+        h0 = make_float2(clamp_abs(h0.x, a.fp8_max), clamp_abs(h0.y, a.fp8_max));
+        h1 = make_float2(clamp_abs(h1.x, a.fp8_max), clamp_abs(h1.y, a.fp8_max));
+      }
+      cl[m][e / 2] = e4m3x2(l0) | (e4m3x2(l1) << 16);
+      ch[m][e / 2] = e4m3x2(h0) | (e4m3x2(h1) << 16);
     }
-    ql[i / 2] = e4m3x2(a0) | (e4m3x2(a1) << 16);
-    qh[i / 2] = e4m3x2(b0) | (e4m3x2(b1) << 16);
   }
   if (live) {
-    // ql/qh[0..1] hold sub-chunk rev, [2..3] the other one (8 codes each)
-    // One 16-byte store per half: the sub-chunk order is put back into column order first (two
-    // store instructions instead of four: fewer L1 wavefronts per row, measurably faster).
-    uint8_t* qrow = a.q + static_cast<int64_t>(r) * kD + 16 * j;
-    const uint4 lo16 = rev ? make_uint4(ql[2], ql[3], ql[0], ql[1]) : make_uint4(ql[0], ql[1], ql[2], ql[3]);
-    const uint4 hi16 = rev ? make_uint4(qh[2], qh[3], qh[0], qh[1]) : make_uint4(qh[0], qh[1], qh[2], qh[3]);
+    // one 16-byte store per half, the two steps put back into column order
+    const uint4 lo16 = rev ? make_uint4(cl[1][0], cl[1][1], cl[0][0], cl[0][1])
+                           : make_uint4(cl[0][0], cl[0][1], cl[1][0], cl[1][1]);
+    const uint4 hi16 = rev ? make_uint4(ch[1][0], ch[1][1], ch[0][0], ch[0][1])
+                           : make_uint4(ch[0][0], ch[0][1], ch[1][0], ch[1][1]);
     st_stream16(qrow, lo16);
-    st_stream16(qrow + 64, hi16);
-    if (j == 0) a.scale[r] = sc;
+    st_stream16(qrow + kD / 2, hi16);
+    if (srow != nullptr) *srow = sc;
   }
 }
 
-// ------------------------------------------------------------------------------ the kernel
-constexpr int kReq = 2;  // cluster-launch-control requests a producer keeps in flight
-
-// Shared memory: [pad to 1024][stages x stage_bytes][weights 2 x 128 fp32][kReq x 16-byte
-// responses][full x S][empty x S][request barriers x kReq][stage start rows x S].
+// Shared memory: [pad to 1024][stages x stage_bytes][kReq x 16-byte responses][full x S][empty x S]
+// [request barriers x kReq][stage start rows x S].
 __host__ __device__ constexpr size_t prologue_smem_bytes(int stages, int stage_bytes) {
-  return 1024 + static_cast<size_t>(stages) * stage_bytes + 2 * kD * sizeof(float) + kReq * 16 +
-         (2 * stages + kReq) * sizeof(uint64_t) + stages * sizeof(int32_t);
+  return 1024 + static_cast<size_t>(stages) * stage_bytes + kReq * 16 + (2 * stages + kReq) * sizeof(uint64_t) +
+         stages * sizeof(int32_t);
 }
 
-template <typename T, typename TT, int SR>
+template <typename T, typename TT, int SR, bool kClamp>
 __global__ void __launch_bounds__(kThreads, 2)
     prologue_tma_kernel(const __grid_constant__ CUtensorMap xmap, const PrologueArgs a) {
+  static_assert(SR % (kHalfWarps * kPassRows) == 0, "a stage splits into whole passes per warp");
+  constexpr int kWarpRows = SR / kHalfWarps;                         // consecutive rows of a stage per warp
+  constexpr int kTabRow = (kD / 2) * static_cast<int>(sizeof(TT));  // bytes of one table row
   extern __shared__ unsigned char smem_raw[];
   // The 128-byte swizzle repeats every 1024 bytes: align the ring to 1024.
   const uint32_t raw = smem_addr(smem_raw);
   unsigned char* smem = smem_raw + ((1024u - (raw & 1023u)) & 1023u);
   const int S = a.stages;
-  float* wsm = reinterpret_cast<float*>(smem + static_cast<size_t>(S) * a.stage_bytes);  // 2 x 128 floats
-  uint4* resp = reinterpret_cast<uint4*>(wsm + 2 * kD);
+  uint4* resp = reinterpret_cast<uint4*>(smem + static_cast<size_t>(S) * a.stage_bytes);
   uint64_t* full = reinterpret_cast<uint64_t*>(resp + kReq);
   uint64_t* empty = full + S;
   uint64_t* cbar = empty + S;
@@ -238,12 +277,11 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr int kTabRow = (kD / 2) * static_cast<int>(sizeof(TT));  // bytes of one table row
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps / 2);  // each stage is consumed by one half of the warps
+      mbar_init(&empty[s], kHalfWarps);  // each stage is consumed by one half of the consumer warps
     }
     for (int c = 0; c < kReq; ++c) mbar_init(&cbar[c], 1);
     fence_barrier_init();
@@ -252,11 +290,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   // Programmatic dependent launch: let the next kernel in the stream start its own set-up now, and
   // wait for the previous one to finish (and its writes to be visible) before touching global memory.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  ClcQueue<kReq> queue;
   // Neither the tensor map (a kernel parameter) nor the work requests touch data the previous kernel
   // writes, so the producer lane starts both before the dependency wait.
   if (threadIdx.x == kConsumerWarps * 32) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&xmap)) : "memory");
-    for (int c = 0; c < kReq; ++c) clc_try_cancel(&resp[c], &cbar[c]);
+    queue.start(resp, cbar);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -269,9 +308,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     uint32_t phase = 0;  // parity of the slot's current use; its release completes phase ^ 1
     int dslot = 0;       // slot and parity of stage k - depth
     uint32_t dphase = 0;
-    // Request n (n = 0, 1, ...) uses response slot n % kReq and completes that slot's barrier phase
-    // n / kReq; responses are consumed in request order. The first kReq were issued above.
-    int issued = kReq, answered = 0;
     uint32_t chunk = blockIdx.x;
     for (;;) {
       if (k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) {
@@ -292,9 +328,9 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       const int32_t rs = static_cast<int32_t>(chunk) * SR;
       const int32_t re = min(rs + SR, a.rows);
-      const int32_t tf = static_cast<int32_t>((static_cast<uint64_t>(rs) * a.magic) >> a.shift);
-      const int32_t tl = static_cast<int32_t>((static_cast<uint64_t>(re - 1) * a.magic) >> a.shift);
-      const uint32_t tbytes = static_cast<uint32_t>(tl - tf + 1) * kTabRow;
+      const uint32_t tf = token_of(static_cast<uint32_t>(rs), a.magic, a.shift);
+      const uint32_t tl = token_of(static_cast<uint32_t>(re - 1), a.magic, a.shift);
+      const uint32_t tbytes = (tl - tf + 1) * kTabRow;
       unsigned char* st = smem + static_cast<size_t>(slot) * a.stage_bytes;
       stage_row[slot] = rs;  // published to the consumers by the barrier's phase completion
       // Rows past the end of the tensor are zero-filled and still counted in full.
@@ -310,26 +346,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         slot = 0;
         phase ^= 1u;
       }
-      // The next chunk: the oldest outstanding request's answer.
-      const int c = answered % kReq;
-      if (!mbar_wait(kWaitLimitNs, &cbar[c], static_cast<uint32_t>(answered / kReq) & 1u)) {
-        ok = false;
-        break;
-      }
-      ++answered;
-      uint32_t next;
-      if (!clc_query(&resp[c], &next)) break;  // no CTA left to take over: this CTA is done
-      chunk = next;
-      clc_try_cancel(&resp[c], &cbar[c]);
-      ++issued;
-    }
-    // Requests still in flight end as failures; they write this CTA's shared memory, so wait.
-    while (ok && answered < issued) {
-      if (!mbar_wait(kWaitLimitNs, &cbar[answered % kReq], static_cast<uint32_t>(answered / kReq) & 1u)) {
-        ok = false;
-        break;
-      }
-      ++answered;
+      const int got = queue.next(&chunk);
+      if (got < 0) ok = false;
+      if (got <= 0) break;
     }
     // End marker for each consumer half (the halves take alternate stages).
     for (int e = 0; ok && e < 2; ++e) {
@@ -350,37 +369,36 @@ __global__ void __launch_bounds__(kThreads, 2)
       // Let the copies already issued land before this CTA's shared memory goes away.
       for (int j = max(0, k - S); j < k; ++j)
         if (!mbar_wait(kWaitLimitNs, &full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
-      for (; answered < issued; ++answered)
-        if (!mbar_wait(kWaitLimitNs, &cbar[answered % kReq], static_cast<uint32_t>(answered / kReq) & 1u)) break;
+      queue.drain();
     }
     return;
   }
 
   // ------------------------------------------------------------------ consumers
-  // Weights as fp32, permuted so that lane j's k-th float4 of a half sits at ((set*2+half)*4+k)*4+j:
-  // the four lanes of a row read 64 contiguous bytes per load. Loaded while the first stages are in
-  // flight; only the consumer warps synchronise on it.
-  for (int i = threadIdx.x; i < 2 * kD; i += kConsumerWarps * 32) {
-    const int set = i / kD, c = i % kD;
-    const int half = c / 64, within = c % 64;
-    const int jj = within / 16, kk = (within % 16) / 4, comp = within % 4;
-    wsm[((((set * 2 + half) * 4 + kk) * 4 + jj) * 4) + comp] = Elem<T>::load1(set ? a.wk : a.wq, c);
-  }
-  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-  const int grp = lane >> 2;  // row group within the warp
-  const int j = lane & 3;     // pairs 16j..16j+15 of each half
-  // A lane's 16 pairs are two sub-chunks of 8. Lanes 2 and 3 walk them in the opposite order, so
-  // that in every shared-memory load the four lanes of a row touch disjoint banks (their fp32 table
-  // and weight entries would otherwise sit 128 bytes apart).
+  const int g = lane / kLPR;  // row of the pass
+  const int j = lane % kLPR;  // pairs 16j..16j+15 of each half
+  // Lanes 2 and 3 walk their two sub-chunks of eight pairs in the opposite order, so that the four
+  // lanes of a row read their fp32 table entries from disjoint banks.
   const int rev = j >> 1;
-  const uint32_t wbase = smem_addr(wsm) + j * 16;
-  const bool clamp = a.fp8_max != 448.0f;
-  // The consumer warps work in two halves on alternate stages (even / odd), so that at any moment
-  // the warps of a scheduler are at different points of their row (the serial parts -- reductions,
-  // square root, reciprocals -- then overlap with the other half's arithmetic). A lane group takes
-  // rows l0, l0 + 32, ... of its half's stages.
-  const int half = warp / (kConsumerWarps / 2);
-  const int l0 = (warp % (kConsumerWarps / 2)) * 8 + grp;
+  // The lane's weights, packed 16-bit, in processing order.
+  LaneWeights wq, wk;
+#pragma unroll
+  for (int m = 0; m < 2; ++m) {
+    const int off = (16 * j + 8 * (m ^ rev)) * 2;  // bytes: eight pairs of the sub-chunk
+    const unsigned char* pq = static_cast<const unsigned char*>(a.wq) + off;
+    const unsigned char* pk = static_cast<const unsigned char*>(a.wk) + off;
+    const uint4 ql = ldg_nc16(pq), qh = ldg_nc16(pq + kD), kl = ldg_nc16(pk), kh = ldg_nc16(pk + kD);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      wq.v[m][e] = word(ql, e);
+      wq.v[m][4 + e] = word(qh, e);
+      wk.v[m][e] = word(kl, e);
+      wk.v[m][4 + e] = word(kh, e);
+    }
+  }
+  const int half = warp / kHalfWarps;
+  const int wrow0 = (warp % kHalfWarps) * kWarpRows + g;  // the lane group's first row of a stage
+  const uint32_t tlane = static_cast<uint32_t>(j * (16 * static_cast<int>(sizeof(TT))));
 
   int slot = half;  // stage k lives in slot k % S; S >= 2
   uint32_t phase = 0;
@@ -393,10 +411,34 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (rs < 0) break;  // end marker
     const uint32_t st = smem_addr(smem + static_cast<size_t>(slot) * a.stage_bytes);
     const int32_t re = min(rs + SR, a.rows);
-    const int32_t tf = static_cast<int32_t>((static_cast<uint64_t>(rs) * a.magic) >> a.shift);
+    const uint32_t tf = token_of(static_cast<uint32_t>(rs), a.magic, a.shift);
+#pragma unroll 1
+    for (int p = 0; p < kWarpRows / kPassRows; ++p) {
+      const int l = wrow0 + p * kPassRows;
+      const int32_t r = rs + l;
+      const bool live = r < re;
+      const uint32_t rr = static_cast<uint32_t>(live ? r : re - 1);  // dead lanes index a live row's table
+      const uint32_t t = token_of(rr, a.magic, a.shift);
+      const bool isk = static_cast<int32_t>(rr - t * static_cast<uint32_t>(a.H)) >= a.Hq;
+      const uint32_t xrow = st + l * 128;
+      const uint32_t tab = st + 2 * half_tile<SR>() + (t - tf) * kTabRow + tlane;
+      uint8_t* qrow = a.q + static_cast<int64_t>(r) * kD + 16 * j;
+      float* srow = (j == 0) ? a.scale + r : nullptr;
+      const int sw = l & 7;  // 128-byte swizzle phase of this row
+      const uint32_t kmask = __ballot_sync(0xffffffffu, isk);
+      if (kmask == 0u) {
+        quant_row<T, TT, SR, kClamp>(a, xrow, sw, j, rev, tab, wq, qrow, srow, live);
+      } else if (kmask == 0xffffffffu) {
+        quant_row<T, TT, SR, kClamp>(a, xrow, sw, j, rev, tab, wk, qrow, srow, live);
+      } else {  // the rows of the pass mix q and k heads
+        LaneWeights wsel;
 #pragma unroll
-    for (int u = 0; u < (SR / kGroupsPerHalf); ++u)
-      prologue_row<T, TT, SR>(a, st, l0 + u * kGroupsPerHalf, j, rev, wbase, rs, re, tf, clamp);
+        for (int m = 0; m < 2; ++m)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) wsel.v[m][e] = isk ? wk.v[m][e] : wq.v[m][e];
+        quant_row<T, TT, SR, kClamp>(a, xrow, sw, j, rev, tab, wsel, qrow, srow, live);
+      }
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the stage's shared memory
     slot += 2;
@@ -422,9 +464,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-}  // namespace
-
-namespace {
+template <typename T, typename TT, int SR>
+void* pick_kernel(bool clamp) {
+  return clamp ? reinterpret_cast<void*>(prologue_tma_kernel<T, TT, SR, true>)
+               : reinterpret_cast<void*>(prologue_tma_kernel<T, TT, SR, false>);
+}
 
 template <int SR>
 bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
@@ -454,7 +498,6 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
   p.rows = static_cast<int32_t>(a.rows);
   p.H = a.H;
   p.Hq = a.Hq;
-  p.inv_h = 1.0f / static_cast<float>(a.H);
   p.eps = a.eps;
   p.fp8_max = a.fp8_max;
   p.rcp_fp8_max = static_cast<float>(1.0 / static_cast<double>(a.fp8_max));
@@ -471,10 +514,12 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
   p.stages = (110 * 1024 - fixed) / p.stage_bytes;
   if (p.stages > 12) p.stages = 12;
   if (p.stages < 2) p.stages = 2;
-  // At most 128 rows (two 64-row stages) in flight per CTA: measured best on the 4k and 32k
-  // prologues. The depth must not exceed the ring: the producer waits on the full barrier of stage
-  // k - depth, whose slot must not have been refilled yet.
-  p.depth = 128 / SR;
+  // Rows in flight per CTA, measured: with 32-row stages (short row ranges per CTA, the 4096-token
+  // workload) 128 rows 11.92 us, 256 rows 11.70 us, 384 rows 11.58 us per launch; with 64-row
+  // stages (the 32768-token workload) 128 rows 130.1 us, 384 rows 132.2 us. The depth must not
+  // exceed the ring: the producer waits on the full barrier of stage k - depth, whose slot must not
+  // have been refilled yet.
+  p.depth = (SR == 32 ? 384 : 128) / SR;
   if (p.depth > p.stages) p.depth = p.stages;
   // The two consumer halves take alternate stages and wait for stage k on its slot's full barrier by
   // phase parity, which is only sound once the slot's previous use (stage k - S) has completed. With
@@ -485,13 +530,14 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
   const size_t smem = prologue_smem_bytes(p.stages, p.stage_bytes);
   if (smem > 227 * 1024) return false;
 
-  void (*kern)(const CUtensorMap, const PrologueArgs);
+  const bool clamp = a.fp8_max != 448.0f;
+  void* kern;
   if (dtype == DT_BF16)
-    kern = (tsz == 4) ? prologue_tma_kernel<__nv_bfloat16, float, SR>
-                      : prologue_tma_kernel<__nv_bfloat16, __nv_bfloat16, SR>;
+    kern = (tsz == 4) ? pick_kernel<__nv_bfloat16, float, SR>(clamp)
+                      : pick_kernel<__nv_bfloat16, __nv_bfloat16, SR>(clamp);
   else
-    kern = (tsz == 4) ? prologue_tma_kernel<__half, float, SR> : prologue_tma_kernel<__half, __half, SR>;
-  if (!ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem)) return false;
+    kern = (tsz == 4) ? pick_kernel<__half, float, SR>(clamp) : pick_kernel<__half, __half, SR>(clamp);
+  if (!ensure_dynamic_smem(kern, smem)) return false;
   // One CTA per chunk of SR rows. Only the CTAs that fit on the GPU at once start; they take over
   // the rest of the grid chunk by chunk (cluster launch control), so the grid is not a wave count.
   const int grid = static_cast<int>((a.rows + SR - 1) / SR);
@@ -507,7 +553,8 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, xmap, p) == cudaSuccess;
+  void* args[] = {&xmap, &p};
+  return cudaLaunchKernelExC(&cfg, kern, args) == cudaSuccess;
 }
 
 }  // namespace
@@ -516,7 +563,6 @@ bool launch_prologue_tma(const RowArgs& a, int dtype, int table_dtype, cudaStrea
   if (a.N != kD || a.R != kD) return false;
   if (a.rows <= 0 || a.rows > 0x7fffffffLL - 128) return false;  // row + stage size stays in int32
   if (a.token_stride != static_cast<int64_t>(a.H) * kD) return false;  // packed [T, H, 128] only
-  if (a.H + 64 >= (1 << 21)) return false;
   if (!(table_dtype == DT_FP32 || table_dtype == dtype)) return false;
   if ((reinterpret_cast<uintptr_t>(a.q) & 15u) != 0) return false;
   // Short row ranges per CTA (a few stages each): 32-row stages halve the pipeline fill and drain.

@@ -57,7 +57,7 @@ constexpr int kReq = 2;  // cluster-launch-control requests a producer keeps in 
 
 // Producer: one lane streams the stages this CTA takes (its own first, then those of CTAs it takes
 // over), posts `markers` end markers (one per group of consumer warps that take stages in turn), and
-// returns. `issued` work requests were started before the dependency wait (ring_setup).
+// returns. Its first kReq work requests were started before the dependency wait (ring_setup).
 __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem, uint64_t* full, uint64_t* empty,
                                         uint64_t* wbar, unsigned char* wsm, uint4* resp, uint64_t* cbar,
                                         int32_t* stage_row, int SR, int esize, int tsize, int markers = 1) {
@@ -74,8 +74,8 @@ __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem
   uint32_t phase = 0, dphase = 0;
   int k = 0;
   bool ok = true;
-  // Request n uses response slot n % kReq and completes that slot's barrier phase n / kReq.
-  int issued = kReq, answered = 0;
+  // The kReq first work requests were issued by ring_setup.
+  ClcQueue<kReq> queue{resp, cbar, kReq, 0, false};
   uint32_t chunk = blockIdx.x;
   for (;;) {
     if (k >= S && !mbar_wait(kWaitLimitNs, &empty[slot], phase ^ 1u)) {
@@ -110,26 +110,10 @@ __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem
       slot = 0;
       phase ^= 1u;
     }
-    // The next stage: the oldest outstanding request's answer.
-    const int c = answered % kReq;
-    if (!mbar_wait(kWaitLimitNs, &cbar[c], static_cast<uint32_t>(answered / kReq) & 1u)) {
-      ok = false;
-      break;
-    }
-    ++answered;
-    uint32_t next;
-    if (!clc_query(&resp[c], &next)) break;  // no CTA left to take over: this CTA is done
-    chunk = next;
-    clc_try_cancel(&resp[c], &cbar[c]);
-    ++issued;
-  }
-  // Requests still in flight end as failures; they write this CTA's shared memory, so wait.
-  while (ok && answered < issued) {
-    if (!mbar_wait(kWaitLimitNs, &cbar[answered % kReq], static_cast<uint32_t>(answered / kReq) & 1u)) {
-      ok = false;
-      break;
-    }
-    ++answered;
+    // The next stage: a chunk taken over from a CTA that has not started (none left: done).
+    const int got = queue.next(&chunk);
+    if (got < 0) ok = false;
+    if (got <= 0) break;
   }
   // End markers: one stage each, so that every group of consumer warps meets one.
   for (int e = 0; ok && e < markers; ++e) {
@@ -149,8 +133,7 @@ __device__ __forceinline__ void produce(const StreamArgs& p, unsigned char* smem
   flag_failure(p.status);
   for (int j = max(0, k - S); j < k; ++j)
     if (!mbar_wait(kWaitLimitNs, &full[j % S], static_cast<uint32_t>(j / S) & 1u)) break;
-  for (; answered < issued; ++answered)
-    if (!mbar_wait(kWaitLimitNs, &cbar[answered % kReq], static_cast<uint32_t>(answered / kReq) & 1u)) break;
+  queue.drain();
 }
 
 // Shared set-up of both kernels: ring layout, barriers, programmatic-launch handshake, the first

@@ -120,6 +120,56 @@ __device__ __forceinline__ bool clc_query(const void* response, uint32_t* ctaid_
   return ok != 0;
 }
 
+// A CTA's work queue over cluster launch control with kReq requests in flight. Request n uses
+// response slot n % kReq and completes phase n / kReq of that slot's barrier; answers are read in
+// issue order. The scheduler need not answer in that order: an earlier request can fail (nothing
+// left to cancel) while a later one, answered first, took a CTA. So a failed answer only stops new
+// requests (none may follow an observed failure); the answers still in flight are read, and a
+// success among them is taken over, never dropped.
+template <int kReq>
+struct ClcQueue {
+  uint4* resp;
+  uint64_t* cbar;
+  int issued;
+  int answered;
+  bool failed;
+
+  __device__ __forceinline__ void start(uint4* r, uint64_t* b) {
+    resp = r;
+    cbar = b;
+    for (int c = 0; c < kReq; ++c) clc_try_cancel(&resp[c], &cbar[c]);
+    issued = kReq;
+    answered = 0;
+    failed = false;
+  }
+
+  // 1: a chunk to take over in *chunk (a new request replaces the answered one unless a failure was
+  // seen); 0: none left and no request in flight; -1: a bounded wait gave up.
+  __device__ __forceinline__ int next(uint32_t* chunk) {
+    while (answered < issued) {
+      const int c = answered % kReq;
+      if (!mbar_wait(kWaitLimitNs, &cbar[c], static_cast<uint32_t>(answered / kReq) & 1u)) return -1;
+      ++answered;
+      if (clc_query(&resp[c], chunk)) {
+        if (!failed) {
+          clc_try_cancel(&resp[c], &cbar[c]);
+          ++issued;
+        }
+        return 1;
+      }
+      failed = true;
+    }
+    return 0;
+  }
+
+  // After a failed wait: let the requests still in flight land (they write this CTA's shared
+  // memory), each wait bounded again.
+  __device__ __forceinline__ void drain() {
+    for (; answered < issued; ++answered)
+      if (!mbar_wait(kWaitLimitNs, &cbar[answered % kReq], static_cast<uint32_t>(answered / kReq) & 1u)) break;
+  }
+};
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

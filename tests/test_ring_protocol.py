@@ -71,3 +71,90 @@ def test_ring_without_the_rule_can_pass_early(S, G, depth):
     register-resident kernels used)."""
     assert S % G != 0 and depth > S - G
     assert first_false_pass(S, G, depth, runs=4000) is not None
+
+
+# ------------------------------------------------------------------------------------------------
+# The work queue (cluster launch control) of the same kernels, simulated on the host.
+#
+# A grid of `grid` chunks, one per CTA; the first `resident` CTAs start, the others wait to be
+# cancelled. A resident CTA keeps kReq requests in flight. The scheduler answers pending requests
+# in any order (across CTAs and within one): a request succeeds with a chunk of a CTA that has not
+# started while there is one, and fails once there is none. A CTA reads its answers in the order it
+# issued them (the response slots are mbarrier phases). Rule of the hardware: no request may follow
+# an observed failure.
+# ------------------------------------------------------------------------------------------------
+def run_queue(grid: int, resident: int, k_req: int, seed: int, take_late: bool, in_order: bool = False):
+    """Returns (processed chunk list, rule violations). take_late=True is the kernels' ClcQueue
+    (a success read after a failure is taken over); False is the discard-after-failure rule."""
+    rng = random.Random(seed)
+    pool = list(range(resident, grid))
+    processed = list(range(resident))   # every resident CTA processes its own chunk first
+    answers = {}                         # (cta, n) -> chunk id or None (failure), once answered
+    pending = []                         # (cta, n) issued, not yet answered
+    state = {}
+    for c in range(resident):
+        state[c] = {"issued": k_req, "answered": 0, "failed": False, "done": False, "draining": False}
+        pending += [(c, n) for n in range(k_req)]
+    violations = 0
+    while True:
+        acts = [("answer", p) for p in pending
+                if not in_order or p[1] == min(n for c, n in pending if c == p[0])]
+        for c, st in state.items():
+            if not st["done"] and st["answered"] < st["issued"] and (c, st["answered"]) in answers:
+                acts.append(("read", c))
+            elif not st["done"] and st["answered"] == st["issued"]:
+                acts.append(("finish", c))
+        if not acts:
+            break
+        kind, v = rng.choice(acts)
+        if kind == "answer":
+            pending.remove(v)
+            answers[v] = pool.pop(rng.randrange(len(pool))) if pool else None
+        elif kind == "finish":
+            state[v]["done"] = True
+        else:
+            st = state[v]
+            got = answers[(v, st["answered"])]
+            st["answered"] += 1
+            if st["draining"]:
+                continue                  # discard rule: answers after the first failure are dropped
+            if got is None:
+                st["failed"] = True
+                if not take_late:
+                    st["draining"] = True
+                continue
+            processed.append(got)
+            if not st["failed"]:
+                pending.append((v, st["issued"]))
+                st["issued"] += 1
+            elif not take_late:
+                violations += 1
+    for c, st in state.items():
+        if st["answered"] != st["issued"]:
+            violations += 1               # a CTA left with a request in flight
+    return processed, violations
+
+
+@pytest.mark.parametrize("grid,resident,k_req", [(40, 8, 2), (17, 16, 2), (100, 3, 3), (9, 9, 2), (64, 12, 1)])
+def test_work_queue_processes_every_chunk_once(grid, resident, k_req):
+    for seed in range(300):
+        done, bad = run_queue(grid, resident, k_req, seed, take_late=True)
+        assert bad == 0
+        assert sorted(done) == list(range(grid)), (seed, sorted(done))
+
+
+def test_dropping_late_answers_can_lose_a_chunk():
+    """The rule the kernels used before: stop reading at the first failure and discard the answers
+    still in flight. When the scheduler answers a later request before an earlier one, a success
+    can arrive after a failure, and its chunk is never processed."""
+    lost = [s for s in range(2000)
+            if sorted(run_queue(40, 8, 2, s, take_late=False)[0]) != list(range(40))]
+    assert lost, "no interleaving lost a chunk"
+
+
+def test_in_order_answers_make_both_rules_agree():
+    """If the scheduler answers each CTA's requests in issue order, a failure is followed only by
+    failures, so discarding the answers after it loses nothing (what the earlier GPU runs saw)."""
+    for seed in range(300):
+        done, bad = run_queue(40, 8, 2, seed, take_late=False, in_order=True)
+        assert bad == 0 and sorted(done) == list(range(40))
