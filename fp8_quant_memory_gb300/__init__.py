@@ -25,6 +25,7 @@ from . import _capi
 __all__ = ["layernorm_fwd", "rmsnorm_fwd", "rmsnorm_fwd_rstd", "rmsnorm_bwd_rstd", "rmsnorm_rope", "rmsnorm_rope_quant", "rmsnorm_rope_quant_groups", "qk_norm_rope_quant", "qk_norm_rope_quant_blocks",
            "rmsnorm_bwd",
            "rmsnorm_bwd_workspace_bytes", "rmsnorm", "RMSNormFunction", "device_status", "check_bounded_wait",
+           "set_strict",
            "stream_floor", "FqError"]
 
 FqError = _capi.FqError
@@ -260,6 +261,12 @@ def device_status(clear: bool = True, device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     _capi.call("fq_device_status", ctypes.byref(word), 1 if clear else 0, _stream(dev))
     return int(word.value)
+
+
+def set_strict(on: bool) -> bool:
+    """Strict mode on or off (returns the previous setting): every call then waits for its stream and
+    raises FqError (status FQ_ERR_DEVICE) if a pipelined kernel gave up on a bounded wait."""
+    return bool(_capi.load().fq_set_strict(1 if on else 0))
 
 
 def check_bounded_wait(limit_ms: int = 50, device=None) -> int:

@@ -22,6 +22,7 @@ SIGNATURES = {
     "fq_version": (_int, []),
     "fq_device_status": (_int, [ctypes.POINTER(ctypes.c_uint), _int, _vp]),
     "fq_check_bounded_wait": (_int, [ctypes.c_uint, _vp]),
+    "fq_set_strict": (_int, [_int]),
     "fq_stream_floor": (_int, [_vp, _vp, _i64, _vp]),
     "fq_rmsnorm_fwd": (_int, [_vp, _vp, _vp, _i64, _i64, _int, _f32, _vp]),
     "fq_rmsnorm_fwd_rstd": (_int, [_vp, _vp, _vp, _vp, _i64, _i64, _int, _f32, _vp]),

@@ -1,6 +1,7 @@
 // fq_api.cu -- the extern "C" entry points declared in include/fq.h: argument validation on the
 // host (before any CUDA call), choice between the vectorised and the scalar kernels, launch, and
 // error reporting through fq_last_error().
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -36,9 +37,36 @@ int ok() {
 
 bool aligned(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int check_launch(const char* what) {
-  const cudaError_t e = cudaGetLastError();
+// Strict mode (fq_set_strict, or FQ_STRICT=1 in the environment at the first call): every compute
+// call waits for its own stream and turns a bounded-wait failure into FQ_ERR_DEVICE.
+std::atomic<int> g_strict{-1};
+
+bool strict_mode() {
+  int v = g_strict.load(std::memory_order_relaxed);
+  if (v < 0) {
+    const char* e = std::getenv("FQ_STRICT");
+    int want = (e != nullptr && e[0] == '1') ? 1 : 0;
+    g_strict.compare_exchange_strong(v, want);
+    v = g_strict.load(std::memory_order_relaxed);
+  }
+  return v == 1;
+}
+
+int check_launch(const char* what, cudaStream_t s) {
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "%s: launch failed: %s", what, cudaGetErrorString(e));
+  if (strict_mode()) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    if (cap == cudaStreamCaptureStatusNone) {  // a stream being captured cannot be waited for
+      unsigned int word = 0;
+      e = fq::read_device_status(&word, 1, s);
+      if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+      if (word & 1u)
+        return fail(FQ_ERR_DEVICE, "%s: a pipelined kernel gave up on a bounded wait and skipped work", what);
+    }
+  }
   return ok();
 }
 
@@ -93,14 +121,14 @@ int launch_rows(const char* fn, const fq::RowArgs& a, int mode, int dtype, int t
   // compute the same result).
   if (vec && mode == fq::MODE_QK && !env_is("FQ_PROLOGUE_KERNEL", "generic") &&
       fq::launch_prologue_tma(a, dtype, table_dtype, s))
-    return check_launch(fn);
+    return check_launch(fn, s);
   if (vec && (mode == fq::MODE_FWD || mode == fq::MODE_ROPE || mode == fq::MODE_ROPE_QUANT) &&
       !env_is("FQ_ROWS_KERNEL", "generic") &&
       fq::launch_rows_tma(a, mode, dtype, table_dtype, s))
-    return check_launch(fn);
+    return check_launch(fn, s);
   if (!(vec && fq::launch_rows_vector(a, mode, dtype, table_dtype, s)))
     fq::launch_rows_scalar(a, mode, dtype, table_dtype, s);
-  return check_launch(fn);
+  return check_launch(fn, s);
 }
 
 }  // namespace
@@ -133,7 +161,7 @@ extern "C" {
 
 const char* fq_last_error(void) { return g_err.c_str(); }
 
-int fq_version(void) { return 1; }
+int fq_version(void) { return 2; }
 
 int fq_device_status(unsigned int* word, int clear, cudaStream_t stream) {
   if (word == nullptr) return fail(FQ_ERR_INVALID_ARG, "fq_device_status: word is null");
@@ -149,6 +177,12 @@ int fq_check_bounded_wait(unsigned int limit_ms, cudaStream_t stream) {
   const cudaError_t e = fq::launch_wait_probe(limit_ms, stream);
   if (e != cudaSuccess) return fail(FQ_ERR_CUDA, "fq_check_bounded_wait: %s", cudaGetErrorString(e));
   return ok();
+}
+
+int fq_set_strict(int on) {
+  const int prev = strict_mode() ? 1 : 0;
+  g_strict.store(on ? 1 : 0, std::memory_order_relaxed);
+  return prev;
 }
 
 int fq_stream_floor(const void* in, void* out, int64_t n16, cudaStream_t stream) {
@@ -210,7 +244,7 @@ int fq_layernorm_fwd(const void* x, const void* gamma, const void* beta, void* y
   const bool vec = (N % 8 == 0) && aligned(x, 16) && aligned(gamma, 16) && aligned(y, 16) &&
                    (beta == nullptr || aligned(beta, 16));
   fq::launch_layernorm(a, dtype, vec, stream);
-  return check_launch(fn);
+  return check_launch(fn, stream);
 }
 
 int fq_rmsnorm_fwd(const void* x, const void* w, void* y, int64_t M, int64_t N, int dtype, float eps,
@@ -386,7 +420,7 @@ int fq_qk_norm_rope_quant_blocks(const void* qk, int64_t token_stride, const voi
   if (!vec || !fq::launch_prologue_blocks(a, static_cast<int32_t>(rows_per_block), dtype, table_dtype, stream))
     return fail(FQ_ERR_UNSUPPORTED,
                 "%s: needs head_dim = rope_dim <= 128, a multiple of 16, and 16-byte aligned tensors", fn);
-  return check_launch(fn);
+  return check_launch(fn, stream);
 }
 size_t fq_rmsnorm_bwd_workspace_bytes(int64_t M, int64_t N) {
   if (M <= 0 || N <= 0) return 0;
@@ -424,7 +458,7 @@ int rmsnorm_bwd(const char* fn, const void* x, const void* w, const void* grad_y
   a.N = static_cast<int32_t>(N);
   a.eps = eps;
   fq::launch_bwd(a, dtype, stream);
-  return check_launch(fn);
+  return check_launch(fn, stream);
 }
 
 }  // namespace

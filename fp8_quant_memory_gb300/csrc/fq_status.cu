@@ -28,10 +28,22 @@ bool ensure_dynamic_smem(const void* kernel, size_t bytes) {
   return true;
 }
 
+// The word's device address, looked up once per device (with that device current) and cached: in
+// host code the variable's name is only a host-side stand-in. A cudaDeviceReset on a device
+// invalidates the cached address (the library's device state is not rebuilt after a reset).
 unsigned int* device_status_ptr() {
-  void* p = nullptr;
-  if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
-  return static_cast<unsigned int*>(p);
+  constexpr int kMaxDevices = 64;
+  static std::mutex mu;
+  static unsigned int* cache[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned int*>(p);
+  }
+  return cache[dev];
 }
 
 cudaError_t read_device_status(unsigned int* word, int clear, cudaStream_t s) {

@@ -46,7 +46,8 @@ enum fq_status {
   FQ_ERR_UNSUPPORTED = 2, /* dtype code not accepted by this entry point */
   FQ_ERR_MISALIGNED = 3,  /* reserved: misaligned inputs take the scalar path instead */
   FQ_ERR_CUDA = 4,        /* a CUDA call failed (launch error, no device); see fq_last_error() */
-  FQ_ERR_DEVICE = 5       /* a kernel reported a failure through the device status word */
+  FQ_ERR_DEVICE = 5       /* strict mode only (fq_set_strict): a kernel reported a failure through the
+                             device status word */
 };
 
 /* Storage dtype codes. */
@@ -61,8 +62,22 @@ int fq_version(void);
 
 /* Reads the device status word of the current device after synchronising `stream`, optionally
  * clearing it. Bit 0 (value 1): a pipelined kernel gave up on a bounded wait and skipped its
- * remaining work. `*word` receives the bits. Returns FQ_OK or FQ_ERR_CUDA. */
+ * remaining work. `*word` receives the bits. Returns FQ_OK or FQ_ERR_CUDA.
+ * Compute calls return as soon as their work is enqueued, before a kernel can have given up on a
+ * wait, so a plain FQ_OK does not say that the work completed: either read this word after the
+ * stream reaches the call, or turn on strict mode (fq_set_strict). The word is one per device and
+ * shared by every stream and call. The library looks up its device address once per device; after
+ * a cudaDeviceReset on that device the library must not be used there again in the same process. */
 int fq_device_status(unsigned int* word, int clear, cudaStream_t stream);
+
+/* Strict mode on (1) or off (0); returns the previous setting. Also turned on by FQ_STRICT=1 in the
+ * environment at the first call. In strict mode every compute entry point, after enqueuing its work,
+ * synchronises its stream, reads and clears the device status word, and returns FQ_ERR_DEVICE if bit
+ * 0 was set -- attributing to this call any bounded-wait failure since the word was last cleared.
+ * While `stream` is being captured into a CUDA graph it cannot be waited for, and strict mode
+ * checks nothing. Strict mode trades the asynchronous launch for an immediate answer (a debugging
+ * and validation mode). The tutorial pages have no counterpart. */
+int fq_set_strict(int on);
 
 /* Diagnostic for the bounded waits of the pipelined kernels: enqueues one block whose single
  * mbarrier wait can never complete (nothing arrives on the barrier). The wait gives up after
@@ -237,7 +252,8 @@ int fq_rmsnorm_bwd_rstd(const void* x, const void* w, const void* grad_y, const 
  * held until the process exits). Problems whose fq_rmsnorm_bwd_workspace_bytes(M, N) exceeds that
  * size are rejected with FQ_ERR_INVALID_ARG.
  * The first call on each device looks up that array's device address (with the device current);
- * make that first call before any stream capture. Every call shares the one array and leaves its
+ * make that first call before any stream capture. A cudaDeviceReset on that device invalidates the
+ * looked-up address: do not call this entry point on that device again in the same process. Every call shares the one array and leaves its
  * contents behind (nothing in it needs clearing: each call overwrites what it reads), so calls
  * that may overlap on the GPU -- on different streams, or from different threads -- race on it and
  * must be serialised by the caller.

@@ -8,8 +8,18 @@
 - fp8 codes:    identical, or one e4m3 step apart on at most 0.1% of the elements
 - dw (fp32 sums): |gpu - ref| <= 1e-3 * max(|ref|, rms(ref)); bf16/fp16 dw within one ulp, or
   within 1e-3 * rms(ref) where the column's sum nearly cancels
+
+The two widened rules (rotated columns, near-cancelling dw columns) also count the elements they
+accept only because of the widening and bound that count: at most 1e-4 of the rotated elements
+(the oracle with every row's rstd moved by 3 fp32 ulps needs the widening on 1.3e-5 of them, on a
+4097 x 1536 bf16 case) and at most 0.1% of the dw columns (one column of 4096 on a 513 x 4096 fp16
+case). Rows of rmsnorm_rope_quant whose scale is further than 1e-5 from the oracle's are accepted
+only when codes and scale are exactly the quantiser of the kernel's own y; scale_rows_by_own_y
+counts them.
 """
 from __future__ import annotations
+
+import math
 
 import torch
 
@@ -31,7 +41,7 @@ def assert_storage_close(gpu: torch.Tensor, ref: torch.Tensor, what: str = "y"):
 
 
 def assert_rope_close(gpu: torch.Tensor, ref: torch.Tensor, normed: torch.Tensor, cos: torch.Tensor,
-                      sin: torch.Tensor, what: str = "y"):
+                      sin: torch.Tensor, what: str = "y", max_widened_frac: float = 1e-4) -> int:
     """Tolerance for rmsnorm_rope / rmsnorm_rope_quant outputs y [M, N] (cos, sin: [M, R/2]).
 
     Head columns: the storage rule. Rotated columns: "rmsnorm_rope_quant.py" (torch_reference_fused)
@@ -60,6 +70,13 @@ def assert_rope_close(gpu: torch.Tensor, ref: torch.Tensor, normed: torch.Tensor
     assert not bool(bad.any()), (
         f"{what}: {int(bad.sum())} of {bad.numel()} elements outside the tolerance; worst err "
         f"{float(err.max()):.3g} at ref {float(b.flatten()[int(err.flatten().argmax())]):.5g}")
+    # elements that pass only because of the widening (all of them in the rotated columns)
+    widened = int((err > torch.clamp(b.abs() * rel, min=abs_)).sum())
+    n_rot = M * R
+    allowed = max(1, math.ceil(max_widened_frac * n_rot)) if n_rot else 0
+    assert widened <= allowed, (
+        f"{what}: {widened} rotated elements pass only under the widened bound (limit {allowed} of {n_rot})")
+    return widened
 
 
 def code_order(q: torch.Tensor) -> torch.Tensor:
@@ -95,7 +112,8 @@ def assert_dw_close(gpu_f32: torch.Tensor, ref_f32: torch.Tensor, rel: float = 1
     assert not bool(bad.any()), f"dw_f32: {int(bad.sum())} columns outside 1e-3 * max(|ref|, rms)"
 
 
-def assert_within_one_ulp(gpu: torch.Tensor, ref: torch.Tensor, what: str = "dw", rms_floor: float = 1e-3):
+def assert_within_one_ulp(gpu: torch.Tensor, ref: torch.Tensor, what: str = "dw", rms_floor: float = 1e-3,
+                          max_floor_frac: float = 1e-3) -> int:
     """bf16/fp16 dw within one ulp of the oracle's, or within rms_floor * rms(ref) of it. A column
     whose sum over rows nearly cancels (|dw| far below the rms of dw) moves by several of its own ulps
     when rstd moves by one fp32 ulp -- which any fp32 order of the sum of squares other than the
@@ -109,5 +127,41 @@ def assert_within_one_ulp(gpu: torch.Tensor, ref: torch.Tensor, what: str = "dw"
     ord_b = torch.where(b < 0, -(b & 0x7FFF), b)
     rb = ref.double()
     floor = rms_floor * float(rb.pow(2).mean().sqrt()) if rb.numel() else 0.0
-    bad = ((ord_a - ord_b).abs() > 1) & ((gc.double() - rb).abs() > floor)
+    far = (ord_a - ord_b).abs() > 1
+    bad = far & ((gc.double() - rb).abs() > floor)
     assert not bool(bad.any()), f"{what}: {int(bad.sum())} columns more than one ulp apart and above the rms floor"
+    # columns accepted only through the rms floor
+    widened = int(far.sum())
+    allowed = max(1, math.ceil(max_floor_frac * far.numel()))
+    assert widened <= allowed, f"{what}: {widened} columns pass only under the rms floor (limit {allowed})"
+    return widened
+
+
+def scale_rows_by_own_y(gpu_s: torch.Tensor, ref_s: torch.Tensor, rel: float = 1e-5) -> int:
+    """Rows of rmsnorm_rope_quant whose scale is further than `rel` from the oracle's. The caller has
+    checked that codes and scales are exactly the quantiser of the kernel's own y (the rule that
+    accepts such a row: a bf16 flip of the row's amax element moves its scale by ~2^-8)."""
+    a = gpu_s.detach().cpu().double()
+    b = ref_s.double()
+    return int(((a - b).abs() > rel * b.abs()).sum())
+
+
+def oracle_prologue_parallel(orc, d: dict, hq: int, hk: int, **kw):
+    """orc.qk_norm_rope_quant over the whole batch, split into one token slice per host core and run
+    on a thread pool (the oracle is a C library called through ctypes, which releases the
+    interpreter lock, and keeps no global state). Same result as one call."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    T = d["qk"].shape[0]
+    cores = max(1, min(os.cpu_count() or 1, 32, T))
+    bounds = [(T * i // cores, T * (i + 1) // cores) for i in range(cores)]
+    bounds = [(a, b) for a, b in bounds if b > a]
+
+    def run(ab):
+        a, b = ab
+        return orc.qk_norm_rope_quant(d["qk"][a:b], d["wq"], d["wk"], d["cos"][a:b], d["sin"][a:b], hq, hk, **kw)
+
+    with ThreadPoolExecutor(len(bounds)) as ex:
+        parts = list(ex.map(run, bounds))
+    return torch.cat([p[0] for p in parts]), torch.cat([p[1] for p in parts])

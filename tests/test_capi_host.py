@@ -182,3 +182,17 @@ def test_bounded_wait_limit_rules(lib):
     for ms in (0, 10001):
         rc, msg = _rc(lib, "fq_check_bounded_wait", ms, NULL)
         assert rc == 1 and "limit_ms" in msg
+
+
+def test_strict_mode_toggles_without_a_device(lib):
+    """fq_set_strict only sets a flag (the synchronisation happens in later compute calls)."""
+    prev = lib.fq_set_strict(1)
+    try:
+        assert lib.fq_set_strict(0) == 1
+        assert lib.fq_set_strict(1) == 0
+    finally:
+        lib.fq_set_strict(prev)
+
+
+def test_version_counts_the_strict_mode_entry_point(lib):
+    assert lib.fq_version() >= 2

@@ -594,3 +594,13 @@ def test_backward_dw_single_row_closed_form(orc):
     _, dw = orc.rmsnorm_bwd_f64(x, torch.ones(16, dtype=torch.float64), g, 0.0)
     r = math.sqrt(float((x ** 2).mean()))
     assert torch.allclose(dw, (g * x / r)[0], rtol=1e-14, atol=0)
+
+
+def test_parallel_prologue_oracle_equals_one_call(orc):
+    """The token-sliced, thread-pooled oracle used at full size is the same computation as one call."""
+    from parity import oracle_prologue_parallel
+
+    d = wl.qk_inputs(301, 6, 2, 128, "bf16", "fp32", seed=4321, std=2.0, positions="uniform", outlier_frac=0.01)
+    q1, s1 = orc.qk_norm_rope_quant(d["qk"], d["wq"], d["wk"], d["cos"], d["sin"], 6, 2)
+    q2, s2 = oracle_prologue_parallel(orc, d, 6, 2)
+    assert torch.equal(q1, q2) and torch.equal(s1, s2)

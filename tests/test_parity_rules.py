@@ -73,3 +73,17 @@ def test_dw_one_ulp_rule_needs_the_rms_floor(orc):
     _, dw_bad, _ = orc.rmsnorm_bwd_rstd(d["x"][1:], d["w"], d["g"][1:], r[1:])
     with pytest.raises(AssertionError):
         assert_within_one_ulp(dw_bad, dw0)
+
+
+def test_rope_rule_bounds_how_many_elements_need_the_widening(orc):
+    """The widened rotated-column bound is not a blanket: it reports how many elements it accepts
+    only because of the widening and rejects a result that needs it more often than the oracle's
+    own rounding-order changes do (rstd moved 3 ulps on every row: a dozen of a million)."""
+    d = wl.rows_inputs(4097, 1536, 256, "bf16", "fp32", seed=970 + 4097)
+    y_ref = orc.rmsnorm_rope(d["x"], d["w"], d["cos"], d["sin"])
+    normed = orc.rmsnorm_fwd(d["x"], d["w"])
+    n = assert_rope_close(_emulate(d, rstd_ulps=3), y_ref, normed, d["cos"], d["sin"])
+    assert 0 < n <= 40
+    with pytest.raises(AssertionError):
+        assert_rope_close(_emulate(d, rstd_ulps=3), y_ref, normed, d["cos"], d["sin"], max_widened_frac=1e-6)
+    assert assert_rope_close(y_ref, y_ref, normed, d["cos"], d["sin"]) == 0

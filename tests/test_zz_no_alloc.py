@@ -4,8 +4,9 @@ It serves callers that cannot allocate device memory or pass a workspace (a plug
 framework owns every device buffer and hands over only tensors; a latency-critical loop that must
 never call cudaMalloc). It keeps its dw partial sums in the library's own fixed-size device array
 instead. These tests call it through the C ABI and compare it with fq_rmsnorm_bwd (the workspace
-entry point) under the parity tolerances, on two calls in a row with different shapes, so a call
-that read the previous call's leftovers would show up. This file is named to be collected last.
+entry point) and with the oracle under the parity tolerances, on two calls in a row with different
+shapes, so a call that read the previous call's leftovers would show up. This file is named to be
+collected last.
 """
 import ctypes
 
@@ -33,20 +34,26 @@ def _noalloc(lib, x, w, g, eps=1e-6):
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_workspace_entry_point_twice(cuda_ok):
+def test_noalloc_matches_workspace_entry_point_twice(orc, cuda_ok):
     import fp8_quant_memory_gb300 as fq
 
     lib = _capi.load()
     # 8192 x 4096 fills the built-in scratch exactly (256 chunks x 4096 columns x 4 bytes); the
     # second, smaller call reuses the array that the first left behind.
     for M, N, seed in ((8192, 4096, 11), (333, 1024, 12)):
-        d = {k: v.cuda() for k, v in wl.rmsnorm_inputs(M, N, "bf16", seed=seed).items()}
+        h = wl.rmsnorm_inputs(M, N, "bf16", seed=seed)
+        d = {k: v.cuda() for k, v in h.items()}
         dx, dw, dw32 = _noalloc(lib, d["x"], d["w"], d["g"])
         dx_ref, dw_ref, dw32_ref = fq.rmsnorm_bwd(d["x"], d["w"], d["g"])
         torch.cuda.synchronize()
         assert_storage_close(dx, dx_ref.cpu(), "dx")
         assert_dw_close(dw32, dw32_ref.cpu())
         assert_within_one_ulp(dw, dw_ref.cpu())
+        # and against the oracle (the Ch.17 page's RMSNormTileLang.backward)
+        dx_o, dw_o, dw32_o = orc.rmsnorm_bwd(h["x"], h["w"], h["g"])
+        assert_storage_close(dx, dx_o, "dx (oracle)")
+        assert_dw_close(dw32, dw32_o)
+        assert_within_one_ulp(dw, dw_o)
 
 
 def test_noalloc_rejects_problems_beyond_the_scratch():
