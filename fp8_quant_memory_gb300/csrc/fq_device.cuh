@@ -81,6 +81,53 @@ __device__ __forceinline__ float2 unpack_again<__half>(uint32_t u) {
   return make_float2(lo, hi);
 }
 
+// Products of 16-bit storage operands rounded once to fp32 (fma.rn.f32.{bf16,f16}: sm_100 and
+// later). Two packed elements (low half first) per call.
+template <typename T>
+struct Mixed;
+
+template <>
+struct Mixed<__nv_bfloat16> {
+  // (x0*w0, x1*w1), exact: the product of two 8-bit significands fits fp32; -0 + p keeps p's sign.
+  static __device__ __forceinline__ float2 mul(uint32_t x, uint32_t w) {
+    float2 r;
+    asm("{\n\t.reg .b16 x0, x1, w0, w1;\n\tmov.b32 {x0, x1}, %2;\n\tmov.b32 {w0, w1}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, x0, w0, %4;\n\tfma.rn.f32.bf16 %1, x1, w1, %4;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "r"(w), "f"(-0.0f));
+    return r;
+  }
+  // (a.x + x0^2, a.y + x1^2)
+  static __device__ __forceinline__ float2 sq_add(uint32_t x, float2 a) {
+    float2 r;
+    asm("{\n\t.reg .b16 x0, x1;\n\tmov.b32 {x0, x1}, %2;\n\t"
+        "fma.rn.f32.bf16 %0, x0, x0, %3;\n\tfma.rn.f32.bf16 %1, x1, x1, %4;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "f"(a.x), "f"(a.y));
+    return r;
+  }
+};
+
+template <>
+struct Mixed<__half> {
+  static __device__ __forceinline__ float2 mul(uint32_t x, uint32_t w) {
+    float2 r;
+    asm("{\n\t.reg .b16 x0, x1, w0, w1;\n\tmov.b32 {x0, x1}, %2;\n\tmov.b32 {w0, w1}, %3;\n\t"
+        "fma.rn.f32.f16 %0, x0, w0, %4;\n\tfma.rn.f32.f16 %1, x1, w1, %4;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "r"(w), "f"(-0.0f));
+    return r;
+  }
+  static __device__ __forceinline__ float2 sq_add(uint32_t x, float2 a) {
+    float2 r;
+    asm("{\n\t.reg .b16 x0, x1;\n\tmov.b32 {x0, x1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, x0, x0, %3;\n\tfma.rn.f32.f16 %1, x1, x1, %4;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "f"(a.x), "f"(a.y));
+    return r;
+  }
+};
+
 // Round a float2 to the storage format and back (the `.to(dtype)` cast of the definition).
 template <typename T>
 __device__ __forceinline__ float2 round_trip(float2 v) {

@@ -107,53 +107,6 @@ __device__ __forceinline__ uint32_t token_of(uint32_t r, uint64_t magic, int32_t
   return static_cast<uint32_t>((static_cast<uint64_t>(r) * magic) >> shift);
 }
 
-// Products of 16-bit storage operands rounded once to fp32 (fma.rn.f32.{bf16,f16}: sm_100 and
-// later). Two packed elements (low half first) per call.
-template <typename T>
-struct Mixed;
-
-template <>
-struct Mixed<__nv_bfloat16> {
-  // (x0*w0, x1*w1), exact: the product of two 8-bit significands fits fp32; -0 + p keeps p's sign.
-  static __device__ __forceinline__ float2 mul(uint32_t x, uint32_t w) {
-    float2 r;
-    asm("{\n\t.reg .b16 x0, x1, w0, w1;\n\tmov.b32 {x0, x1}, %2;\n\tmov.b32 {w0, w1}, %3;\n\t"
-        "fma.rn.f32.bf16 %0, x0, w0, %4;\n\tfma.rn.f32.bf16 %1, x1, w1, %4;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "r"(x), "r"(w), "f"(-0.0f));
-    return r;
-  }
-  // (a.x + x0^2, a.y + x1^2)
-  static __device__ __forceinline__ float2 sq_add(uint32_t x, float2 a) {
-    float2 r;
-    asm("{\n\t.reg .b16 x0, x1;\n\tmov.b32 {x0, x1}, %2;\n\t"
-        "fma.rn.f32.bf16 %0, x0, x0, %3;\n\tfma.rn.f32.bf16 %1, x1, x1, %4;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "r"(x), "f"(a.x), "f"(a.y));
-    return r;
-  }
-};
-
-template <>
-struct Mixed<__half> {
-  static __device__ __forceinline__ float2 mul(uint32_t x, uint32_t w) {
-    float2 r;
-    asm("{\n\t.reg .b16 x0, x1, w0, w1;\n\tmov.b32 {x0, x1}, %2;\n\tmov.b32 {w0, w1}, %3;\n\t"
-        "fma.rn.f32.f16 %0, x0, w0, %4;\n\tfma.rn.f32.f16 %1, x1, w1, %4;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "r"(x), "r"(w), "f"(-0.0f));
-    return r;
-  }
-  static __device__ __forceinline__ float2 sq_add(uint32_t x, float2 a) {
-    float2 r;
-    asm("{\n\t.reg .b16 x0, x1;\n\tmov.b32 {x0, x1}, %2;\n\t"
-        "fma.rn.f32.f16 %0, x0, x0, %3;\n\tfma.rn.f32.f16 %1, x1, x1, %4;\n\t}"
-        : "=f"(r.x), "=f"(r.y)
-        : "r"(x), "f"(a.x), "f"(a.y));
-    return r;
-  }
-};
-
 // Table entries of one sub-chunk (eight pairs) of one table row in shared memory -> 4 float2.
 template <typename TT>
 __device__ __forceinline__ void lds_table8(uint32_t addr, float2 (&v)[4]) {

@@ -547,17 +547,6 @@ __device__ __forceinline__ float scale_of(float m, float fmax, float rcp) {
   return __fmaf_rn(__fmaf_rn(-s0, fmax, m), rcp, s0);
 }
 
-template <typename T>
-__device__ __forceinline__ uint2 codes8(uint4 y, float s, float r, bool clamp, float fmax) {
-  float2 q[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    q[e] = div2_by(Elem<T>::unpack(rows::word(y, e)), s, r);
-    if (clamp) q[e] = make_float2(clamp_abs(q[e].x, fmax), clamp_abs(q[e].y, fmax));
-  }
-  return pack_e4m3x8(q[0], q[1], q[2], q[3]);
-}
-
 // Reduce-scatter of per-slot maxima over segments of SEG lanes (VPT values per lane, both powers of
 // two): at each level the lanes of a pair (lane mask O) keep opposite halves of their values and take
 // the maximum with the partner's copy of the half they keep; once a lane is down to one value the
@@ -579,10 +568,37 @@ __device__ __forceinline__ void seg_reduce_scatter(float (&m)[VPT], int lane) {
   if constexpr (O > 1) seg_reduce_scatter<(N > 1 ? N / 2 : 1), O / 2, VPT>(m, lane);
 }
 
+// norm8 that also folds the fp32 values' |v| maximum into m before they are rounded to the storage
+// dtype. Rounding to nearest is monotone and odd, so max_i |RN(v_i)| = RN(max_i |v_i|): the maximum
+// of the rounded y is the rounded maximum, taken without unpacking y again.
 template <typename T>
-__device__ __forceinline__ float absmax8(uint4 y) {
-  return absmax4(absmax4(0.f, Elem<T>::unpack(y.x), Elem<T>::unpack(y.y)), Elem<T>::unpack(y.z),
-                 Elem<T>::unpack(y.w));
+__device__ __forceinline__ uint4 norm8_max(uint4 u, uint4 wv, float2 rstd2, float& m) {
+  const float2 v0 = mul2(mul2(Elem<T>::unpack(u.x), rstd2), Elem<T>::unpack(wv.x));
+  const float2 v1 = mul2(mul2(Elem<T>::unpack(u.y), rstd2), Elem<T>::unpack(wv.y));
+  const float2 v2 = mul2(mul2(Elem<T>::unpack(u.z), rstd2), Elem<T>::unpack(wv.z));
+  const float2 v3 = mul2(mul2(Elem<T>::unpack(u.w), rstd2), Elem<T>::unpack(wv.w));
+  m = absmax4(absmax4(m, v0, v1), v2, v3);
+  return make_uint4(Elem<T>::pack(v0), Elem<T>::pack(v1), Elem<T>::pack(v2), Elem<T>::pack(v3));
+}
+
+// The storage dtype's rounding of one fp32 value, as fp32.
+template <typename T>
+__device__ __forceinline__ float round_to(float m) {
+  return Elem<T>::unpack(Elem<T>::pack(make_float2(m, m))).x;
+}
+
+// Codes of eight stored y values as e4m3(RN(y * r)), r = RN(1 / scale): within one fp32 ulp of the
+// quotient y / scale, so a code can differ from the quotient's only where y / scale sits at an e4m3
+// rounding boundary. The product keeps the sign of zero (y = -0 codes as 0x80, as y / scale does).
+template <typename T>
+__device__ __forceinline__ uint2 codes8_rcp(uint4 y, float r, bool clamp, float fmax) {
+  float2 q[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    q[e] = mul2(Elem<T>::unpack(rows::word(y, e)), splat2(r));
+    if (clamp) q[e] = make_float2(clamp_abs(q[e].x, fmax), clamp_abs(q[e].y, fmax));
+  }
+  return pack_e4m3x8(q[0], q[1], q[2], q[3]);
 }
 
 // Barrier of the TPR warps that share a row (named barrier 1 + team); team_all also ANDs a predicate
@@ -689,10 +705,16 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_wide_quant
     const float2 rstd2 = splat2(rstd_from_ss(ss, static_cast<float>(N), a.eps));
     // The last slot first: its rotary lanes read their partner's vector and their cos / sin entries
     // from the stage, which is released right after.
+    // Per row: one running |y| maximum; per group: one per slot (fp32, before rounding: see norm8_max).
+    float mk[GROUPED ? VW : 1];
+#pragma unroll
+    for (int k = 0; k < (GROUPED ? VW : 1); ++k) mk[k] = 0.f;
     {
       constexpr int k = VW - 1;
-      uint4 y = norm8<T>(xv[k], ws[lane + 32 * k], rstd2);
+      float mrot = 0.f;  // the slot's maximum: its normalised values, or after rotation its rotated ones
+      uint4 y = norm8_max<T>(xv[k], ws[lane + 32 * k], rstd2, mrot);
       if (rot) {
+        mrot = 0.f;
         const uint4 yp = norm8<T>(xs[32 * k + partner], ws[32 * k + partner], rstd2);
         float2 c[4], sn[4];
         const int64_t off = static_cast<int64_t>(wr) * half + 8 * pblk;
@@ -702,27 +724,23 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_wide_quant
         for (int e = 0; e < 4; ++e) {
           const float2 own = Elem<T>::unpack(rows::word(y, e)), other = Elem<T>::unpack(rows::word(yp, e));
           const float2 s2 = is_lo ? neg2(sn[e]) : sn[e];  // lo' = lo*c + hi*(-s), hi' = hi*c + lo*s
-          rows::set_word(y, e, Elem<T>::pack(add2(mul2(own, c[e]), mul2(other, s2))));
+          const float2 v = add2(mul2(own, c[e]), mul2(other, s2));
+          mrot = absmax4(mrot, v, make_float2(0.f, 0.f));
+          rows::set_word(y, e, Elem<T>::pack(v));
         }
       }
       xv[k] = y;
+      mk[GROUPED ? k : 0] = mrot;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&g.empty[rel_slot]);  // everything this warp needs is in registers
     uint4* yrow = a.y != nullptr
                       ? reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N) + vb
                       : nullptr;
-    // Per row: one running |y| maximum; per group: one per slot.
-    float mk[GROUPED ? VW : 1];
-    mk[0] = 0.f;
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
-      if (k < VW - 1) xv[k] = norm8<T>(xv[k], ws[lane + 32 * k], rstd2);
+      if (k < VW - 1) xv[k] = norm8_max<T>(xv[k], ws[lane + 32 * k], rstd2, mk[GROUPED ? k : 0]);
       if (yrow != nullptr) st_stream16(yrow + lane + 32 * k, xv[k]);
-      if constexpr (GROUPED)
-        mk[k] = absmax8<T>(xv[k]);
-      else
-        mk[0] = fmaxf(mk[0], absmax8<T>(xv[k]));
     }
     uint2* qrow = reinterpret_cast<uint2*>(a.q + static_cast<int64_t>(r) * N) + vb;
     if constexpr (!GROUPED) {
@@ -732,10 +750,10 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_wide_quant
         team_sync(team, 32 * TPR);
         m = fmaxf(xch[team * TPR][1], xch[team * TPR + 1][1]);
       }
-      const float sc = scale_of(fmaxf(m, 1e-4f), fmax, rcp);
+      const float sc = scale_of(fmaxf(round_to<T>(m), 1e-4f), fmax, rcp);
       const float rc = __frcp_rn(sc);
 #pragma unroll
-      for (int k = 0; k < VW; ++k) st_stream8(qrow + lane + 32 * k, codes8<T>(xv[k], sc, rc, clamp, fmax));
+      for (int k = 0; k < VW; ++k) st_stream8(qrow + lane + 32 * k, codes8_rcp<T>(xv[k], rc, clamp, fmax));
       if (hh == 0 && lane == 0) a.scale[r] = sc;
     } else if constexpr (GV > 0) {
       // One group per (slot, segment of GV lanes). The slots are reduced in blocks of BLK (the
@@ -756,7 +774,7 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_wide_quant
         if constexpr (GV > 1) seg_reduce_scatter<BLK, GV / 2, BLK>(m, lane);
 #pragma unroll
         for (int i = 0; i < NF; ++i) {
-          sgv[bk][i] = scale_of(fmaxf(m[i], 1e-4f), fmax, rcp);
+          sgv[bk][i] = scale_of(fmaxf(round_to<T>(m[i]), 1e-4f), fmax, rcp);
           rgv[bk][i] = __frcp_rn(sgv[bk][i]);
           const int k = bk * BLK + (BLK >= GV ? i + NF * j : (j * BLK) / GV);
           if (BLK >= GV || (j & (GV / BLK - 1)) == 0) srow[k * (32 / GV) + sgm] = sgv[bk][i];
@@ -766,9 +784,8 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_wide_quant
       for (int k = 0; k < VW; ++k) {
         const int bk = k / BLK, kb = k % BLK;
         const int src = sgm * GV + (BLK >= GV ? kb / NF : kb * (GV / BLK));
-        const float sg = __shfl_sync(0xffffffffu, sgv[bk][kb % NF], src);
         const float rg = __shfl_sync(0xffffffffu, rgv[bk][kb % NF], src);
-        st_stream8(qrow + lane + 32 * k, codes8<T>(xv[k], sg, rg, clamp, fmax));
+        st_stream8(qrow + lane + 32 * k, codes8_rcp<T>(xv[k], rg, clamp, fmax));
       }
     } else {
       // Group maxima: within a slot a group is gv consecutive lanes (gv <= 32) ...
@@ -788,9 +805,9 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_wide_quant
       float* srow = a.scale + static_cast<int64_t>(r) * G;
 #pragma unroll
       for (int k = 0; k < VW; ++k) {
-        const float sg = scale_of(fmaxf(mk[k], 1e-4f), fmax, rcp);
+        const float sg = scale_of(fmaxf(round_to<T>(mk[k]), 1e-4f), fmax, rcp);
         const float rg = __frcp_rn(sg);
-        st_stream8(qrow + lane + 32 * k, codes8<T>(xv[k], sg, rg, clamp, fmax));
+        st_stream8(qrow + lane + 32 * k, codes8_rcp<T>(xv[k], rg, clamp, fmax));
         const int col = 8 * (vb + lane + 32 * k);
         if ((col & (a.group - 1)) == 0) srow[col >> lg] = sg;  // the group's first vector
       }

@@ -165,3 +165,12 @@ def oracle_prologue_parallel(orc, d: dict, hq: int, hk: int, **kw):
     with ThreadPoolExecutor(len(bounds)) as ex:
         parts = list(ex.map(run, bounds))
     return torch.cat([p[0] for p in parts]), torch.cat([p[1] for p in parts])
+
+
+def assert_own_quantiser(q: torch.Tensor, s: torch.Tensor, q_own: torch.Tensor, s_own: torch.Tensor):
+    """The kernel's codes and scales against the oracle's quantiser applied to the kernel's own y:
+    scales bit for bit (the scale is RN(max(amax, 1e-4) / fp8_max) of the same rounded y), codes under
+    the code rule (kernels that code y as e4m3(RN(y * RN(1/scale))) differ from the quotient y / scale
+    only where it sits at an e4m3 rounding boundary)."""
+    assert torch.equal(s.detach().cpu(), s_own), "scales differ from the quantiser of the kernel's own y"
+    assert_codes_close(q, q_own, "codes vs the quantiser of the kernel's own y")

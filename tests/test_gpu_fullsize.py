@@ -14,7 +14,7 @@ import torch
 
 import fp8_quant_memory_gb300 as fq
 from fp8_quant_memory_gb300 import workloads as wl
-from parity import (assert_codes_close, assert_dw_close, assert_rope_close, assert_scale_close,
+from parity import (assert_own_quantiser, assert_codes_close, assert_dw_close, assert_rope_close, assert_scale_close,
                     assert_storage_close, assert_within_one_ulp, oracle_prologue_parallel,
                     scale_rows_by_own_y)
 
@@ -88,7 +88,7 @@ def test_rope_quant_tiny_full(orc, cuda_ok):
     y_ref, q_ref, s_ref = orc.rmsnorm_rope_quant(d["x"], d["w"], d["cos"], d["sin"])
     assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
     q_own, s_own = orc.quant_rows(y.cpu())
-    assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
+    assert_own_quantiser(q, s, q_own, s_own)
     assert_codes_close(q, q_ref)
     assert scale_rows_by_own_y(s, s_ref) == 0
     assert_scale_close(s, s_ref)

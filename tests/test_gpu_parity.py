@@ -8,7 +8,7 @@ import torch
 
 import fp8_quant_memory_gb300 as fq
 from fp8_quant_memory_gb300 import workloads as wl
-from parity import (assert_codes_close, assert_dw_close, assert_rope_close, assert_scale_close,
+from parity import (assert_own_quantiser, assert_codes_close, assert_dw_close, assert_rope_close, assert_scale_close,
                     assert_storage_close, assert_within_one_ulp, scale_rows_by_own_y)
 
 pytestmark = pytest.mark.gpu
@@ -129,9 +129,9 @@ def test_rmsnorm_rope_quant_parity(orc, cuda_ok, case, want_y):
     y, q, s = fq.rmsnorm_rope_quant(g["x"], g["w"], g["cos"], g["sin"], want_y=True)
     torch.cuda.synchronize()
     assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
-    # The codes and scales are the quantiser applied to the kernel's own y: exact.
+    # The scales are the quantiser applied to the kernel's own y exactly, the codes under the code rule.
     q_own, s_own = orc.quant_rows(y.cpu())
-    assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
+    assert_own_quantiser(q, s, q_own, s_own)
     assert_codes_close(q, q_ref)
     # Scales within 1e-5 of the oracle's, except rows accepted by the own-y rule above (a bf16 flip
     # of the amax element); none on the tiny workload, and rare elsewhere.
@@ -152,7 +152,7 @@ def test_rmsnorm_rope_quant_scalar_path_matches(orc, cuda_ok):
     y, q, s = fq.rmsnorm_rope_quant(misalign(g["x"]), g["w"], g["cos"], g["sin"])
     assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
     q_own, s_own = orc.quant_rows(y.cpu())
-    assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
+    assert_own_quantiser(q, s, q_own, s_own)
 
 
 # ----------------------------------------------------------------------------------- group-wise scales
@@ -180,9 +180,9 @@ def test_rmsnorm_rope_quant_groups_parity(orc, cuda_ok, case):
     torch.cuda.synchronize()
     assert s.shape == (M, N // gs)
     assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
-    # codes and scales are the group-wise quantiser applied to the kernel's own y: exact
+    # the group-wise quantiser applied to the kernel's own y: scales exactly, codes under the code rule
     q_own, s_own = orc.quant_groups(y.cpu(), gs)
-    assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
+    assert_own_quantiser(q, s, q_own, s_own)
     assert_codes_close(q, q_ref)
     n_own = scale_rows_by_own_y(s, s_ref)
     assert n_own <= max(1, s.numel() // 1000), f"{n_own} of {s.numel()} group scales accepted only by the own-y rule"
@@ -207,7 +207,7 @@ def test_rmsnorm_rope_quant_groups_scalar_path_matches(orc, cuda_ok):
     y, q, s = fq.rmsnorm_rope_quant_groups(misalign(g["x"]), g["w"], g["cos"], g["sin"], 128)
     assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
     q_own, s_own = orc.quant_groups(y.cpu(), 128)
-    assert torch.equal(q.cpu(), q_own) and torch.equal(s.cpu(), s_own)
+    assert_own_quantiser(q, s, q_own, s_own)
 
 
 # ----------------------------------------------------------------------------------- wide quantising rows
@@ -235,8 +235,8 @@ WIDE_QUANT_CASES = [
 def test_wide_rows_quant_stream_kernel(orc, cuda_ok, monkeypatch, case, kernel):
     """RMSNorm + RoPE + FP8 on >= 4096 rows of >= 1024 elements (the TMA-fed register-resident kernel
     where the width, rope_dim and group size allow it, the TMA-fed shared-memory kernel, and the
-    generic kernel on the same inputs): y against the oracle, codes and scales exactly the quantiser
-    of the kernel's own y."""
+    generic kernel on the same inputs): y against the oracle, scales exactly and codes under the code
+    rule against the quantiser of the kernel's own y."""
     _rows_kernel(monkeypatch, kernel)
     M, N, R, gs, dt, tdt, want_y = case
     d = wl.rows_inputs(M, N, R, dt, tdt, seed=970 + M)
@@ -251,7 +251,7 @@ def test_wide_rows_quant_stream_kernel(orc, cuda_ok, monkeypatch, case, kernel):
         q_own, s_own = orc.quant_groups(y.cpu(), gs)
     torch.cuda.synchronize()
     assert_rope_close(y, y_ref, orc.rmsnorm_fwd(d["x"], d["w"]), d["cos"], d["sin"])
-    assert torch.equal(q.cpu(), q_own) and torch.equal(sc.cpu(), s_own)
+    assert_own_quantiser(q, sc, q_own, s_own)
     assert_codes_close(q, q_ref)
     n_own = scale_rows_by_own_y(sc, s_ref)
     assert n_own <= max(1, sc.numel() // 1000), f"{n_own} of {sc.numel()} scales accepted only by the own-y rule"
@@ -307,7 +307,7 @@ def test_negative_zero_inputs_give_negative_zero_codes(orc, cuda_ok, monkeypatch
         assert torch.signbit(y.cpu()[i, j]) and float(y.cpu()[i, j]) == 0.0
         assert int(qc[i, j]) == 0x80
     assert int(qc[3, 11]) == 0x00
-    assert torch.equal(qc, q_own) and torch.equal(s.cpu(), s_own)
+    assert_own_quantiser(qc, s, q_own, s_own)
 
 
 # ----------------------------------------------------------------------------------- rmsnorm_rope
