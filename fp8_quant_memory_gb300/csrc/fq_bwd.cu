@@ -193,6 +193,10 @@ __global__ void __launch_bounds__(kThreads)
     bwd_stage2_kernel(const float* partial, int64_t chunks, int N, void* dw, float* dw_f32) {
   constexpr int kStreams = kThreads / 8;  // 32 chunk streams
   __shared__ float part[kStreams][33];
+  // Programmatic dependent launch: this grid may be scheduled while stage 1 drains; the wait orders
+  // every read of the partial sums after stage 1 has finished and its writes are visible.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int c4 = threadIdx.x & 7;
   const int k = threadIdx.x >> 3;
   const int j0 = blockIdx.x * 32 + 4 * c4;
@@ -552,8 +556,16 @@ void launch_bwd_t(const BwdArgs& a, cudaStream_t s) {
     else if (vec && nv <= 1024) launch_stage1<T, 256, 4, 1>(a, p, s);
     else bwd_stage1_scalar_kernel<T><<<static_cast<unsigned>(p.chunks), kThreads, 0, s>>>(a, p.rows_per_chunk);
   }
-  const unsigned grid2 = static_cast<unsigned>((a.N + 31) / 32);
-  bwd_stage2_kernel<T><<<grid2, kThreads, 0, s>>>(a.partial, p.chunks, a.N, a.dw, a.dw_f32);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>((a.N + 31) / 32));
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, bwd_stage2_kernel<T>, static_cast<const float*>(a.partial), p.chunks, a.N, a.dw, a.dw_f32);
 }
 
 }  // namespace

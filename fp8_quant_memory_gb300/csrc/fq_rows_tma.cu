@@ -24,6 +24,7 @@
 // y is written with 16-byte evict-first stores. x and the tables are read from HBM exactly once.
 #include <cstdlib>
 #include <string>
+#include <type_traits>
 
 #include "fq_device.cuh"
 #include "fq_internal.h"
@@ -191,9 +192,10 @@ __device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* s
 }
 
 // ---------------------------------------------------------------------------------- narrow rows
-// Up to four vectors per lane the kernel fits two CTAs per SM without spilling; wider rows take one.
+// Up to four vectors per lane (and the four-lane fp16 rotary shape) the kernel fits two CTAs per SM
+// without spilling; wider rows take one.
 template <typename T, typename TT, int MODE, int LPR, int HS, int TS>
-__global__ void __launch_bounds__(kThreads, (HS + 2 * TS) <= 4 ? 2 : 1) rows_tma_kernel(const StreamArgs p) {
+__global__ void __launch_bounds__(kThreads, ((HS + 2 * TS) <= 4 || LPR <= 4) ? 2 : 1) rows_tma_kernel(const StreamArgs p) {
   extern __shared__ unsigned char smem_raw[];
   constexpr int kV = HS + 2 * TS;
   constexpr int SR = kConsumerWarps * (32 / LPR);  // one row per lane group per stage
@@ -1079,7 +1081,14 @@ bool dispatch_narrow(const RowArgs& a, cudaStream_t s) {
   if constexpr (MODE == MODE_FWD) {
     FQ_TMA_TRY(8, 2, 0) FQ_TMA_TRY(16, 2, 0) FQ_TMA_TRY(32, 2, 0)
   } else {
-    FQ_TMA_TRY(8, 0, 1) FQ_TMA_TRY(8, 2, 1) FQ_TMA_TRY(16, 2, 1) FQ_TMA_TRY(32, 2, 1) FQ_TMA_TRY(32, 4, 1)
+    FQ_TMA_TRY(8, 0, 1)
+    // fp16 rows of up to 128 head and 64 rotary columns (the 65536 x 192 workload: 16 head and 4 rotary
+    // vectors): four lanes per row fill every slot and need two shuffle levels, 10.85 against 11.11 us
+    // for eight lanes. (bf16 would spill at two CTAs per SM in this shape.)
+    if constexpr (std::is_same<T, __half>::value) {
+      FQ_TMA_TRY(4, 4, 1)
+    }
+    FQ_TMA_TRY(8, 2, 1) FQ_TMA_TRY(16, 2, 1) FQ_TMA_TRY(32, 2, 1) FQ_TMA_TRY(32, 4, 1)
   }
 #undef FQ_TMA_TRY
   return false;
