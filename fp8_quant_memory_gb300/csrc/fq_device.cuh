@@ -223,9 +223,23 @@ __device__ __forceinline__ uint32_t e4m3x2(float2 v) {  // v.x -> low byte, v.y 
   return d;
 }
 
+// 4 quotients -> 4 codes in one word (a.x in the lowest byte). The two 16-bit halves are joined in
+// the same inline block as the conversions: measured one instruction per word less than shifting
+// and or-ing two zero-extended halves.
+__device__ __forceinline__ uint32_t e4m3x4(float2 a, float2 b) {
+  uint32_t d;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 // 8 quotients -> 8 codes (element 0 at the lowest address).
 __device__ __forceinline__ uint2 pack_e4m3x8(float2 a, float2 b, float2 c, float2 d) {
-  return make_uint2(e4m3x2(a) | (e4m3x2(b) << 16), e4m3x2(c) | (e4m3x2(d) << 16));
+  return make_uint2(e4m3x4(a, b), e4m3x4(c, d));
 }
 
 __device__ __forceinline__ float clamp_abs(float v, float m) { return fminf(fmaxf(v, -m), m); }

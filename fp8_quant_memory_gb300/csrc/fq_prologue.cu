@@ -70,7 +70,7 @@ struct PrologueArgs {
   uint8_t* q;
   float* scale;
   unsigned int* status;
-  uint64_t magic;        // t = (r * magic) >> shift == r / H for r < 2^31
+  uint32_t magic;        // t = (r * magic) >> shift == r / H for r < 2^31 (magic < 2^32 for every H)
   int32_t shift;
   int32_t rows;          // T * H
   int32_t H, Hq;
@@ -103,8 +103,8 @@ __device__ __forceinline__ float rcp_approx(float v) {
   return r;
 }
 
-__device__ __forceinline__ uint32_t token_of(uint32_t r, uint64_t magic, int32_t shift) {
-  return static_cast<uint32_t>((static_cast<uint64_t>(r) * magic) >> shift);
+__device__ __forceinline__ uint32_t token_of(uint32_t r, uint32_t magic, int32_t shift) {
+  return static_cast<uint32_t>((static_cast<uint64_t>(r) * magic) >> shift);  // one 32 x 32 -> 64 product
 }
 
 // Table entries of one sub-chunk (eight pairs) of one table row in shared memory -> 4 float2.
@@ -188,8 +188,8 @@ __device__ __forceinline__ void quant_row(const PrologueArgs& a, uint32_t xrow, 
         h0 = make_float2(clamp_abs(h0.x, a.fp8_max), clamp_abs(h0.y, a.fp8_max));
         h1 = make_float2(clamp_abs(h1.x, a.fp8_max), clamp_abs(h1.y, a.fp8_max));
       }
-      cl[m][e / 2] = e4m3x2(l0) | (e4m3x2(l1) << 16);
-      ch[m][e / 2] = e4m3x2(h0) | (e4m3x2(h1) << 16);
+      cl[m][e / 2] = e4m3x4(l0, l1);
+      ch[m][e / 2] = e4m3x4(h0, h1);
     }
   }
   if (live) {
@@ -455,10 +455,13 @@ bool launch_sr(const RowArgs& a, int dtype, int table_dtype, cudaStream_t s) {
   p.fp8_max = a.fp8_max;
   p.rcp_fp8_max = static_cast<float>(1.0 / static_cast<double>(a.fp8_max));
   // r / H as (r * magic) >> shift for every r < 2^31: shift = 31 + ceil(log2 H), magic = ceil(2^shift / H).
+  // magic < 2^shift / 2^(ceil(log2 H) - 1) = 2^32 (and 2^31 for H = 1), so it fits 32 bits.
   int lg = 0;
   while ((1LL << lg) < a.H) ++lg;
   p.shift = 31 + lg;
-  p.magic = static_cast<uint64_t>(((static_cast<unsigned __int128>(1) << p.shift) + a.H - 1) / a.H);
+  const uint64_t magic = static_cast<uint64_t>(((static_cast<unsigned __int128>(1) << p.shift) + a.H - 1) / a.H);
+  if (magic > 0xffffffffull) return false;
+  p.magic = static_cast<uint32_t>(magic);
   const int tab_rows = (SR - 1) / a.H + 2;  // tokens one stage can touch
   p.tab_block = ((tab_rows * (kD / 2) * tsz) + 127) & ~127;
   p.stage_bytes = ((2 * half_tile<SR>() + 2 * p.tab_block) + 1023) & ~1023;
