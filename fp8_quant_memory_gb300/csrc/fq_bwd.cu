@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kThreads, 2) bwd_stage1_kernel(const BwdArgs a
 #pragma unroll
     for (int b = 0; b < RB; ++b) {
       const float rstd = (a.rstd_in != nullptr) ? (rv[b] ? a.rstd_in[row[b]] : 1.f) : rstd_approx(ss[b], fN, a.eps);
-      const float c = __fdiv_rn(__fmul_rn(sg[b], rstd), fN);
+      const float c = div_n(__fmul_rn(sg[b], rstd), fN);
       const float2 rstd2 = splat2(rstd), c2 = splat2(c);
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads) bwd_stage1_scalar_kernel(const BwdAr
     }
     __syncthreads();
     const float rstd = (a.rstd_in != nullptr) ? a.rstd_in[r] : rstd_approx(ss, static_cast<float>(N), a.eps);
-    const float c = __fdiv_rn(__fmul_rn(sg, rstd), static_cast<float>(N));
+    const float c = div_n(__fmul_rn(sg, rstd), static_cast<float>(N));
     for (int j = tid; j < N; j += kThreads) {
       const float gf = Elem<T>::load1(a.g, r * N + j);
       const float xn = __fmul_rn(Elem<T>::load1(a.x, r * N + j), rstd);
@@ -449,14 +449,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2) bwd_stage1_stream_kernel(co
       rb[2 * warp + 1] = sg_w;
     }
     if (!consumers_all(got)) return;  // a stage never arrived: every consumer stops here
+    // the warps' sums in fixed order, two warps per 16-byte read (rb is 16-byte aligned)
     float ss = 0.f, sg = 0.f;
 #pragma unroll
-    for (int w = 0; w < kStreamWarps; ++w) {  // fixed order
-      ss += rb[2 * w];
-      sg += rb[2 * w + 1];
+    for (int w = 0; w < kStreamWarps; w += 2) {
+      const float4 v = reinterpret_cast<const float4*>(rb)[w / 2];
+      ss += v.x;
+      sg += v.y;
+      ss += v.z;
+      sg += v.w;
     }
     const float rstd = SAVED ? a.rstd_in[c0 + k] : rstd_approx(ss, fN, a.eps);
-    const float c = __fdiv_rn(__fmul_rn(sg, rstd), fN);
+    const float c = div_n(__fmul_rn(sg, rstd), fN);
     const float2 rstd2 = splat2(rstd), c2 = splat2(c);
     T* dxrow = static_cast<T*>(a.dx) + (c0 + k) * N;
 #pragma unroll

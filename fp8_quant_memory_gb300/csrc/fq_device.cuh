@@ -270,10 +270,19 @@ __device__ __forceinline__ float absmax4(float m, float2 a, float2 b) {
   return r;
 }
 
-// rstd from the row's sum of squares: 1/sqrt(ss/N + eps), every step correctly rounded in fp32.
-// Used where an FP8 code or a saved rstd depends on it.
+// x / n correctly rounded, for a row length n >= 1. When n is a power of two, 1/n is exact and x * (1/n)
+// is the same real number as x / n, so one rounded product gives the quotient bit for bit (subnormal
+// results included); other lengths take the IEEE division.
+__device__ __forceinline__ float div_n(float x, float n) {
+  const uint32_t b = __float_as_uint(n);
+  return (b & 0x7fffffu) == 0u ? __fmul_rn(x, __uint_as_float(0x7f000000u - b)) : __fdiv_rn(x, n);
+}
+
+// rstd from the row's sum of squares: 1/sqrt(ss/N + eps), every step correctly rounded in fp32 (the
+// correctly rounded reciprocal is the IEEE quotient 1/s). Used where an FP8 code or a saved rstd
+// depends on it.
 __device__ __forceinline__ float rstd_from_ss(float ss, float n, float eps) {
-  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, n), eps)));
+  return __frcp_rn(__fsqrt_rn(__fadd_rn(div_n(ss, n), eps)));
 }
 
 // The same with the hardware reciprocal square root and the approximate quotient (each within 2 ulp

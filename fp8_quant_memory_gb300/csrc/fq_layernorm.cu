@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kThreads) ln_vec_kernel(const RowArgs a) {
       s1 = add2(s1, add2(Elem<T>::unpack(xv[k].z), Elem<T>::unpack(xv[k].w)));
     }
     const float2 st = add2(s0, s1);
-    const float mean = __fdiv_rn(group_sum<32>(st.x + st.y), fN);
+    const float mean = div_n(group_sum<32>(st.x + st.y), fN);
     const float2 mean2 = splat2(mean);
     // pass 2: variance of the deviations (vectors past the row end hold zeros: not counted)
     float2 q0 = make_float2(0.f, 0.f), q1 = make_float2(0.f, 0.f);
@@ -63,8 +63,8 @@ __global__ void __launch_bounds__(kThreads) ln_vec_kernel(const RowArgs a) {
       }
     }
     const float2 qt = add2(q0, q1);
-    const float var = __fdiv_rn(group_sum<32>(qt.x + qt.y), fN);
-    const float2 rstd2 = splat2(__fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, a.eps))));
+    const float var = div_n(group_sum<32>(qt.x + qt.y), fN);
+    const float2 rstd2 = splat2(__frcp_rn(__fsqrt_rn(__fadd_rn(var, a.eps))));
     // pass 3: y
     T* yrow = static_cast<T*>(a.y) + static_cast<int64_t>(r) * N;
 #pragma unroll
@@ -99,14 +99,14 @@ __global__ void __launch_bounds__(kThreads) ln_scalar_kernel(const RowArgs a, in
        r += static_cast<int64_t>(gridDim.x) * kWarps) {
     float s = 0.f;
     for (int j = lane; j < N; j += 32) s = __fadd_rn(s, ld1(dt, a.x, r * N + j));
-    const float mean = __fdiv_rn(group_sum<32>(s), fN);
+    const float mean = div_n(group_sum<32>(s), fN);
     float q = 0.f;
     for (int j = lane; j < N; j += 32) {
       const float c = __fsub_rn(ld1(dt, a.x, r * N + j), mean);
       q = __fmaf_rn(c, c, q);
     }
-    const float var = __fdiv_rn(group_sum<32>(q), fN);
-    const float rstd = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, a.eps)));
+    const float var = div_n(group_sum<32>(q), fN);
+    const float rstd = __frcp_rn(__fsqrt_rn(__fadd_rn(var, a.eps)));
     for (int j = lane; j < N; j += 32) {
       const float c = __fsub_rn(ld1(dt, a.x, r * N + j), mean);
       const float n = __fmul_rn(__fmul_rn(c, rstd), ld1(dt, a.wq, j));

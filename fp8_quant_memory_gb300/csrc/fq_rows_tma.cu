@@ -974,7 +974,7 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_ln_kernel(
       team_sync(team, 32 * TPR);
       sum = xch[team * TPR][0] + xch[team * TPR + 1][0];
     }
-    const float mean = __fdiv_rn(sum, fN);
+    const float mean = div_n(sum, fN);
     const float2 mean2 = splat2(mean);
     float2 q0 = make_float2(0.f, 0.f), q1 = q0, q2 = q0, q3 = q0;
 #pragma unroll
@@ -994,8 +994,8 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_ln_kernel(
       team_sync(team, 32 * TPR);
       qs = xch[team * TPR][1] + xch[team * TPR + 1][1];
     }
-    const float var = __fdiv_rn(qs, fN);
-    const float2 rstd2 = splat2(__fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(var, a.eps))));
+    const float var = div_n(qs, fN);
+    const float2 rstd2 = splat2(__frcp_rn(__fsqrt_rn(__fadd_rn(var, a.eps))));
     uint4* yrow = reinterpret_cast<uint4*>(static_cast<T*>(a.y) + static_cast<int64_t>(r) * N) + vb;
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
