@@ -193,22 +193,25 @@ __device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* s
 
 // ---------------------------------------------------------------------------------- narrow rows
 // Up to four vectors per lane (and the four-lane fp16 rotary shape) the kernel fits two CTAs per SM
-// without spilling; wider rows take one.
-template <typename T, typename TT, int MODE, int LPR, int HS, int TS>
+// without spilling; wider rows take one. G consumer groups take the stages in turn (stage k goes to
+// group k % G): with two, a stage holds half as many rows, so a launch has twice as many work units
+// to spread over the SMs.
+template <typename T, typename TT, int MODE, int LPR, int HS, int TS, int G = 1>
 __global__ void __launch_bounds__(kThreads, ((HS + 2 * TS) <= 4 || LPR <= 4) ? 2 : 1) rows_tma_kernel(const StreamArgs p) {
   extern __shared__ unsigned char smem_raw[];
   constexpr int kV = HS + 2 * TS;
-  constexpr int SR = kConsumerWarps * (32 / LPR);  // one row per lane group per stage
-  const Ring g = ring_setup(p, smem_raw, kConsumerWarps);
+  constexpr int kGroupWarps = kConsumerWarps / G;
+  constexpr int SR = kGroupWarps * (32 / LPR);  // one row per lane group per stage
+  const Ring g = ring_setup(p, smem_raw, kGroupWarps, kConsumerWarps);
   const RowArgs& a = p.a;
   const int warp = threadIdx.x >> 5, lane32 = threadIdx.x & 31;
   if (warp == kConsumerWarps) {
     if (lane32 == 0)
-      produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, SR, sizeof(T), sizeof(TT));
+      produce(p, g.smem, g.full, g.empty, g.wbar, g.w, g.resp, g.cbar, g.stage_row, SR, sizeof(T), sizeof(TT), G);
     return;
   }
   const int lane = lane32 & (LPR - 1);
-  const int l = warp * (32 / LPR) + lane32 / LPR;  // row within each stage
+  const int l = (warp % kGroupWarps) * (32 / LPR) + lane32 / LPR;  // row within each stage
   const int N = a.N;
   const int hv = (N - a.R) >> 3, th = a.R >> 4, half = a.R >> 1;
   const float fN = static_cast<float>(N);
@@ -219,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, ((HS + 2 * TS) <= 4 || LPR <= 4) ? 2
   for (int s = 0; s < kV; ++s)
     wv[s] = slot_ok<LPR, HS, TS>(s, lane, hv, th) ? ld_cached16(w + slot_col<LPR, HS, TS>(s, lane, hv, th))
                                                   : make_uint4(0u, 0u, 0u, 0u);
-  int slot = 0;
+  int slot = warp / kGroupWarps;  // this group's first stage; it takes every G-th after it
   uint32_t phase = 0;
   for (;;) {
     if (!mbar_wait(kWaitLimitNs, &g.full[slot], phase)) {
@@ -242,8 +245,9 @@ __global__ void __launch_bounds__(kThreads, ((HS + 2 * TS) <= 4 || LPR <= 4) ? 2
                                                     st + p.tab_off + p.tab_block, static_cast<int64_t>(lr) * half, wv);
     __syncwarp();
     if (lane32 == 0) mbar_arrive(&g.empty[slot]);  // x and this stage's table rows have been read
-    if (++slot == p.stages) {
-      slot = 0;
+    slot += G;  // the ring holds a multiple of G stages: a slot always belongs to the same group
+    if (slot >= p.stages) {
+      slot -= p.stages;
       phase ^= 1u;
     }
   }
@@ -1063,13 +1067,14 @@ bool launch_stream(K kern, int threads, StreamArgs p, int stage_rows, int x_row_
   return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess;
 }
 
-template <typename T, typename TT, int MODE, int LPR, int HS, int TS>
+template <typename T, typename TT, int MODE, int LPR, int HS, int TS, int G = 1>
 bool launch_narrow(const RowArgs& a, cudaStream_t s) {
   StreamArgs p{};
   p.a = a;
-  constexpr int SR = kConsumerWarps * (32 / LPR);
-  return launch_stream(rows_tma_kernel<T, TT, MODE, LPR, HS, TS>, kThreads, p, SR,
-                       a.N * static_cast<int>(sizeof(T)), (a.R / 2) * static_cast<int>(sizeof(TT)), s);
+  constexpr int SR = (kConsumerWarps / G) * (32 / LPR);
+  return launch_stream(rows_tma_kernel<T, TT, MODE, LPR, HS, TS, G>, kThreads, p, SR,
+                       a.N * static_cast<int>(sizeof(T)), (a.R / 2) * static_cast<int>(sizeof(TT)), s, 0, 0,
+                       48 * 1024, G);
 }
 
 template <typename T, typename TT, int MODE>
@@ -1084,9 +1089,10 @@ bool dispatch_narrow(const RowArgs& a, cudaStream_t s) {
     FQ_TMA_TRY(8, 0, 1)
     // fp16 rows of up to 128 head and 64 rotary columns (the 65536 x 192 workload: 16 head and 4 rotary
     // vectors): four lanes per row fill every slot and need two shuffle levels, 10.85 against 11.11 us
-    // for eight lanes. (bf16 would spill at two CTAs per SM in this shape.)
+    // for eight lanes; two consumer groups (32-row stages, 2048 work units instead of 1024 for 304
+    // resident CTAs) 10.45 against 11.00 us. (bf16 would spill at two CTAs per SM in this shape.)
     if constexpr (std::is_same<T, __half>::value) {
-      FQ_TMA_TRY(4, 4, 1)
+      if (hv <= 16 && th <= 4) return launch_narrow<T, TT, MODE, 4, 4, 1, 2>(a, s);
     }
     FQ_TMA_TRY(8, 2, 1) FQ_TMA_TRY(16, 2, 1) FQ_TMA_TRY(32, 2, 1) FQ_TMA_TRY(32, 4, 1)
   }
