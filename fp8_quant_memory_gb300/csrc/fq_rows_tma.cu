@@ -19,7 +19,7 @@
 //     two or three passes over the staged row; the weight row is copied into shared memory once per
 //     CTA. Two CTAs share an SM, so a stage is four rows and the ring fills and drains in small steps;
 //   - wide rows, registers (RMSNorm forward, RMSNorm + RoPE + FP8 and LayerNorm on rows of 1024 to
-//     4096): one CTA per SM, three consumer groups of four warps taking the stages in turn, one or
+//     4096): one CTA per SM, two to four consumer groups of four warps taking the stages in turn, one or
 //     two warps per row; a warp copies its row into registers and releases the stage at once.
 // y is written with 16-byte evict-first stores. x and the tables are read from HBM exactly once.
 #include <cstdlib>
@@ -194,8 +194,8 @@ __device__ __forceinline__ Ring ring_setup(const StreamArgs& p, unsigned char* s
 // ---------------------------------------------------------------------------------- narrow rows
 // Up to four vectors per lane (and the four-lane fp16 rotary shape) the kernel fits two CTAs per SM
 // without spilling; wider rows take one. G consumer groups take the stages in turn (stage k goes to
-// group k % G): with two, a stage holds half as many rows, so a launch has twice as many work units
-// to spread over the SMs.
+// group k % G): a stage holds 1/G of the rows, so a launch has G times as many work units to spread
+// over the SMs.
 template <typename T, typename TT, int MODE, int LPR, int HS, int TS, int G = 1>
 __global__ void __launch_bounds__(kThreads, ((HS + 2 * TS) <= 4 || LPR <= 4) ? 2 : 1) rows_tma_kernel(const StreamArgs p) {
   extern __shared__ unsigned char smem_raw[];
@@ -525,9 +525,8 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_rope_kernel(const 
 // ------------------------------------------------------- wide rows, FP8, register-resident rows
 // RMSNorm + NeoX partial RoPE + FP8 codes with one scale per row or per group of columns
 // ("rmsnorm_rope_quant.py" (Ch.13 fusion), rms_norm_rope_quant_fused) for rows of N = 256 * VPT
-// elements, rope_dim <= 256, group sizes that are powers of two. Twelve consumer warps in three
-// groups of four take the stages in turn (one CTA per SM, so a stage of four rows and its table rows
-// fit six times); each warp copies its row -- VPT 16-byte vectors per lane, vector v = lane + 32k --
+// elements, rope_dim <= 256, group sizes that are powers of two. Consumer warps in groups of four
+// take the stages in turn (one CTA per SM; the ring holds a multiple of the group count); each warp copies its row -- VPT 16-byte vectors per lane, vector v = lane + 32k --
 // into registers, and with it, on the lanes that hold rotary vectors (all in the last slot, since
 // N / 8 is a multiple of 32 and rope_dim / 8 <= 32), the rotation partner's vector and the eight
 // cos and sin entries of its pairs; then it releases the stage. Everything after that runs on
@@ -537,14 +536,22 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_rope_kernel(const 
 // definition); the |y| maxima (per row over the warp; per group over the group's lanes of a slot,
 // then across slots for groups of more than 32 vectors); and the codes as correctly rounded
 // quotients. The warp's rows and the stage ring are independent, so the copy of the next stages
-// overlaps this work, and at most three rows per SM wait for data at a time.
+// overlaps this work.
 // Warps per consumer group (a stage holds kRegRows / TPR rows). Consumer groups take the stages in
-// turn: three when a warp holds up to 12 vector slots (13 warps: registers are allotted for 16, so
-// 128 per thread), two for 16 slots, whose 64 registers of row data need more room (168 per
-// thread). Rows of 4096 are split over two warps of 8 slots each, so they run with three groups.
+// turn: four when a warp holds up to 8 vector slots (17 warps, 96 registers per thread), three for
+// 12 slots (13 warps: registers are allotted for 16, so 128 per thread), two for 16 slots, whose 64
+// registers of row data need more room (168 per thread). Rows of 4096 are split over two warps of 8
+// slots each, so they run with four groups: eight rows in flight per SM instead of six took the
+// 4096 x 4096 workloads from 11.79 to 11.34 us (RMSNorm + RoPE + FP8), 12.11 to 11.76 us
+// (LayerNorm) and the 8192 x 4096 RMSNorm forward from 21.48 to 21.28 us. The kernel with group-wise
+// scales keeps three groups at 8 slots: at 96 registers it spills 12 bytes and ran 1% slower.
 constexpr int kRegRows = 4;
-__host__ __device__ constexpr int reg_groups(int vpt) { return vpt <= 12 ? 3 : 2; }
-__host__ __device__ constexpr int reg_threads(int vpt) { return (kRegRows * reg_groups(vpt) + 1) * 32; }
+__host__ __device__ constexpr int reg_groups(int vpt, bool grouped = false) {
+  return vpt <= 8 && !grouped ? 4 : (vpt <= 12 ? 3 : 2);
+}
+__host__ __device__ constexpr int reg_threads(int vpt, bool grouped = false) {
+  return (kRegRows * reg_groups(vpt, grouped) + 1) * 32;
+}
 
 // RN(m / fmax) from rcp = RN(1 / fmax): one product and Markstein's correction (the residual
 // m - s0 * fmax is exact in one FMA). m >= 1e-4 and fmax a normal float keep every step normal.
@@ -630,10 +637,10 @@ __device__ __forceinline__ bool team_all(bool v, int team, int threads) {
 // pair adds its sums of squares and takes the larger |y| maximum through shared memory, and a group
 // never spans the two halves (the host sends groups wider than half a row elsewhere).
 template <typename T, typename TT, int VPT, int GV, int TPR>
-__global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_wide_quant_kernel(const StreamArgs p) {
+__global__ void __launch_bounds__(reg_threads(VPT / TPR, GV != 0), 1) rows_tma_wide_quant_kernel(const StreamArgs p) {
   constexpr bool GROUPED = GV != 0;
   constexpr int VW = VPT / TPR;                  // slots per warp
-  constexpr int kRegGroups = reg_groups(VW);
+  constexpr int kRegGroups = reg_groups(VW, GROUPED);
   constexpr int kRegWarps = kRegRows * kRegGroups;
   constexpr int SR = kRegRows / TPR;             // rows per stage
   static_assert(TPR == 1 || TPR == 2, "one or two warps per row");
@@ -1089,10 +1096,12 @@ bool dispatch_narrow(const RowArgs& a, cudaStream_t s) {
     FQ_TMA_TRY(8, 0, 1)
     // fp16 rows of up to 128 head and 64 rotary columns (the 65536 x 192 workload: 16 head and 4 rotary
     // vectors): four lanes per row fill every slot and need two shuffle levels, 10.85 against 11.11 us
-    // for eight lanes; two consumer groups (32-row stages, 2048 work units instead of 1024 for 304
-    // resident CTAs) 10.45 against 11.00 us. (bf16 would spill at two CTAs per SM in this shape.)
+    // for eight lanes; consumer groups that take the stages in turn make the work units finer for
+    // the 304 resident CTAs: four groups (16-row stages, 4096 units) 10.28 us, two (32-row stages)
+    // 10.43-10.45, one (64-row stages, 1024 units) 11.00. (bf16 would spill at two CTAs per SM in this
+    // shape.)
     if constexpr (std::is_same<T, __half>::value) {
-      if (hv <= 16 && th <= 4) return launch_narrow<T, TT, MODE, 4, 4, 1, 2>(a, s);
+      if (hv <= 16 && th <= 4) return launch_narrow<T, TT, MODE, 4, 4, 1, 4>(a, s);
     }
     FQ_TMA_TRY(8, 2, 1) FQ_TMA_TRY(16, 2, 1) FQ_TMA_TRY(32, 2, 1) FQ_TMA_TRY(32, 4, 1)
   }
@@ -1151,9 +1160,10 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
     if (quant && !staged && a.N % 256 == 0 && (vpt == 4 || vpt == 8 || vpt == 12 || vpt == 16) && a.R <= 256 &&
         a.R % 16 == 0 && pow2_group) {
 #define FQ_REG_K2(T, TT, V, GV, TPR)                                                                         \
-  return launch_stream(rows_tma_wide_quant_kernel<T, TT, V, GV, TPR>, reg_threads((V) / (TPR)), p,              \
-                       kRegRows / (TPR), xrow, trow, s, 0, 220 * 1024, 96 * 1024, reg_groups((V) / (TPR)));
-// Rows of 4096: two warps per row, so that three consumer groups fit the registers. (A power-of-two
+  return launch_stream(rows_tma_wide_quant_kernel<T, TT, V, GV, TPR>, reg_threads((V) / (TPR), (GV) != 0), p,  \
+                       kRegRows / (TPR), xrow, trow, s, 0, 220 * 1024, 96 * 1024,                         \
+                       reg_groups((V) / (TPR), (GV) != 0));
+// Rows of 4096: two warps per row, so that three or four consumer groups fit the registers. (A power-of-two
 // group narrower than the row is at most half of it, so no group spans the two warps; a group of the
 // whole row takes the per-row kernel, which does not read the group size.)
 #define FQ_REG_K(T, TT, V, GV)                                                      \
