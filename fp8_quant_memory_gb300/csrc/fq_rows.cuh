@@ -100,16 +100,27 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
   constexpr int kV = HS + 2 * TS;  // vector slots per lane: head..., tail-lo..., tail-hi...
   const int N = a.N;
 
-  // a2: sum of squares -> rstd
+  // a2: sum of squares -> rstd. RMSNorm + RoPE without quantisation (MODE_ROPE) takes the squares
+  // straight from the 16-bit storage operands (one FMA each, exact products) and normalises as
+  // (x * w) * rstd with x * w exact: the same values as (x * rstd) * w up to one fp32 rounding,
+  // the size of the approximate rstd this mode already uses, and no unpacking of x or w.
+  constexpr bool kMixed = MODE == MODE_ROPE;
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int s = 0; s < kV; ++s) {
-    const float2 f0 = Elem<T>::unpack(xv[s].x), f1 = Elem<T>::unpack(xv[s].y);
-    const float2 f2 = Elem<T>::unpack(xv[s].z), f3 = Elem<T>::unpack(xv[s].w);
-    acc0 = fma2(f0, f0, acc0);
-    acc1 = fma2(f1, f1, acc1);
-    acc0 = fma2(f2, f2, acc0);
-    acc1 = fma2(f3, f3, acc1);
+    if constexpr (kMixed) {
+      acc0 = Mixed<T>::sq_add(xv[s].x, acc0);
+      acc1 = Mixed<T>::sq_add(xv[s].y, acc1);
+      acc0 = Mixed<T>::sq_add(xv[s].z, acc0);
+      acc1 = Mixed<T>::sq_add(xv[s].w, acc1);
+    } else {
+      const float2 f0 = Elem<T>::unpack(xv[s].x), f1 = Elem<T>::unpack(xv[s].y);
+      const float2 f2 = Elem<T>::unpack(xv[s].z), f3 = Elem<T>::unpack(xv[s].w);
+      acc0 = fma2(f0, f0, acc0);
+      acc1 = fma2(f1, f1, acc1);
+      acc0 = fma2(f2, f2, acc0);
+      acc1 = fma2(f3, f3, acc1);
+    }
   }
   const float2 acc = add2(acc0, acc1);
   const float ss = group_sum<LPR>(acc.x + acc.y);
@@ -139,7 +150,8 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
     uint4 packed;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const float2 n = mul2(mul2(Elem<T>::unpack(word(xv[s], k)), rstd2), Elem<T>::unpack(word(wv, k)));
+      const float2 n = kMixed ? mul2(Mixed<T>::mul(word(xv[s], k), word(wv, k)), rstd2)
+                              : mul2(mul2(Elem<T>::unpack(word(xv[s], k)), rstd2), Elem<T>::unpack(word(wv, k)));
       if constexpr (MODE == MODE_QK) {
         yf[s][k] = n;
       } else {
@@ -183,8 +195,10 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
       uint4 plo4, phi4;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        float2 lo = mul2(mul2(Elem<T>::unpack(word(xv[slo], k)), rstd2), Elem<T>::unpack(word(wlo, k)));
-        float2 hi = mul2(mul2(Elem<T>::unpack(word(xv[shi], k)), rstd2), Elem<T>::unpack(word(whi, k)));
+        float2 lo = kMixed ? mul2(Mixed<T>::mul(word(xv[slo], k), word(wlo, k)), rstd2)
+                           : mul2(mul2(Elem<T>::unpack(word(xv[slo], k)), rstd2), Elem<T>::unpack(word(wlo, k)));
+        float2 hi = kMixed ? mul2(Mixed<T>::mul(word(xv[shi], k), word(whi, k)), rstd2)
+                           : mul2(mul2(Elem<T>::unpack(word(xv[shi], k)), rstd2), Elem<T>::unpack(word(whi, k)));
         if constexpr (kRound) {
           lo = round_trip<T>(lo);
           hi = round_trip<T>(hi);
