@@ -106,6 +106,16 @@ struct Mixed<__nv_bfloat16> {
         : "r"(x), "f"(a.x), "f"(a.y));
     return r;
   }
+  // (a.x + x0, a.y + x1) rounded once each, as an fp32 add of the unpacked values: x * 1 is exact,
+  // and an exact zero sum takes the sign the addition gives it.
+  static __device__ __forceinline__ float2 add(uint32_t x, float2 a) {
+    float2 r;
+    asm("{\n\t.reg .b16 x0, x1, one;\n\tmov.b32 {x0, x1}, %2;\n\tmov.b16 one, 0x3F80;\n\t"
+        "fma.rn.f32.bf16 %0, x0, one, %3;\n\tfma.rn.f32.bf16 %1, x1, one, %4;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "f"(a.x), "f"(a.y));
+    return r;
+  }
 };
 
 template <>
@@ -122,6 +132,14 @@ struct Mixed<__half> {
     float2 r;
     asm("{\n\t.reg .b16 x0, x1;\n\tmov.b32 {x0, x1}, %2;\n\t"
         "fma.rn.f32.f16 %0, x0, x0, %3;\n\tfma.rn.f32.f16 %1, x1, x1, %4;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "r"(x), "f"(a.x), "f"(a.y));
+    return r;
+  }
+  static __device__ __forceinline__ float2 add(uint32_t x, float2 a) {
+    float2 r;
+    asm("{\n\t.reg .b16 x0, x1, one;\n\tmov.b32 {x0, x1}, %2;\n\tmov.b16 one, 0x3C00;\n\t"
+        "fma.rn.f32.f16 %0, x0, one, %3;\n\tfma.rn.f32.f16 %1, x1, one, %4;\n\t}"
         : "=f"(r.x), "=f"(r.y)
         : "r"(x), "f"(a.x), "f"(a.y));
     return r;

@@ -264,6 +264,18 @@ __device__ __forceinline__ float2 sq_acc(uint4 u, float2 acc) {
   return fma2(f3, f3, acc);
 }
 
+// The same sums with the squares taken straight from the 16-bit operands (fma.rn.f32.bf16 / .f16):
+// x^2 of a 16-bit value is exact in fp32 and each step rounds once, as fma2 on the unpacked values
+// does, so the sums are bit-identical without unpacking x (fewer instructions and registers: the
+// register-resident kernels below no longer spill and fit one more consumer group).
+template <typename T>
+__device__ __forceinline__ float2 sq_acc_mixed(uint4 u, float2 acc) {
+  acc = Mixed<T>::sq_add(u.x, acc);
+  acc = Mixed<T>::sq_add(u.y, acc);
+  acc = Mixed<T>::sq_add(u.z, acc);
+  return Mixed<T>::sq_add(u.w, acc);
+}
+
 template <typename T>
 __device__ __forceinline__ uint4 norm8(uint4 u, uint4 wv, float2 rstd2) {
   uint4 out;
@@ -542,16 +554,15 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_rope_kernel(const 
 // 12 slots (13 warps: registers are allotted for 16, so 128 per thread), two for 16 slots, whose 64
 // registers of row data need more room (168 per thread). Rows of 4096 are split over two warps of 8
 // slots each, so they run with four groups: eight rows in flight per SM instead of six took the
-// 4096 x 4096 workloads from 11.79 to 11.34 us (RMSNorm + RoPE + FP8), 12.11 to 11.76 us
-// (LayerNorm) and the 8192 x 4096 RMSNorm forward from 21.48 to 21.28 us. The kernel with group-wise
-// scales keeps three groups at 8 slots: at 96 registers it spills 12 bytes and ran 1% slower.
+// 4096 x 4096 workloads from 11.79 to 11.34 us (RMSNorm + RoPE + FP8) and from 12.11 to 11.76 us
+// (LayerNorm). The kernels that need at most 80 registers at 8 slots -- the RMSNorm forward (72) and
+// LayerNorm with its sums and centring taken straight from the 16-bit operands (80) -- take a fifth
+// group (21 warps): 21.27 -> 21.20 us on the 8192 x 4096 forward, 11.76 -> 11.55 us on the
+// 4096 x 4096 LayerNorm.
 constexpr int kRegRows = 4;
-__host__ __device__ constexpr int reg_groups(int vpt, bool grouped = false) {
-  return vpt <= 8 && !grouped ? 4 : (vpt <= 12 ? 3 : 2);
-}
-__host__ __device__ constexpr int reg_threads(int vpt, bool grouped = false) {
-  return (kRegRows * reg_groups(vpt, grouped) + 1) * 32;
-}
+__host__ __device__ constexpr int reg_groups(int vpt) { return vpt <= 8 ? 4 : (vpt <= 12 ? 3 : 2); }
+__host__ __device__ constexpr int reg_groups_lean(int vpt) { return vpt <= 8 ? 5 : reg_groups(vpt); }
+__host__ __device__ constexpr int reg_threads(int groups) { return (kRegRows * groups + 1) * 32; }
 
 // RN(m / fmax) from rcp = RN(1 / fmax): one product and Markstein's correction (the residual
 // m - s0 * fmax is exact in one FMA). m >= 1e-4 and fmax a normal float keep every step normal.
@@ -637,10 +648,10 @@ __device__ __forceinline__ bool team_all(bool v, int team, int threads) {
 // pair adds its sums of squares and takes the larger |y| maximum through shared memory, and a group
 // never spans the two halves (the host sends groups wider than half a row elsewhere).
 template <typename T, typename TT, int VPT, int GV, int TPR>
-__global__ void __launch_bounds__(reg_threads(VPT / TPR, GV != 0), 1) rows_tma_wide_quant_kernel(const StreamArgs p) {
+__global__ void __launch_bounds__(reg_threads(reg_groups(VPT / TPR)), 1) rows_tma_wide_quant_kernel(const StreamArgs p) {
   constexpr bool GROUPED = GV != 0;
   constexpr int VW = VPT / TPR;                  // slots per warp
-  constexpr int kRegGroups = reg_groups(VW, GROUPED);
+  constexpr int kRegGroups = reg_groups(VW);
   constexpr int kRegWarps = kRegRows * kRegGroups;
   constexpr int SR = kRegRows / TPR;             // rows per stage
   static_assert(TPR == 1 || TPR == 2, "one or two warps per row");
@@ -705,8 +716,8 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR, GV != 0), 1) rows_tma_w
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < VW; k += 2) {
-      acc0 = sq_acc<T>(xv[k], acc0);
-      acc1 = sq_acc<T>(xv[k + 1], acc1);
+      acc0 = sq_acc_mixed<T>(xv[k], acc0);
+      acc1 = sq_acc_mixed<T>(xv[k + 1], acc1);
     }
     const float2 acc = add2(acc0, acc1);
     float ss = group_sum<32>(acc.x + acc.y);
@@ -834,9 +845,9 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR, GV != 0), 1) rows_tma_w
 // columns): the warp copies its part of the row into registers and releases the stage, adds its
 // squares in four chains, and writes y = dtype((x * rstd) * w) from the registers.
 template <typename T, int VPT, int TPR>
-__global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_reg_fwd_kernel(const StreamArgs p) {
+__global__ void __launch_bounds__(reg_threads(reg_groups_lean(VPT / TPR)), 1) rows_tma_reg_fwd_kernel(const StreamArgs p) {
   constexpr int VW = VPT / TPR;
-  constexpr int kRegGroups = reg_groups(VW);
+  constexpr int kRegGroups = reg_groups_lean(VW);
   constexpr int kRegWarps = kRegRows * kRegGroups;
   constexpr int SR = kRegRows / TPR;
   static_assert(TPR == 1 || TPR == 2, "one or two warps per row");
@@ -887,7 +898,7 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_reg_fwd_ke
     if (!live) continue;
     float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
-    for (int k = 0; k < VW; ++k) acc[k & 3] = sq_acc<T>(xv[k], acc[k & 3]);
+    for (int k = 0; k < VW; ++k) acc[k & 3] = sq_acc_mixed<T>(xv[k], acc[k & 3]);
     const float2 sum = add2(add2(acc[0], acc[1]), add2(acc[2], acc[3]));
     float ss = group_sum<32>(sum.x + sum.y);
     if constexpr (TPR > 1) {
@@ -917,9 +928,9 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_reg_fwd_ke
 // y = dtype(((x - mean) * rstd) * g + b) with each step rounded as the definition's fp32 ops. With
 // two warps per row their partial sums meet in shared memory, added in the same order by both.
 template <typename T, int VPT, int TPR>
-__global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_ln_kernel(const StreamArgs p) {
+__global__ void __launch_bounds__(reg_threads(reg_groups_lean(VPT / TPR)), 1) rows_tma_ln_kernel(const StreamArgs p) {
   constexpr int VW = VPT / TPR;
-  constexpr int kRegGroups = reg_groups(VW);
+  constexpr int kRegGroups = reg_groups_lean(VW);
   constexpr int kRegWarps = kRegRows * kRegGroups;
   constexpr int SR = kRegRows / TPR;
   static_assert(TPR == 1 || TPR == 2, "one or two warps per row");
@@ -975,8 +986,8 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_ln_kernel(
     for (int k = 0; k < VW; ++k) {
       float2& sa = (k & 1) ? s1 : s0;
       float2& sb = (k & 1) ? s3 : s2;
-      sa = add2(sa, add2(Elem<T>::unpack(xv[k].x), Elem<T>::unpack(xv[k].y)));
-      sb = add2(sb, add2(Elem<T>::unpack(xv[k].z), Elem<T>::unpack(xv[k].w)));
+      sa = Mixed<T>::add(xv[k].y, Mixed<T>::add(xv[k].x, sa));
+      sb = Mixed<T>::add(xv[k].w, Mixed<T>::add(xv[k].z, sb));
     }
     const float2 st = add2(add2(s0, s1), add2(s2, s3));
     float sum = group_sum<32>(st.x + st.y);
@@ -986,13 +997,13 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_ln_kernel(
       sum = xch[team * TPR][0] + xch[team * TPR + 1][0];
     }
     const float mean = div_n(sum, fN);
-    const float2 mean2 = splat2(mean);
+    const float2 nmean2 = splat2(-mean);  // x - mean as x * 1 + (-mean): one rounding, as the subtraction
     float2 q0 = make_float2(0.f, 0.f), q1 = q0, q2 = q0, q3 = q0;
 #pragma unroll
     for (int k = 0; k < VW; ++k) {
       if (vb + lane + 32 * k >= nv) continue;
-      const float2 c0 = sub2(Elem<T>::unpack(xv[k].x), mean2), c1 = sub2(Elem<T>::unpack(xv[k].y), mean2);
-      const float2 c2 = sub2(Elem<T>::unpack(xv[k].z), mean2), c3 = sub2(Elem<T>::unpack(xv[k].w), mean2);
+      const float2 c0 = Mixed<T>::add(xv[k].x, nmean2), c1 = Mixed<T>::add(xv[k].y, nmean2);
+      const float2 c2 = Mixed<T>::add(xv[k].z, nmean2), c3 = Mixed<T>::add(xv[k].w, nmean2);
       float2& qa = (k & 1) ? q1 : q0;
       float2& qb = (k & 1) ? q3 : q2;
       qa = fma2(c0, c0, fma2(c1, c1, qa));
@@ -1017,9 +1028,9 @@ __global__ void __launch_bounds__(reg_threads(VPT / TPR), 1) rows_tma_ln_kernel(
       uint4 out;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 c = sub2(Elem<T>::unpack(rows::word(xv[k], e)), mean2);
+        const float2 c = Mixed<T>::add(rows::word(xv[k], e), nmean2);
         const float2 n = mul2(mul2(c, rstd2), Elem<T>::unpack(rows::word(gv, e)));
-        rows::set_word(out, e, Elem<T>::pack(add2_rn(n, Elem<T>::unpack(rows::word(bv, e)))));
+        rows::set_word(out, e, Elem<T>::pack(Mixed<T>::add(rows::word(bv, e), n)));  // n + bias, one rounding
       }
       st_stream16(yrow + v, out);
     }
@@ -1121,8 +1132,8 @@ bool launch_layernorm_tma(const RowArgs& a, int dtype, cudaStream_t s) {
   p.w_bytes = xrow;                           // the gain row
   p.b_bytes = a.bias != nullptr ? xrow : 0;   // the bias row, right after it
 #define FQ_LN_K(T, V, TPR)                                                                                 \
-  launch_stream(rows_tma_ln_kernel<T, V, TPR>, reg_threads((V) / (TPR)), p, kRegRows / (TPR), xrow, 0, s,     \
-                p.b_bytes, 220 * 1024, 96 * 1024, reg_groups((V) / (TPR)))
+  launch_stream(rows_tma_ln_kernel<T, V, TPR>, reg_threads(reg_groups_lean((V) / (TPR))), p, kRegRows / (TPR), xrow, \
+                0, s, p.b_bytes, 220 * 1024, 96 * 1024, reg_groups_lean((V) / (TPR)))
 #define FQ_LN(V)                                                                                      \
   return dtype == DT_BF16 ? FQ_LN_K(__nv_bfloat16, V, (V) == 16 ? 2 : 1) : FQ_LN_K(__half, V, (V) == 16 ? 2 : 1)
   const int nv = a.N / 8;
@@ -1160,9 +1171,8 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
     if (quant && !staged && a.N % 256 == 0 && (vpt == 4 || vpt == 8 || vpt == 12 || vpt == 16) && a.R <= 256 &&
         a.R % 16 == 0 && pow2_group) {
 #define FQ_REG_K2(T, TT, V, GV, TPR)                                                                         \
-  return launch_stream(rows_tma_wide_quant_kernel<T, TT, V, GV, TPR>, reg_threads((V) / (TPR), (GV) != 0), p,  \
-                       kRegRows / (TPR), xrow, trow, s, 0, 220 * 1024, 96 * 1024,                         \
-                       reg_groups((V) / (TPR), (GV) != 0));
+  return launch_stream(rows_tma_wide_quant_kernel<T, TT, V, GV, TPR>, reg_threads(reg_groups((V) / (TPR))), p, \
+                       kRegRows / (TPR), xrow, trow, s, 0, 220 * 1024, 96 * 1024, reg_groups((V) / (TPR)));
 // Rows of 4096: two warps per row, so that three or four consumer groups fit the registers. (A power-of-two
 // group narrower than the row is at most half of it, so no group spans the two warps; a group of the
 // whole row takes the per-row kernel, which does not read the group size.)
@@ -1219,8 +1229,8 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
     const char* sel = getenv("FQ_ROWS_KERNEL");
     if (a.N <= 4096 && !(sel != nullptr && std::string(sel) == "staged")) {
 #define FQ_RF_K(T, V, TPR)                                                                                 \
-  launch_stream(rows_tma_reg_fwd_kernel<T, V, TPR>, reg_threads((V) / (TPR)), p, kRegRows / (TPR), xrow, 0, s, \
-                0, 220 * 1024, 96 * 1024, reg_groups((V) / (TPR)))
+  launch_stream(rows_tma_reg_fwd_kernel<T, V, TPR>, reg_threads(reg_groups_lean((V) / (TPR))), p, kRegRows / (TPR), \
+                xrow, 0, s, 0, 220 * 1024, 96 * 1024, reg_groups_lean((V) / (TPR)))
 #define FQ_RF(V)                                                                                                  \
   return dtype == DT_BF16 ? FQ_RF_K(__nv_bfloat16, V, (V) == 16 ? 2 : 1) : FQ_RF_K(__half, V, (V) == 16 ? 2 : 1)
       const int nv = a.N / 8;
