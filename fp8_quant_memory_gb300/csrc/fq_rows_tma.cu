@@ -550,18 +550,16 @@ __global__ void __launch_bounds__(kWideThreads) rows_tma_wide_rope_kernel(const 
 // quotients. The warp's rows and the stage ring are independent, so the copy of the next stages
 // overlaps this work.
 // Warps per consumer group (a stage holds kRegRows / TPR rows). Consumer groups take the stages in
-// turn: four when a warp holds up to 8 vector slots (17 warps, 96 registers per thread), three for
+// turn: five when a warp holds up to 8 vector slots (21 warps, 80 registers per thread), three for
 // 12 slots (13 warps: registers are allotted for 16, so 128 per thread), two for 16 slots, whose 64
 // registers of row data need more room (168 per thread). Rows of 4096 are split over two warps of 8
-// slots each, so they run with four groups: eight rows in flight per SM instead of six took the
-// 4096 x 4096 workloads from 11.79 to 11.34 us (RMSNorm + RoPE + FP8) and from 12.11 to 11.76 us
-// (LayerNorm). The kernels that need at most 80 registers at 8 slots -- the RMSNorm forward (72) and
-// LayerNorm with its sums and centring taken straight from the 16-bit operands (80) -- take a fifth
-// group (21 warps): 21.27 -> 21.20 us on the 8192 x 4096 forward, 11.76 -> 11.55 us on the
-// 4096 x 4096 LayerNorm.
+// slots each, so they run with five groups: ten rows in flight per SM. The kernels are latency-bound,
+// so rows in flight count most; measured on the 4096 x 4096 workloads (RMSNorm + RoPE + FP8,
+// LayerNorm) and the 8192 x 4096 RMSNorm forward, in us: three groups 11.79, 12.11, 21.48; four
+// 10.82 (after the mixed-precision squares, which removed a spill), 11.76, 21.28; five 10.66, 11.55,
+// 21.19; six (72 registers) 10.76, 11.54, 21.19.
 constexpr int kRegRows = 4;
-__host__ __device__ constexpr int reg_groups(int vpt) { return vpt <= 8 ? 4 : (vpt <= 12 ? 3 : 2); }
-__host__ __device__ constexpr int reg_groups_lean(int vpt) { return vpt <= 8 ? 5 : reg_groups(vpt); }
+__host__ __device__ constexpr int reg_groups(int vpt) { return vpt <= 8 ? 5 : (vpt <= 12 ? 3 : 2); }
 __host__ __device__ constexpr int reg_threads(int groups) { return (kRegRows * groups + 1) * 32; }
 
 // RN(m / fmax) from rcp = RN(1 / fmax): one product and Markstein's correction (the residual
@@ -845,9 +843,9 @@ __global__ void __launch_bounds__(reg_threads(reg_groups(VPT / TPR)), 1) rows_tm
 // columns): the warp copies its part of the row into registers and releases the stage, adds its
 // squares in four chains, and writes y = dtype((x * rstd) * w) from the registers.
 template <typename T, int VPT, int TPR>
-__global__ void __launch_bounds__(reg_threads(reg_groups_lean(VPT / TPR)), 1) rows_tma_reg_fwd_kernel(const StreamArgs p) {
+__global__ void __launch_bounds__(reg_threads(reg_groups(VPT / TPR)), 1) rows_tma_reg_fwd_kernel(const StreamArgs p) {
   constexpr int VW = VPT / TPR;
-  constexpr int kRegGroups = reg_groups_lean(VW);
+  constexpr int kRegGroups = reg_groups(VW);
   constexpr int kRegWarps = kRegRows * kRegGroups;
   constexpr int SR = kRegRows / TPR;
   static_assert(TPR == 1 || TPR == 2, "one or two warps per row");
@@ -928,9 +926,9 @@ __global__ void __launch_bounds__(reg_threads(reg_groups_lean(VPT / TPR)), 1) ro
 // y = dtype(((x - mean) * rstd) * g + b) with each step rounded as the definition's fp32 ops. With
 // two warps per row their partial sums meet in shared memory, added in the same order by both.
 template <typename T, int VPT, int TPR>
-__global__ void __launch_bounds__(reg_threads(reg_groups_lean(VPT / TPR)), 1) rows_tma_ln_kernel(const StreamArgs p) {
+__global__ void __launch_bounds__(reg_threads(reg_groups(VPT / TPR)), 1) rows_tma_ln_kernel(const StreamArgs p) {
   constexpr int VW = VPT / TPR;
-  constexpr int kRegGroups = reg_groups_lean(VW);
+  constexpr int kRegGroups = reg_groups(VW);
   constexpr int kRegWarps = kRegRows * kRegGroups;
   constexpr int SR = kRegRows / TPR;
   static_assert(TPR == 1 || TPR == 2, "one or two warps per row");
@@ -1132,8 +1130,8 @@ bool launch_layernorm_tma(const RowArgs& a, int dtype, cudaStream_t s) {
   p.w_bytes = xrow;                           // the gain row
   p.b_bytes = a.bias != nullptr ? xrow : 0;   // the bias row, right after it
 #define FQ_LN_K(T, V, TPR)                                                                                 \
-  launch_stream(rows_tma_ln_kernel<T, V, TPR>, reg_threads(reg_groups_lean((V) / (TPR))), p, kRegRows / (TPR), xrow, \
-                0, s, p.b_bytes, 220 * 1024, 96 * 1024, reg_groups_lean((V) / (TPR)))
+  launch_stream(rows_tma_ln_kernel<T, V, TPR>, reg_threads(reg_groups((V) / (TPR))), p, kRegRows / (TPR), xrow, \
+                0, s, p.b_bytes, 220 * 1024, 96 * 1024, reg_groups((V) / (TPR)))
 #define FQ_LN(V)                                                                                      \
   return dtype == DT_BF16 ? FQ_LN_K(__nv_bfloat16, V, (V) == 16 ? 2 : 1) : FQ_LN_K(__half, V, (V) == 16 ? 2 : 1)
   const int nv = a.N / 8;
@@ -1229,8 +1227,8 @@ bool launch_rows_tma(const RowArgs& a, int mode, int dtype, int table_dtype, cud
     const char* sel = getenv("FQ_ROWS_KERNEL");
     if (a.N <= 4096 && !(sel != nullptr && std::string(sel) == "staged")) {
 #define FQ_RF_K(T, V, TPR)                                                                                 \
-  launch_stream(rows_tma_reg_fwd_kernel<T, V, TPR>, reg_threads(reg_groups_lean((V) / (TPR))), p, kRegRows / (TPR), \
-                xrow, 0, s, 0, 220 * 1024, 96 * 1024, reg_groups_lean((V) / (TPR)))
+  launch_stream(rows_tma_reg_fwd_kernel<T, V, TPR>, reg_threads(reg_groups((V) / (TPR))), p, kRegRows / (TPR), \
+                xrow, 0, s, 0, 220 * 1024, 96 * 1024, reg_groups((V) / (TPR)))
 #define FQ_RF(V)                                                                                                  \
   return dtype == DT_BF16 ? FQ_RF_K(__nv_bfloat16, V, (V) == 16 ? 2 : 1) : FQ_RF_K(__half, V, (V) == 16 ? 2 : 1)
       const int nv = a.N / 8;
