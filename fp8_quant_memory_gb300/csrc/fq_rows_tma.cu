@@ -603,6 +603,15 @@ __device__ __forceinline__ uint4 norm8_max(uint4 u, uint4 wv, float2 rstd2, floa
   return make_uint4(Elem<T>::pack(v0), Elem<T>::pack(v1), Elem<T>::pack(v2), Elem<T>::pack(v3));
 }
 
+// Maximum of v over the warp in one instruction (redux.sync on f32, sm_100-class SMs) instead of five
+// shuffle-and-max levels. A maximum selects one of its inputs, so the result equals the shuffle
+// tree's for the non-negative, non-NaN |y| maxima it is used on.
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
 // The storage dtype's rounding of one fp32 value, as fp32.
 template <typename T>
 __device__ __forceinline__ float round_to(float m) {
@@ -766,7 +775,7 @@ __global__ void __launch_bounds__(reg_threads(reg_groups(VPT / TPR)), 1) rows_tm
     }
     uint2* qrow = reinterpret_cast<uint2*>(a.q + static_cast<int64_t>(r) * N) + vb;
     if constexpr (!GROUPED) {
-      float m = group_max<32>(mk[0]);
+      float m = warp_max(mk[0]);
       if constexpr (TPR > 1) {
         if (lane == 0) xch[warp][1] = m;
         team_sync(team, 32 * TPR);
