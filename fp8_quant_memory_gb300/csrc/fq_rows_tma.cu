@@ -13,14 +13,16 @@
 // what the register-hungry, latency-bound global-load kernels lacked. The consumer warps read x from
 // the stage:
 //   - narrow rows: eight consumer warps with the lane-group layout and arithmetic of the generic row
-//     kernel (fq_rows.cuh), one row per lane group per stage, tables read from the stage;
+//     kernel (fq_rows.cuh), one row per lane group per stage, tables read from the stage; the warps
+//     work as one group or as several groups that take the stages in turn (finer work units);
 //   - wide rows, shared memory (RMSNorm forward beyond 4096 columns, RMSNorm + RoPE, the quantising
 //     shapes the register kernels do not take): four consumer warps, one row per warp per stage,
 //     two or three passes over the staged row; the weight row is copied into shared memory once per
 //     CTA. Two CTAs share an SM, so a stage is four rows and the ring fills and drains in small steps;
 //   - wide rows, registers (RMSNorm forward, RMSNorm + RoPE + FP8 and LayerNorm on rows of 1024 to
-//     4096): one CTA per SM, two to four consumer groups of four warps taking the stages in turn, one or
-//     two warps per row; a warp copies its row into registers and releases the stage at once.
+//     4096): one CTA per SM, two, three or five consumer groups of four warps taking the stages in
+//     turn, one or two warps per row; a warp copies its row into registers and releases the stage
+//     at once.
 // y is written with 16-byte evict-first stores. x and the tables are read from HBM exactly once.
 #include <cstdlib>
 #include <string>
