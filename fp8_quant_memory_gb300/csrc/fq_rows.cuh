@@ -100,27 +100,19 @@ __device__ __forceinline__ void row_body(const RowArgs& a, int32_t r, bool rv, i
   constexpr int kV = HS + 2 * TS;  // vector slots per lane: head..., tail-lo..., tail-hi...
   const int N = a.N;
 
-  // a2: sum of squares -> rstd. RMSNorm + RoPE without quantisation (MODE_ROPE) takes the squares
-  // straight from the 16-bit storage operands (one FMA each, exact products) and normalises as
-  // (x * w) * rstd with x * w exact: the same values as (x * rstd) * w up to one fp32 rounding,
-  // the size of the approximate rstd this mode already uses, and no unpacking of x or w.
+  // a2: sum of squares -> rstd, the squares taken straight from the 16-bit storage operands (x*x of a
+  // 16-bit value is exact in fp32 and each FMA rounds once, as an FMA on the unpacked values does:
+  // the same sums without unpacking x). RMSNorm + RoPE without quantisation (MODE_ROPE) also
+  // normalises as (x * w) * rstd with x * w exact: the same values as (x * rstd) * w up to one fp32
+  // rounding, the size of the approximate rstd this mode already uses, and no unpacking of x or w.
   constexpr bool kMixed = MODE == MODE_ROPE;
   float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
   for (int s = 0; s < kV; ++s) {
-    if constexpr (kMixed) {
-      acc0 = Mixed<T>::sq_add(xv[s].x, acc0);
-      acc1 = Mixed<T>::sq_add(xv[s].y, acc1);
-      acc0 = Mixed<T>::sq_add(xv[s].z, acc0);
-      acc1 = Mixed<T>::sq_add(xv[s].w, acc1);
-    } else {
-      const float2 f0 = Elem<T>::unpack(xv[s].x), f1 = Elem<T>::unpack(xv[s].y);
-      const float2 f2 = Elem<T>::unpack(xv[s].z), f3 = Elem<T>::unpack(xv[s].w);
-      acc0 = fma2(f0, f0, acc0);
-      acc1 = fma2(f1, f1, acc1);
-      acc0 = fma2(f2, f2, acc0);
-      acc1 = fma2(f3, f3, acc1);
-    }
+    acc0 = Mixed<T>::sq_add(xv[s].x, acc0);
+    acc1 = Mixed<T>::sq_add(xv[s].y, acc1);
+    acc0 = Mixed<T>::sq_add(xv[s].z, acc0);
+    acc1 = Mixed<T>::sq_add(xv[s].w, acc1);
   }
   const float2 acc = add2(acc0, acc1);
   const float ss = group_sum<LPR>(acc.x + acc.y);
