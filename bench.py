@@ -764,6 +764,8 @@ SECONDARY = {
                                                       note=" (Ch.13 ledger fused workload)"),
     "rope_quant_groups_ledger_4k": lambda dev: RopeQuantCase(dev, M=4096, N=4096, R=128, group_size=128,
                                                              write_y=False, n_sets=8),
+    "rope_quant_16k": lambda dev: RopeQuantCase(dev, M=16384, N=4096, R=128, write_y=False, n_sets=4,
+                                                note=" (the ledger workload at four times the rows)"),
     "prologue_4k_design_a": lambda dev: PrologueDesignCase(dev, 1, "A"),
     "prologue_4k_design_b": lambda dev: PrologueDesignCase(dev, 8, "B"),
     "prologue_4k_design_c": lambda dev: PrologueDesignCase(dev, HQ + HK, "C"),
