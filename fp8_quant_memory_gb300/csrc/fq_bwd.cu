@@ -417,7 +417,12 @@ __global__ void __launch_bounds__(kStreamThreads, 2) bwd_stage1_stream_kernel(co
   const float fN = static_cast<float>(N);
   int slot = 0;
   uint32_t phase = 0;
+  // The saved rstd of row k is loaded one row ahead, so its global-load latency overlaps the
+  // previous row's work instead of sitting between the row sums and the dx pass.
+  float rstd_next = (SAVED && n > 0) ? a.rstd_in[c0] : 0.f;
   for (int k = 0; k < n; ++k) {
+    const float rstd_saved = rstd_next;
+    if (SAVED && k + 1 < n) rstd_next = a.rstd_in[c0 + k + 1];
     const bool got = mbar_wait(kWaitLimitNs, &full[slot], phase);
     if (!got) flag_failure(p.status);
     const unsigned char* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
@@ -459,7 +464,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) bwd_stage1_stream_kernel(co
       ss += v.z;
       sg += v.w;
     }
-    const float rstd = SAVED ? a.rstd_in[c0 + k] : rstd_approx(ss, fN, a.eps);
+    const float rstd = SAVED ? rstd_saved : rstd_approx(ss, fN, a.eps);
     const float c = div_n(__fmul_rn(sg, rstd), fN);
     const float2 rstd2 = splat2(rstd), c2 = splat2(c);
     T* dxrow = static_cast<T*>(a.dx) + (c0 + k) * N;
