@@ -57,9 +57,13 @@ def first_false_pass(S, G, depth, runs=400, n_stages=60):
     return next((seed for seed in range(runs) if false_pass(S, G, depth, n_stages, seed)), None)
 
 
-@pytest.mark.parametrize("S,G,depth", [(12, 3, 6), (6, 3, 6), (9, 3, 6), (11, 2, 4), (5, 2, 2), (8, 1, 8), (4, 2, 4)])
+@pytest.mark.parametrize("S,G,depth", [(12, 3, 6), (6, 3, 6), (9, 3, 6), (11, 2, 4), (5, 2, 2), (8, 1, 8), (4, 2, 4),
+                                         (10, 5, 10), (10, 5, 6), (12, 4, 6), (12, 2, 12), (6, 1, 4)])
 def test_ring_rules_never_pass_early(S, G, depth):
-    """Every configuration the launchers allow: S % G == 0 or depth <= S - G."""
+    """Every configuration the launchers allow: S % G == 0 or depth <= S - G. Among them the rings the
+    kernels run: ten stages for five groups with all or six in flight (register-resident rows),
+    twelve stages for four groups (narrow fp16 rows), twelve for the prologue's two halves with all
+    in flight, six for one group (backward)."""
     assert S % G == 0 or depth <= S - G
     assert first_false_pass(S, G, depth) is None
 
