@@ -44,6 +44,8 @@ PROLOGUE_CASES = [
     (11, 2, 2, 100, 50, "bf16", "bf16", 1.0, 0, 448.0),          # odd-ish width: scalar path
     (9, 2, 1, 128, 0, "bf16", "fp32", 1.0, 0, 448.0),            # no rotation
     (7, 40, 8, 128, 128, "bf16", "fp16", 1.0, 0, 448.0),         # table dtype != storage dtype
+    (29, 16, 8, 128, 128, "bf16", "fp32", 1.0, 0, 240.0),        # head counts multiples of 8, fp8_max < 448
+    (31, 8, 8, 128, 128, "fp16", "fp16", 1.0, 0, 448.0),         # head counts multiples of 8, fp16 tables
 ]
 
 
